@@ -1,0 +1,182 @@
+/*
+ * mla.h — C ABI of libmla: Multi-head Latent Attention (MLA) decode with
+ * matrix absorption over a paged latent KV cache, for one NVIDIA GB300
+ * (sm_103a).
+ *
+ * Method (cited by page and section):
+ *   - MLA operator write-up (nxmr.cn/news/151634) §1: every cached token of a
+ *     layer holds a 512-d latent c_KV plus a 64-d decoupled RoPE key k_R,
+ *     576 elements, 1.125 KB in bf16.
+ *   - same page §4 (the absorption-equivalence script): K = c_KV·W_UK^T per
+ *     head ("path A") equals absorbing W_UK into the query,
+ *     q_abs = q_nope·W_UK ("path B"); score = (q_abs·c_KV + q_R·k_R) · scale
+ *     with scale = (d_hc + d_R)^-1/2 = 1/sqrt(192).
+ *   - same page §3: page_size 64 (a 64-token page is 73,728 B and suits bulk
+ *     tensor copies), tile of 64 tokens, multi-stage pipeline.
+ *   - "From MLA to GLA" (hotelren.com/news/5324130) §1: grouped latent
+ *     attention (GLA), heads split into groups that each own a latent.
+ *
+ * One decode step of one layer is four calls on one stream:
+ *   mla_absorb_q  →  mla_decode_paged  →  mla_combine_splits  →  mla_project_uv
+ *
+ * Conventions shared by every entry point
+ *   - All tensor arguments are DEVICE pointers owned by the caller. The
+ *     library never allocates device memory, keeps no global state and never
+ *     synchronises the stream except in mla_get_device_status.
+ *   - bf16 tensors are passed as raw 16-bit storage (void*); fp32 as float*;
+ *     indices as int32.  All tensors are dense, row-major, no padding.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL
+ *     is the legacy default stream).  The int return value reports argument
+ *     validation and launch errors only (mla_status).  Errors found on the
+ *     device (bad block_table entry, bad sequence length, a bounded wait that
+ *     gave up) are written to a sticky status word inside the decode
+ *     workspace; read it with mla_get_device_status.
+ *   - Nothing is thrown across the ABI.  Every call is thread-safe as long as
+ *     concurrent calls do not share output buffers or workspaces.
+ *
+ * Notation (dims struct):
+ *   B batch, Lq new tokens per sequence, H heads, d_hc = 128 content head dim,
+ *   d_c = 512 latent width, d_R = 64 RoPE width, G latent groups (1 = MLA,
+ *   2 = GLA), d_g = d_c / G latent width per group, P = page_size = 64.
+ *   Head h belongs to group g(h) = floor(h * G / H) (contiguous head blocks).
+ *   Cache row of one token = [c_0 | ... | c_{G-1} | k_R], d_c + d_R = 576 bf16.
+ */
+#ifndef MLA_H_
+#define MLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct mla_dims {
+  int B;                 /* batch (sequences), >= 1                          */
+  int Lq;                /* new query tokens per sequence, 1..2              */
+  int H;                 /* heads, multiple of 16, 16..128                   */
+  int d_hc;              /* content head dim, must be 128                    */
+  int d_c;               /* total latent width, must be 512                  */
+  int d_R;               /* decoupled RoPE width, must be 64                 */
+  int G;                 /* latent groups: 1 (MLA) or 2 (GLA)                */
+  int page_size;         /* tokens per cache page, must be 64                */
+  int max_pages_per_seq; /* row length of block_table                        */
+  int num_pages;         /* physical pages in the cache                      */
+  float scale;           /* softmax scale, normally 1/sqrt(d_hc + d_R)       */
+  int causal;            /* 1: query l sees keys 0 .. n-Lq+l (required if Lq>1) */
+} mla_dims;
+
+typedef enum mla_status {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = -1,  /* null pointer, non-positive size, bad scale  */
+  MLA_ERR_UNSUPPORTED = -2,  /* dims outside the supported set above       */
+  MLA_ERR_MISALIGNED = -3,   /* a pointer is not 16-byte aligned           */
+  MLA_ERR_WORKSPACE = -4,    /* workspace missing or too small             */
+  MLA_ERR_CUDA = -5,         /* a CUDA runtime / driver call failed        */
+  MLA_ERR_BAD_TABLE = -6,    /* device: block_table entry out of range     */
+  MLA_ERR_BAD_SEQLEN = -8,   /* device: seq_len < Lq or > max_pages*P      */
+  MLA_ERR_TIMEOUT = -7       /* device: a bounded pipeline wait gave up    */
+} mla_status;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* mla_status_string(int status);
+
+/*
+ * mla_absorb_q — absorb W_UK into the query (MLA operator write-up §4,
+ * "path B": einsum qhd,hdc->qhc) and append the RoPE part.
+ *
+ *   q_cat[b,l,h, 0:d_g]        = bf16( sum_d q_nope[b,l,h,d] * W_UK[h,d,:] )
+ *   q_cat[b,l,h, d_g:d_g+d_R]  = q_rope[b,l,h,:]
+ *
+ * q_nope bf16 [B,Lq,H,d_hc]; q_rope bf16 [B,Lq,H,d_R];
+ * W_UK bf16 [H,d_hc,d_g] (head h's block maps the 128-d content query to its
+ * group's d_g-wide latent); q_cat bf16 [B,Lq,H,d_g+d_R] (output).
+ * fp32 accumulation on the tensor cores, one rounding to bf16.
+ * Errors: MLA_ERR_INVALID_ARG (null), MLA_ERR_UNSUPPORTED (dims),
+ * MLA_ERR_MISALIGNED (any pointer not 16-byte aligned), MLA_ERR_CUDA.
+ */
+int mla_absorb_q(const mla_dims* dims, const void* q_nope, const void* q_rope,
+                 const void* W_UK, void* q_cat, void* stream);
+
+/*
+ * Number of partial-output slots mla_decode_paged writes for these dims on
+ * the current device (depends on the device's SM count).  o_part must hold
+ * slots * Lq*H * d_c floats and lse_part slots * Lq*H floats.
+ */
+int mla_decode_num_slots(const mla_dims* dims, int* slots);
+
+/*
+ * Bytes of workspace mla_decode_paged needs (split plan + sticky status
+ * word).  The caller allocates it, zero-fills it ONCE (that clears the status
+ * word) and may reuse it for any number of calls with the same or smaller
+ * dims.
+ */
+int mla_decode_workspace_size(const mla_dims* dims, size_t* bytes);
+
+/*
+ * mla_decode_paged — split-KV flash-decoding over the paged latent cache.
+ *
+ * For each sequence b (n = seq_lens[b] cached tokens, the last Lq of them
+ * being the new tokens) and query row (l, h) with visible keys
+ * s = 0 .. n-Lq+l:
+ *     score_s = (q_cat[b,l,h,0:d_g] . c_{g(h)}[s] + q_cat[b,l,h,d_g:] . k_R[s]) * scale
+ * over the cache rows gathered through block_table (token s of sequence b is
+ * row s % P of physical page block_table[b, s / P]).  The work is split into
+ * contiguous page ranges; each range produces, per query row, the normalised
+ * latent partial o = sum_s p_s c_{g(h)}[s] / sum_s p_s and its natural-log
+ * log-sum-exp lse = log sum_s exp(score_s) (-inf for an empty range).
+ *
+ * q_cat    bf16 [B,Lq,H,d_g+d_R] (from mla_absorb_q), 16-byte aligned
+ * kv_cache bf16 [num_pages, P, d_c+d_R], 16-byte aligned
+ * block_table int32 [B, max_pages_per_seq]; entries past ceil(n/P) unused
+ * seq_lens int32 [B]
+ * o_part  fp32 [slots, Lq*H, d_c]   (scratch for mla_combine_splits)
+ * lse_part fp32 [slots, Lq*H]
+ * workspace / ws_bytes: see mla_decode_workspace_size.
+ * num_splits: 0 = automatic (all SMs busy); otherwise the number of
+ *   concurrent work units (CTA clusters) to use, clamped to the device.
+ * Errors: synchronous MLA_ERR_INVALID_ARG / UNSUPPORTED / MISALIGNED /
+ * WORKSPACE / CUDA; asynchronous MLA_ERR_BAD_TABLE, MLA_ERR_BAD_SEQLEN,
+ * MLA_ERR_TIMEOUT into the workspace status word.  Out-of-range table
+ * entries are never dereferenced (clamped, and the status is set).
+ */
+int mla_decode_paged(const mla_dims* dims, const void* q_cat,
+                     const void* kv_cache, const int32_t* block_table,
+                     const int32_t* seq_lens, int num_splits, float* o_part,
+                     float* lse_part, void* workspace, size_t ws_bytes,
+                     void* stream);
+
+/*
+ * mla_combine_splits — merge the split partials of mla_decode_paged by
+ * log-sum-exp (flash-decoding reduction):
+ *     L = log sum_k exp(lse_k),   o_lat = sum_k exp(lse_k - L) * o_k
+ * Ranges with lse = -inf contribute nothing.
+ * o_part / lse_part / workspace: exactly as passed to mla_decode_paged (the
+ * workspace carries the split plan).  o_lat bf16 [B,Lq,H,d_g] (each head's
+ * own group slice of the latent); lse fp32 [B,Lq,H] (may be NULL).
+ */
+int mla_combine_splits(const mla_dims* dims, const float* o_part,
+                       const float* lse_part, const void* workspace,
+                       size_t ws_bytes, void* o_lat, float* lse, void* stream);
+
+/*
+ * mla_project_uv — map the latent output back to the head dimension with
+ * W_UV (the up-projection of the values, applied after attention):
+ *     out[b,l,h,:] = W_UV[h] (d_hc x d_g) . o_lat[b,l,h,:]
+ * o_lat bf16 [B,Lq,H,d_g]; W_UV bf16 [H,d_hc,d_g]; out bf16 [B,Lq,H,d_hc].
+ * fp32 accumulation on the tensor cores.
+ */
+int mla_project_uv(const mla_dims* dims, const void* o_lat, const void* W_UV,
+                   void* out, void* stream);
+
+/*
+ * Synchronise `stream`, then return the sticky device status of `workspace`
+ * (MLA_OK or the first device error recorded since the workspace was zeroed).
+ */
+int mla_get_device_status(const void* workspace, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_H_ */

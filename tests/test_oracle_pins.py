@@ -1,0 +1,280 @@
+"""Pins of the fp64 oracle to facts fixed by the pages and by mathematics.
+
+Each test is chosen so that a plausible slip in the oracle (a dropped term, a
+wrong scale, a transposed projection, a wrong page lookup, an off-by-one in
+the causal window, a wrong head-to-group map) fails at least one of them:
+
+  absorption identity     (MLA operator write-up §4: naive == absorbed scores)
+  closed forms            (one key; two keys with hand-set scores; zero query)
+  invariants              (page permutation, causal prefix, group isolation)
+  log-sum-exp merge       (splitting the keys and merging == no split)
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mla_latent_kv_10_gb300.inputs import D_C, D_HC, D_R, PAGE, make_case, workload
+
+
+def bf(t):
+    return t.to(torch.float64).numpy()
+
+
+# ---------------------------------------------------------------- absorption
+
+@pytest.mark.parametrize("G", [1, 2])
+def test_absorbed_scores_equal_naive_scores(G):
+    """§4 equivalence script: decompressing K = c.W_UK^T and absorbing W_UK
+    into the query give the same scores; in fp64 they agree to 1e-10."""
+    c = make_case(B=2, Lq=2, H=16, G=G, seq_lens=[37, 200], table="perm", seed=11)
+    for (b, l, h) in [(0, 0, 0), (1, 1, 5), (1, 0, 15), (0, 1, 8)]:
+        sa, sb = oracle.scores_both(c.dims, c.q_nope, c.q_rope, c.W_UK, c.cache,
+                                    c.block_table, c.seq_lens, b, l, h)
+        assert sa.shape == (int(c.seq_lens[b]),)
+        assert np.max(np.abs(sa - sb)) <= 1e-10
+        assert np.max(np.abs(sa)) > 0.1  # non-trivial scores
+
+
+def test_absorption_at_the_scripts_dims():
+    """The §4 script's own dims: 128 heads, d_hc 128, d_c 512, d_R 64, S 2048."""
+    c = make_case(B=1, Lq=1, H=128, G=1, seq_lens=[2048], table="contig", seed=42)
+    for h in (0, 77, 127):
+        sa, sb = oracle.scores_both(c.dims, c.q_nope, c.q_rope, c.W_UK, c.cache,
+                                    c.block_table, c.seq_lens, 0, 0, h)
+        assert np.max(np.abs(sa - sb)) <= 1e-10
+
+
+# ---------------------------------------------------------------- closed forms
+
+def _zero_case(B, H, seq_lens, G=1, Lq=1, table="contig", seed=1):
+    c = make_case(B=B, Lq=Lq, H=H, G=G, seq_lens=seq_lens, table=table, seed=seed)
+    return c
+
+
+def test_single_key_returns_projected_latent():
+    """One visible key: its softmax weight is exactly 1, so out = W_UV[h].c_0
+    and o_lat = c_0 whatever the query."""
+    c = make_case(B=3, Lq=1, H=16, seq_lens=[1, 1, 1], table="perm", seed=5)
+    out, o_lat, lse = oracle.decode(c.dims, **c.tensors())
+    for b in range(3):
+        page = int(c.block_table[b, 0])
+        c0 = bf(c.cache[page, 0, :D_C])
+        for h in range(16):
+            np.testing.assert_allclose(o_lat[b, 0, h], c0, rtol=0, atol=1e-12)
+            np.testing.assert_allclose(out[b, 0, h], bf(c.W_UV[h]) @ c0, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("lens", [[37, 200], [64, 65], [1, 128]])
+def test_zero_query_gives_mean_over_exactly_n_keys(lens):
+    """q = 0: every score is 0, weights are uniform over the n visible keys,
+    out = W_UV[h].mean(c), lse = log n.  Pins the masking of the partial
+    last page (the mean is over exactly n rows, not whole pages)."""
+    c = make_case(B=2, Lq=1, H=16, seq_lens=lens, table="perm", seed=9, q_zero=True)
+    out, o_lat, lse = oracle.decode(c.dims, **c.tensors())
+    for b, n in enumerate(lens):
+        rows = np.stack([bf(c.cache[int(c.block_table[b, s // PAGE]), s % PAGE, :D_C]) for s in range(n)])
+        mean = rows.mean(axis=0)
+        for h in (0, 7, 15):
+            np.testing.assert_allclose(o_lat[b, 0, h], mean, atol=1e-12)
+            np.testing.assert_allclose(out[b, 0, h], bf(c.W_UV[h]) @ mean, atol=1e-11)
+            assert lse[b, 0, h] == pytest.approx(math.log(n), abs=1e-12)
+
+
+def test_zero_query_causal_window_sizes():
+    """Lq=2, q=0: query l sees n - 2 + l + 1 keys, so lse = log(n - 1 + l)."""
+    c = make_case(B=2, Lq=2, H=16, seq_lens=[65, 3], table="perm", seed=4, q_zero=True)
+    _, _, lse = oracle.decode(c.dims, **c.tensors())
+    for b, n in enumerate([65, 3]):
+        for l in range(2):
+            assert lse[b, l, 3] == pytest.approx(math.log(n - 1 + l), abs=1e-12)
+
+
+def _structured_two_key_case(G=1, head=0):
+    """Two keys, hand-set so the scores are known in closed form."""
+    c = make_case(B=1, Lq=1, H=16, G=G, seq_lens=[2], table="contig", seed=3)
+    for t in (c.q_nope, c.q_rope, c.cache, c.W_UK, c.W_UV):
+        t.zero_()
+    return c
+
+
+@pytest.mark.parametrize("G,head", [(1, 0), (1, 9), (2, 3), (2, 12)])
+def test_two_keys_content_score_closed_form(G, head):
+    """q_nope = x e_0, W_UK[h][0][5] = w, key 0 latent = a e_5 (in the head's
+    group slice), key 1 latent = 0, RoPE parts 0, W_UV[h][3][5] = v.
+    The §4 einsum sc,hdc->shd gives K_0[0] = a w, so score_0 = x a w / sqrt(192),
+    score_1 = 0, p_0 = sigmoid(score_0) and out[3] = v a p_0, other entries 0.
+    Pins the scale, the orientation of W_UK and W_UV, the group slice and the
+    softmax together."""
+    x, w, a, v = 2.0, 0.5, 4.0, 0.25
+    c = _structured_two_key_case(G, head)
+    d_g = D_C // G
+    g = head * G // 16
+    c.q_nope[0, 0, head, 0] = x
+    c.W_UK[head, 0, 5] = w
+    c.W_UV[head, 3, 5] = v
+    page = int(c.block_table[0, 0])
+    c.cache[page, 0, g * d_g + 5] = a
+    out, o_lat, lse = oracle.decode(c.dims, **c.tensors())
+    s0 = x * a * w / math.sqrt(D_HC + D_R)
+    p0 = 1.0 / (1.0 + math.exp(-s0))
+    expect = np.zeros(D_HC)
+    expect[3] = v * a * p0
+    np.testing.assert_allclose(out[0, 0, head], expect, atol=1e-13)
+    assert lse[0, 0, head] == pytest.approx(math.log(math.exp(s0) + 1.0), abs=1e-13)
+    expect_lat = np.zeros(d_g)
+    expect_lat[5] = a * p0
+    np.testing.assert_allclose(o_lat[0, 0, head], expect_lat, atol=1e-13)
+    other = (head + 1) % 16
+    np.testing.assert_allclose(out[0, 0, other], 0.0, atol=1e-15)
+
+
+def test_two_keys_rope_score_closed_form():
+    """q_rope = y e_7, key 0's k_R = z e_7 (cache columns d_c..d_c+63), all
+    content parts 0: score_0 = y z / sqrt(192), score_1 = 0."""
+    y, z = 3.0, 1.5
+    c = _structured_two_key_case()
+    head = 4
+    c.q_rope[0, 0, head, 7] = y
+    page = int(c.block_table[0, 0])
+    c.cache[page, 0, D_C + 7] = z
+    c.cache[page, 0, 11] = 1.0      # latent of key 0, to read p_0 back
+    _, o_lat, lse = oracle.decode(c.dims, **c.tensors())
+    s0 = y * z / math.sqrt(D_HC + D_R)
+    p0 = 1.0 / (1.0 + math.exp(-s0))
+    assert o_lat[0, 0, head, 11] == pytest.approx(p0, abs=1e-14)
+    assert lse[0, 0, head] == pytest.approx(math.log(math.exp(s0) + 1.0), abs=1e-13)
+
+
+# ---------------------------------------------------------------- invariants
+
+def test_page_permutation_invariance():
+    """Moving physical pages and rewriting block_table leaves every output
+    unchanged (paging is only an address map)."""
+    c = make_case(B=2, Lq=2, H=16, seq_lens=[130, 64], table="contig", seed=21)
+    ref = oracle.decode(c.dims, **c.tensors())
+    rng = np.random.default_rng(0)
+    perm = rng.permutation(c.dims["num_pages"])          # new slot of old page i
+    cache2 = torch.empty_like(c.cache)
+    cache2[torch.from_numpy(perm)] = c.cache
+    bt2 = c.block_table.clone()
+    m = bt2 >= 0
+    bt2[m] = torch.from_numpy(perm.astype(np.int32))[bt2[m].long()]
+    t = c.tensors()
+    t.update(cache=cache2, block_table=bt2)
+    got = oracle.decode(c.dims, **t)
+    for r, g in zip(ref, got):
+        np.testing.assert_array_equal(r, g)
+
+
+def test_causal_prefix_equals_shorter_decode():
+    """Query 0 of an Lq=2 call on n keys equals an Lq=1 call on the first n-1
+    keys with the same query row (it cannot see the newest token)."""
+    c = make_case(B=3, Lq=2, H=16, seq_lens=[66, 129, 2], table="perm", seed=8)
+    out2, lat2, lse2 = oracle.decode(c.dims, **c.tensors())
+    t = c.tensors()
+    t.update(q_nope=c.q_nope[:, :1].contiguous(), q_rope=c.q_rope[:, :1].contiguous(),
+             seq_lens=c.seq_lens - 1)
+    d1 = dict(c.dims, Lq=1)
+    out1, lat1, lse1 = oracle.decode(d1, **t)
+    np.testing.assert_array_equal(out2[:, 0], out1[:, 0])
+    np.testing.assert_array_equal(lat2[:, 0], lat1[:, 0])
+    np.testing.assert_array_equal(lse2[:, 0], lse1[:, 0])
+    # and query 1 differs (it sees one more key)
+    assert np.max(np.abs(out2[:, 1] - out1[:, 0])) > 1e-6
+
+
+def test_grouped_latent_isolation():
+    """GLA, G=2: heads 0..H/2-1 read only latent slice 0 (cache columns
+    0..255), heads H/2..H-1 only slice 1 (256..511); the RoPE key is shared.
+    Changing slice 1 of the cache moves only the second half of the heads."""
+    c = make_case(B=2, Lq=1, H=16, G=2, seq_lens=[70, 33], table="perm", seed=13)
+    out_a, lat_a, lse_a = oracle.decode(c.dims, **c.tensors())
+    t = c.tensors()
+    cache2 = c.cache.clone()
+    cache2[:, :, 256:512] = torch.randn(cache2[:, :, 256:512].shape).to(torch.bfloat16)
+    t.update(cache=cache2)
+    out_b, lat_b, lse_b = oracle.decode(c.dims, **t)
+    np.testing.assert_array_equal(out_a[:, :, :8], out_b[:, :, :8])
+    np.testing.assert_array_equal(lse_a[:, :, :8], lse_b[:, :, :8])
+    assert np.all(np.abs(out_a[:, :, 8:] - out_b[:, :, 8:]).max(axis=-1) > 1e-6)
+    # changing the shared RoPE key moves every head
+    cache3 = c.cache.clone()
+    cache3[:, :, D_C:] = torch.randn(cache3[:, :, D_C:].shape).to(torch.bfloat16)
+    t.update(cache=cache3)
+    out_c, _, _ = oracle.decode(c.dims, **t)
+    assert np.all(np.abs(out_a - out_c).max(axis=-1) > 1e-6)
+
+
+def test_selected_pairs_match_full_run():
+    """The sampled-pairs mode computes exactly the entries of a full run."""
+    c = workload("tiny")
+    full = oracle.decode(c.dims, **c.tensors())
+    sel = [(0, 3), (1, 15), (1, 0)]
+    part = oracle.decode(c.dims, **c.tensors(), sel=sel)
+    for f, p in zip(full, part):
+        for b, h in sel:
+            np.testing.assert_array_equal(f[b, :, h], p[b, :, h])
+    assert np.isnan(part[0][0, 0, 1]).all()
+
+
+# ---------------------------------------------------------------- merge
+
+def test_lse_merge_of_split_softmax_equals_unsplit():
+    """Softmax over disjoint key ranges, merged by log-sum-exp, equals the
+    softmax over all keys; an empty range (lse = -inf) changes nothing."""
+    rng = np.random.default_rng(1)
+    R, n, D = 5, 97, 12
+    s = rng.normal(size=(R, n)) * 3
+    v = rng.normal(size=(n, D))
+    cuts = [0, 10, 10, 60, n]                   # includes an empty range
+    parts, lses = [], []
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        if a == b:
+            parts.append(np.zeros((R, D)))
+            lses.append(np.full(R, -np.inf))
+            continue
+        e = np.exp(s[:, a:b])
+        parts.append((e @ v[a:b]) / e.sum(axis=1, keepdims=True))
+        lses.append(np.log(e.sum(axis=1)))
+    o, L = oracle.lse_merge(np.stack(parts), np.stack(lses))
+    e = np.exp(s)
+    np.testing.assert_allclose(o, (e @ v) / e.sum(axis=1, keepdims=True), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(L, np.log(e.sum(axis=1)), rtol=1e-13)
+    o1, L1 = oracle.lse_merge(np.stack(parts)[2:3], np.stack(lses)[2:3])
+    np.testing.assert_array_equal(o1, parts[2])
+
+
+def test_lse_merge_all_empty_row():
+    o, L = oracle.lse_merge(np.ones((2, 1, 3)), np.full((2, 1), -np.inf))
+    assert L[0] == -np.inf and np.all(o == 0)
+
+
+# ---------------------------------------------------------------- step helpers
+
+def test_absorb_and_project_are_the_plain_products():
+    """The absorbed query and the value up-projection are plain batched
+    products: check them against numpy matmul on the same bf16 values."""
+    c = make_case(B=2, Lq=2, H=16, G=2, seq_lens=[5, 9], seed=2)
+    qa = oracle.absorb(c.q_nope, c.W_UK)
+    ref = np.einsum("blhd,hdc->blhc", bf(c.q_nope), bf(c.W_UK))
+    np.testing.assert_allclose(qa, ref, rtol=1e-12, atol=1e-12)
+    o_lat = torch.randn(2, 2, 16, 256).to(torch.bfloat16)
+    pu = oracle.project_uv(o_lat, c.W_UV)
+    np.testing.assert_allclose(pu, np.einsum("hdc,blhc->blhd", bf(c.W_UV), bf(o_lat)), rtol=1e-12, atol=1e-12)
+
+
+def test_oracle_rejects_bad_tables():
+    c = workload("tiny")
+    t = c.tensors()
+    bt = c.block_table.clone()
+    bt[1, 2] = c.dims["num_pages"]
+    t.update(block_table=bt)
+    with pytest.raises(ValueError):
+        oracle.decode(c.dims, **t)
+    t = c.tensors()
+    t.update(seq_lens=torch.tensor([37, 10_000], dtype=torch.int32))
+    with pytest.raises(ValueError):
+        oracle.decode(c.dims, **t)
