@@ -1,0 +1,354 @@
+"""Benchmark of one MLA decode step (one layer) on GB300.
+
+A step is the whole hot path on one batch of synthetic input:
+    mla_absorb_q -> mla_decode_paged (plan + decode) -> mla_combine_splits -> mla_project_uv
+
+Default workload: DeepSeek-V3 dims, B=16, Lq=1, H=128, all seq_lens 4096,
+64-token pages, contiguous block tables.  Its 75.5 MB cache fits in the
+129 MB L2, so the timed loop rotates through 4 copies of the cache (302 MB),
+which keeps every step's cache reads coming from HBM.
+
+Prints ONE JSON line (rank 0).  `value` is latent-KV GB/s of the whole step
+(algorithmic bytes / step time); TFLOP/s, tokens/s and the roofline fraction
+ride along.  `--impl reference` times the fp64 CPU oracle on a bounded sample
+of the same workload instead.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+For N > 1 launch with torchrun; each rank runs its own batch (weak scaling, no
+collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MLA decode latent-KV GB/s & TFLOPS per layer, % of GB300 roofline; tokens/s"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+WORKLOAD_TEXT = {
+    "tiny": "tiny MLA decode B=2 Lq=1 H=16 seq {37,200}",
+    "dsv3": "DeepSeek-V3-dim decode B=16 Lq=1 H=128 seq 4096 contiguous",
+    "long": "long-context decode B=16 Lq=1 H=128 seq U[32768,65536] shuffled pages",
+    "spec": "speculative decode B=64 Lq=2 causal H=128 seq U[1024,16384] shuffled pages",
+    "gla": "grouped-latent decode G=2 B=32 Lq=1 H=128 seq 8192 contiguous",
+}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.f = None
+
+    def start(self):
+        try:
+            self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.Q, "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.flush()
+        self.f.seek(0)
+        rows = [l.strip().split(",") for l in self.f.read().splitlines() if l.strip()]
+        self.f.close()
+        os.unlink(self.f.name)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            try:
+                sm.append(float(r[1]))
+                mx = float(r[2])
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args, world, rank):
+    """The fp64 oracle timed on host cores over a bounded sample."""
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    from mla_latent_kv_10_gb300 import accounting as acc
+    from mla_latent_kv_10_gb300.inputs import workload
+
+    case = workload(args.workload)
+    d = case.dims
+    seq = case.seq_lens.tolist()
+    B, H = d["B"], d["H"]
+    step_bytes = acc.step_bytes(seq, d["Lq"], H, d["G"])
+    step_flops = acc.step_flops(seq, d["Lq"], H, d["G"])
+    nt = oracle.num_threads()
+    rng = np.random.default_rng(0)
+    # size one step's sample so the whole run stays within minutes
+    pairs_per_step = max(nt, 1)
+    times = []
+    work = 0.0
+    for i in range(args.warmup + args.steps):
+        bs = rng.integers(0, B, pairs_per_step)
+        hs = rng.integers(0, H, pairs_per_step)
+        sel = list(zip(bs.tolist(), hs.tolist()))
+        t0 = time.perf_counter()
+        oracle.decode(d, **case.tensors(), sel=sel, nthreads=nt)
+        dt = time.perf_counter() - t0
+        frac = sum(seq[b] for b, _ in sel) / (sum(seq) * H)
+        if i >= args.warmup:
+            times.append(dt)
+            work += frac
+    total = sum(times)
+    value = step_bytes * work / total / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / max(work, 1e-30) / args.steps * work / args.steps if False else 1e3 * total / args.steps / max(work / args.steps, 1e-30),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "tflops": step_flops * work / total / 1e12,
+        "config": {"workload": WORKLOAD_TEXT[args.workload], "B": B, "Lq": d["Lq"], "H": H, "G": d["G"],
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": nt, "kind": "oracle",
+                         "sample": "%d random (sequence, head) pairs per step; metric scaled by the "
+                                   "fraction of the step's work they cover" % pairs_per_step},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def cpu_baseline(case, budget_s=12.0):
+    """Oracle on a bounded sample of the workload, scaled to GB/s."""
+    import numpy as np
+    import oracle
+    from mla_latent_kv_10_gb300 import accounting as acc
+
+    d = case.dims
+    seq = case.seq_lens.tolist()
+    nt = oracle.num_threads()
+    B, H = d["B"], d["H"]
+    rng = np.random.default_rng(1)
+    step_bytes = acc.step_bytes(seq, d["Lq"], H, d["G"])
+    n_pairs = nt
+    sel = list(zip(rng.integers(0, B, n_pairs).tolist(), rng.integers(0, H, n_pairs).tolist()))
+    t0 = time.perf_counter()
+    oracle.decode(d, **case.tensors(), sel=sel, nthreads=nt)
+    t1 = time.perf_counter() - t0
+    rounds = max(1, int(budget_s / max(t1, 1e-3)) - 1)
+    total_t, frac = t1, sum(seq[b] for b, _ in sel) / (sum(seq) * H)
+    if rounds > 1 and t1 < budget_s / 2:
+        sel2 = list(zip(rng.integers(0, B, n_pairs * rounds).tolist(), rng.integers(0, H, n_pairs * rounds).tolist()))
+        t0 = time.perf_counter()
+        oracle.decode(d, **case.tensors(), sel=sel2, nthreads=nt)
+        total_t += time.perf_counter() - t0
+        frac += sum(seq[b] for b, _ in sel2) / (sum(seq) * H)
+        n_pairs += len(sel2)
+    return {"value": step_bytes * frac / total_t / 1e9, "unit": "GB/s", "cores": nt, "kind": "oracle",
+            "sample": "%d random (sequence, head) pairs of the same workload, %.1f s; scaled by the "
+                      "fraction of the step's work they cover" % (n_pairs, total_t)}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="dsv3", choices=sorted(WORKLOAD_TEXT))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--splits", type=int, default=0)
+    args = ap.parse_args()
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+
+    import torch
+    import mla_latent_kv_10_gb300 as mla
+    from mla_latent_kv_10_gb300 import accounting as acc
+    from mla_latent_kv_10_gb300.inputs import workload
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    mla.load_library()
+
+    # each rank decodes its own batch (weak scaling): same shape, own seed
+    case = workload(args.workload) if rank == 0 else workload(args.workload)
+    d = case.dims
+    seq = case.seq_lens.tolist()
+    B, Lq, H, G = d["B"], d["Lq"], d["H"], d["G"]
+    t = {k: v.to(dev) for k, v in case.tensors().items()}
+    cache_bytes = t["cache"].numel() * 2
+    copies = max(1, math.ceil(2.2 * L2_BYTES / cache_bytes))
+    caches = [t["cache"]] + [t["cache"].clone() for _ in range(copies - 1)]
+    bufs = mla.DecodeBuffers(d, dev)
+    stream = torch.cuda.current_stream(dev)
+
+    step_bytes = acc.step_bytes(seq, Lq, H, G)
+    step_flops = acc.step_flops(seq, Lq, H, G)
+    dec_bytes = acc.decode_bytes(seq, Lq, H, G)
+    dec_flops = acc.decode_flops(seq, Lq, H, G, causal=bool(d["causal"]))
+
+    def step(i, ev=None):
+        mla.mla_absorb_q(d, t["q_nope"], t["q_rope"], t["W_UK"], bufs.q_cat, stream)
+        if ev is not None:
+            ev[0].record(stream)
+        mla.mla_decode_paged(d, bufs.q_cat, caches[i % copies], t["block_table"], t["seq_lens"], args.splits,
+                             bufs.o_part, bufs.lse_part, bufs.workspace, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        mla.mla_combine_splits(d, bufs.o_part, bufs.lse_part, bufs.workspace, bufs.o_lat, bufs.lse, stream)
+        mla.mla_project_uv(d, bufs.o_lat, t["W_UV"], bufs.out, stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+    status = mla.mla_get_device_status(bufs.workspace, stream)
+    if status != 0:
+        raise SystemExit("device status after warm-up: %s" % mla.mla_status_string(status))
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    time.sleep(0.3)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(i, evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    if pg:
+        pg.barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    dec_ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
+    if pg:
+        x = torch.tensor([total_ms], device=dev)
+        pg.all_reduce(x, op=pg.ReduceOp.MAX)
+        total_ms = float(x.item())
+    ms = total_ms / args.steps
+    status = mla.mla_get_device_status(bufs.workspace, stream)
+
+    # end to end through the public API with host buffers: inputs H2D from
+    # pinned memory, result D2H, every step
+    h_in = {k: case.tensors()[k].pin_memory() for k in ("q_nope", "q_rope", "block_table", "seq_lens")}
+    h_out = torch.empty(bufs.out.shape, dtype=bufs.out.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in h_in.values())
+    d2h = h_out.numel() * h_out.element_size()
+
+    def e2e_step(i):
+        for k, v in h_in.items():
+            t[k].copy_(v, non_blocking=True)
+        step(i)
+        h_out.copy_(bufs.out, non_blocking=True)
+
+    for i in range(3):
+        e2e_step(i)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        e2e_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    if pg:
+        x = torch.tensor([e2e_ms], device=dev)
+        pg.all_reduce(x, op=pg.ReduceOp.MAX)
+        e2e_ms = float(x.item())
+
+    peaks, peak_src = load_peaks()
+    hbm = peaks["hbm_gbs"]
+    achieved = dec_bytes / (dec_ms * 1e-3) / 1e9
+    tflops_dec = dec_flops / (dec_ms * 1e-3) / 1e12
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC,
+        "value": world * step_bytes / (ms * 1e-3) / 1e9,
+        "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) cache and queries, N(0,1/d_g) weights)",
+        "config": {"workload": WORKLOAD_TEXT[args.workload], "B": B, "Lq": Lq, "H": H, "G": G,
+                   "seq_len_mean": sum(seq) / len(seq), "page_size": 64,
+                   "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "inputs larger than L2: %d rotating cache copies (%.0f MB)" % (copies, copies * cache_bytes / 1e6)},
+        "tflops": world * step_flops / (ms * 1e-3) / 1e12,
+        "tokens_per_s": world * B * Lq / (ms * 1e-3),
+        "roofline_frac_step": max(step_bytes / (ms * 1e-3) / 1e9 / hbm,
+                                  step_flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"]),
+        "decode_kernel": {"ms": dec_ms, "gbs": achieved, "tflops": tflops_dec,
+                          "tensor_frac": tflops_dec / peaks["bf16_tflops"],
+                          "bytes": dec_bytes, "flops": dec_flops},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "traffic": None, "peak_source": peak_src,
+                     "kernel": "mla_decode_paged (plan + decode)"},
+        "e2e": {"value": world * step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 5 * args.steps,
+        "clocks": clocks,
+        "device_status": mla.mla_status_string(status),
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(case)
+    print(json.dumps(line))
+    if pg:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,181 @@
+"""MLA decode with matrix absorption over a paged latent KV cache, on GB300.
+
+The compute lives in ``libmla.so`` (hand-written CUDA for sm_103a behind the
+C ABI of ``include/mla.h``).  This package is its thin Python binding: the
+functions below carry the C names, marshal torch tensors into pointers and
+sizes, and raise ``MLAError`` on a non-zero status.  There is no fallback:
+if the library is missing, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+__all__ = [
+    "MLAError", "Dims", "load_library", "library_path",
+    "mla_absorb_q", "mla_decode_paged", "mla_combine_splits", "mla_project_uv",
+    "mla_decode_workspace_size", "mla_decode_num_slots", "mla_get_device_status",
+    "mla_status_string", "make_dims", "DecodeBuffers", "decode_step",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+library_path = os.path.join(_PKG, "libmla.so")
+
+
+class MLAError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__("%s failed: %s (%d)" % (where, mla_status_string(code), code))
+
+
+class Dims(ctypes.Structure):
+    """Mirror of ``mla_dims``."""
+    _fields_ = [(n, ctypes.c_int) for n in (
+        "B", "Lq", "H", "d_hc", "d_c", "d_R", "G", "page_size", "max_pages_per_seq", "num_pages")] + [
+        ("scale", ctypes.c_float), ("causal", ctypes.c_int)]
+
+
+_lib = None
+_STATUS = {0: "MLA_OK", -1: "MLA_ERR_INVALID_ARG", -2: "MLA_ERR_UNSUPPORTED", -3: "MLA_ERR_MISALIGNED",
+           -4: "MLA_ERR_WORKSPACE", -5: "MLA_ERR_CUDA", -6: "MLA_ERR_BAD_TABLE",
+           -7: "MLA_ERR_TIMEOUT", -8: "MLA_ERR_BAD_SEQLEN"}
+
+
+def load_library():
+    """Load libmla.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(library_path):
+        raise RuntimeError("libmla.so is not built (run __graft_entry__.build()); "
+                           "there is no fallback implementation")
+    lib = ctypes.CDLL(library_path)
+    P, I, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    DP = ctypes.POINTER(Dims)
+    sig = {
+        "mla_absorb_q": [DP, P, P, P, P, P],
+        "mla_decode_num_slots": [DP, ctypes.POINTER(I)],
+        "mla_decode_workspace_size": [DP, ctypes.POINTER(S)],
+        "mla_decode_paged": [DP, P, P, P, P, I, P, P, P, S, P],
+        "mla_combine_splits": [DP, P, P, P, S, P, P, P],
+        "mla_project_uv": [DP, P, P, P, P],
+        "mla_get_device_status": [P, P],
+    }
+    for name, args in sig.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = I
+    lib.mla_status_string.argtypes = [I]
+    lib.mla_status_string.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def mla_status_string(code: int) -> str:
+    if _lib is not None:
+        return _lib.mla_status_string(int(code)).decode()
+    return _STATUS.get(int(code), "MLA_ERR_UNKNOWN")
+
+
+def make_dims(d: dict) -> Dims:
+    """dims dict (as produced by ``inputs.make_case``) -> ``mla_dims``."""
+    return Dims(B=d["B"], Lq=d["Lq"], H=d["H"], d_hc=d["d_hc"], d_c=d["d_c"], d_R=d["d_R"],
+                G=d["G"], page_size=d["page_size"], max_pages_per_seq=d["max_pages"],
+                num_pages=d["num_pages"], scale=float(d["scale"]), causal=int(d.get("causal", 1)))
+
+
+def _dims(d):
+    return ctypes.byref(d if isinstance(d, Dims) else make_dims(d))
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream()
+    if hasattr(stream, "cuda_stream"):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _check(rc, where):
+    if rc != 0:
+        raise MLAError(rc, where)
+
+
+def mla_absorb_q(dims, q_nope, q_rope, W_UK, q_cat, stream=None):
+    _check(load_library().mla_absorb_q(_dims(dims), _ptr(q_nope), _ptr(q_rope), _ptr(W_UK),
+                                       _ptr(q_cat), _stream(stream)), "mla_absorb_q")
+
+
+def mla_decode_workspace_size(dims) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load_library().mla_decode_workspace_size(_dims(dims), ctypes.byref(n)), "mla_decode_workspace_size")
+    return n.value
+
+
+def mla_decode_num_slots(dims) -> int:
+    n = ctypes.c_int(0)
+    _check(load_library().mla_decode_num_slots(_dims(dims), ctypes.byref(n)), "mla_decode_num_slots")
+    return n.value
+
+
+def mla_decode_paged(dims, q_cat, kv_cache, block_table, seq_lens, num_splits, o_part, lse_part,
+                     workspace, stream=None):
+    _check(load_library().mla_decode_paged(
+        _dims(dims), _ptr(q_cat), _ptr(kv_cache), _ptr(block_table), _ptr(seq_lens), int(num_splits),
+        _ptr(o_part), _ptr(lse_part), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)), "mla_decode_paged")
+
+
+def mla_combine_splits(dims, o_part, lse_part, workspace, o_lat, lse=None, stream=None):
+    _check(load_library().mla_combine_splits(
+        _dims(dims), _ptr(o_part), _ptr(lse_part), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(o_lat), _ptr(lse), _stream(stream)),
+        "mla_combine_splits")
+
+
+def mla_project_uv(dims, o_lat, W_UV, out, stream=None):
+    _check(load_library().mla_project_uv(_dims(dims), _ptr(o_lat), _ptr(W_UV), _ptr(out), _stream(stream)),
+           "mla_project_uv")
+
+
+def mla_get_device_status(workspace, stream=None) -> int:
+    return load_library().mla_get_device_status(_ptr(workspace), _stream(stream))
+
+
+class DecodeBuffers:
+    """Device buffers of one decode step for fixed dims (torch allocations;
+    the library itself never allocates)."""
+
+    def __init__(self, dims: dict, device="cuda"):
+        import torch
+        self.dims = dict(dims)
+        B, Lq, H, G = dims["B"], dims["Lq"], dims["H"], dims["G"]
+        d_g = dims["d_c"] // G
+        self.slots = mla_decode_num_slots(dims)
+        rows = Lq * H
+        self.q_cat = torch.empty(B, Lq, H, d_g + dims["d_R"], dtype=torch.bfloat16, device=device)
+        self.o_part = torch.empty(self.slots, rows, dims["d_c"], dtype=torch.float32, device=device)
+        self.lse_part = torch.empty(self.slots, rows, dtype=torch.float32, device=device)
+        self.workspace = torch.zeros(mla_decode_workspace_size(dims), dtype=torch.uint8, device=device)
+        self.o_lat = torch.empty(B, Lq, H, d_g, dtype=torch.bfloat16, device=device)
+        self.lse = torch.empty(B, Lq, H, dtype=torch.float32, device=device)
+        self.out = torch.empty(B, Lq, H, dims["d_hc"], dtype=torch.bfloat16, device=device)
+
+
+def decode_step(dims, bufs: DecodeBuffers, q_nope, q_rope, W_UK, W_UV, cache, block_table, seq_lens,
+                num_splits=0, stream=None):
+    """The whole hot path of one layer's decode step: absorb, paged decode,
+    combine, project.  All tensors on the device; results land in ``bufs``."""
+    mla_absorb_q(dims, q_nope, q_rope, W_UK, bufs.q_cat, stream)
+    mla_decode_paged(dims, bufs.q_cat, cache, block_table, seq_lens, num_splits, bufs.o_part,
+                     bufs.lse_part, bufs.workspace, stream)
+    mla_combine_splits(dims, bufs.o_part, bufs.lse_part, bufs.workspace, bufs.o_lat, bufs.lse, stream)
+    mla_project_uv(dims, bufs.o_lat, W_UV, bufs.out, stream)
+    return bufs.out

@@ -1,0 +1,217 @@
+// mla_api.cu — the C ABI declared in include/mla.h: argument validation,
+// tensor-map encoding, kernel launches.  No allocation, no global state
+// beyond per-device launch-configuration caches.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "mla_internal.h"
+
+using namespace mla;
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// bf16 tensor map with 128-byte swizzle; dims innermost first; strides in
+// bytes for dims 1..rank-1.
+int make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
+             const cuuint64_t* strides, const cuuint32_t* box) {
+  auto fn = encode_fn();
+  if (!fn) return MLA_ERR_CUDA;
+  cuuint32_t elem[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides,
+                  box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_dims(const mla_dims* d) {
+  if (!d) return MLA_ERR_INVALID_ARG;
+  if (d->B < 1 || d->Lq < 1 || d->H < 1 || d->max_pages_per_seq < 1 || d->num_pages < 1)
+    return MLA_ERR_INVALID_ARG;
+  if (!(d->scale > 0.f) || !std::isfinite(d->scale)) return MLA_ERR_INVALID_ARG;
+  if (d->d_hc != kDhc || d->d_c != kDc || d->d_R != kDr || d->page_size != kPage)
+    return MLA_ERR_UNSUPPORTED;
+  if (d->G != 1 && d->G != 2) return MLA_ERR_UNSUPPORTED;
+  if (d->Lq > 2 || d->H % 16 != 0 || d->H > 128 || d->H % d->G != 0) return MLA_ERR_UNSUPPORTED;
+  // TMA row coordinate page*64 and table indices stay in int32
+  if ((long long)d->num_pages * kPage >= (1LL << 31)) return MLA_ERR_UNSUPPORTED;
+  if ((long long)d->B * d->max_pages_per_seq >= (1LL << 31)) return MLA_ERR_UNSUPPORTED;
+  if ((long long)d->max_pages_per_seq * kPage >= (1LL << 31)) return MLA_ERR_UNSUPPORTED;
+  return MLA_OK;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA; }
+
+int row_blocks(const mla_dims* d) { return (d->Lq * d->H + kRowsPerCta - 1) / kRowsPerCta; }
+
+}  // namespace
+
+extern "C" {
+
+const char* mla_status_string(int s) {
+  switch (s) {
+    case MLA_OK: return "MLA_OK";
+    case MLA_ERR_INVALID_ARG: return "MLA_ERR_INVALID_ARG";
+    case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED";
+    case MLA_ERR_MISALIGNED: return "MLA_ERR_MISALIGNED";
+    case MLA_ERR_WORKSPACE: return "MLA_ERR_WORKSPACE";
+    case MLA_ERR_CUDA: return "MLA_ERR_CUDA";
+    case MLA_ERR_BAD_TABLE: return "MLA_ERR_BAD_TABLE";
+    case MLA_ERR_BAD_SEQLEN: return "MLA_ERR_BAD_SEQLEN";
+    case MLA_ERR_TIMEOUT: return "MLA_ERR_TIMEOUT";
+    default: return "MLA_ERR_UNKNOWN";
+  }
+}
+
+int mla_absorb_q(const mla_dims* d, const void* q_nope, const void* q_rope, const void* W_UK,
+                 void* q_cat, void* stream) {
+  int rc = check_dims(d);
+  if (rc != MLA_OK) return rc;
+  if (!q_nope || !q_rope || !W_UK || !q_cat) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(q_nope) || !aligned16(q_rope) || !aligned16(W_UK) || !aligned16(q_cat))
+    return MLA_ERR_MISALIGNED;
+  const int M = d->B * d->Lq, H = d->H, dg = kDc / d->G;
+  CUtensorMap tA, tB;
+  {
+    cuuint64_t dims[3] = {(cuuint64_t)kDhc, (cuuint64_t)H, (cuuint64_t)M};
+    cuuint64_t strides[2] = {(cuuint64_t)kDhc * 2, (cuuint64_t)H * kDhc * 2};
+    cuuint32_t box[3] = {64, 1, kRowsPerCta};
+    if ((rc = make_map(&tA, q_nope, 3, dims, strides, box)) != MLA_OK) return rc;
+  }
+  {
+    cuuint64_t dims[3] = {(cuuint64_t)dg, (cuuint64_t)kDhc, (cuuint64_t)H};
+    cuuint64_t strides[2] = {(cuuint64_t)dg * 2, (cuuint64_t)kDhc * dg * 2};
+    cuuint32_t box[3] = {64, kDhc, 1};
+    if ((rc = make_map(&tB, W_UK, 3, dims, strides, box)) != MLA_OK) return rc;
+  }
+  return cuda_status(launch_absorb(tA, tB, q_rope, q_cat, M, H, dg, static_cast<cudaStream_t>(stream)));
+}
+
+int mla_project_uv(const mla_dims* d, const void* o_lat, const void* W_UV, void* out, void* stream) {
+  int rc = check_dims(d);
+  if (rc != MLA_OK) return rc;
+  if (!o_lat || !W_UV || !out) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(o_lat) || !aligned16(W_UV) || !aligned16(out)) return MLA_ERR_MISALIGNED;
+  const int M = d->B * d->Lq, H = d->H, dg = kDc / d->G;
+  CUtensorMap tA, tB;
+  {
+    cuuint64_t dims[3] = {(cuuint64_t)dg, (cuuint64_t)H, (cuuint64_t)M};
+    cuuint64_t strides[2] = {(cuuint64_t)dg * 2, (cuuint64_t)H * dg * 2};
+    cuuint32_t box[3] = {64, 1, kRowsPerCta};
+    if ((rc = make_map(&tA, o_lat, 3, dims, strides, box)) != MLA_OK) return rc;
+  }
+  {
+    cuuint64_t dims[3] = {(cuuint64_t)dg, (cuuint64_t)kDhc, (cuuint64_t)H};
+    cuuint64_t strides[2] = {(cuuint64_t)dg * 2, (cuuint64_t)kDhc * dg * 2};
+    cuuint32_t box[3] = {64, kDhc, 1};
+    if ((rc = make_map(&tB, W_UV, 3, dims, strides, box)) != MLA_OK) return rc;
+  }
+  return cuda_status(launch_project(tA, tB, out, M, H, dg, static_cast<cudaStream_t>(stream)));
+}
+
+int mla_decode_workspace_size(const mla_dims* d, size_t* bytes) {
+  int rc = check_dims(d);
+  if (rc != MLA_OK) return rc;
+  if (!bytes) return MLA_ERR_INVALID_ARG;
+  *bytes = ws_bytes_for(d->B);
+  return MLA_OK;
+}
+
+int mla_decode_num_slots(const mla_dims* d, int* slots) {
+  int rc = check_dims(d);
+  if (rc != MLA_OK) return rc;
+  if (!slots) return MLA_ERR_INVALID_ARG;
+  int units = 0;
+  if ((rc = decode_max_units(2 * row_blocks(d), &units)) != MLA_OK) return rc;
+  *slots = d->B + units - 1;
+  return MLA_OK;
+}
+
+int mla_decode_paged(const mla_dims* d, const void* q_cat, const void* kv_cache,
+                     const int32_t* block_table, const int32_t* seq_lens, int num_splits,
+                     float* o_part, float* lse_part, void* workspace, size_t ws_bytes, void* stream) {
+  int rc = check_dims(d);
+  if (rc != MLA_OK) return rc;
+  if (!q_cat || !kv_cache || !block_table || !seq_lens || !o_part || !lse_part || num_splits < 0)
+    return MLA_ERR_INVALID_ARG;
+  if (!workspace || ws_bytes < ws_bytes_for(d->B)) return MLA_ERR_WORKSPACE;
+  if (!aligned16(q_cat) || !aligned16(kv_cache) || !aligned16(o_part) || !aligned16(workspace) ||
+      (reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u) ||
+      (reinterpret_cast<uintptr_t>(lse_part) & 3u))
+    return MLA_ERR_MISALIGNED;
+  const int csize = 2 * row_blocks(d);
+  int units = 0;
+  if ((rc = decode_max_units(csize, &units)) != MLA_OK) return rc;
+  if (num_splits > 0 && num_splits < units) units = num_splits;
+  auto st = static_cast<cudaStream_t>(stream);
+  CUtensorMap tm;
+  {
+    cuuint64_t dims[2] = {(cuuint64_t)kRow, (cuuint64_t)d->num_pages * kPage};
+    cuuint64_t strides[1] = {(cuuint64_t)kRow * 2};
+    cuuint32_t box[2] = {64, kPage};
+    if ((rc = make_map(&tm, kv_cache, 2, dims, strides, box)) != MLA_OK) return rc;
+  }
+  auto* ws = static_cast<WsHeader*>(workspace);
+  cudaError_t e = launch_plan(seq_lens, block_table, ws, d->B, d->Lq, d->max_pages_per_seq,
+                              d->num_pages, units, st);
+  if (e != cudaSuccess) return MLA_ERR_CUDA;
+  DecodeArgs a;
+  a.q_cat = static_cast<const __nv_bfloat16*>(q_cat);
+  a.block_table = block_table;
+  a.o_part = o_part;
+  a.lse_part = lse_part;
+  a.ws = ws;
+  a.B = d->B;
+  a.Lq = d->Lq;
+  a.H = d->H;
+  a.G = d->G;
+  a.d_g = kDc / d->G;
+  a.max_pages = d->max_pages_per_seq;
+  a.num_pages = d->num_pages;
+  a.causal = d->causal ? 1 : 0;
+  a.rows = d->Lq * d->H;
+  a.scale_log2 = d->scale * 1.4426950408889634f;
+  return cuda_status(launch_decode(tm, a, units, csize, st));
+}
+
+int mla_combine_splits(const mla_dims* d, const float* o_part, const float* lse_part,
+                       const void* workspace, size_t ws_bytes, void* o_lat, float* lse,
+                       void* stream) {
+  int rc = check_dims(d);
+  if (rc != MLA_OK) return rc;
+  if (!o_part || !lse_part || !o_lat) return MLA_ERR_INVALID_ARG;
+  if (!workspace || ws_bytes < ws_bytes_for(d->B)) return MLA_ERR_WORKSPACE;
+  if (!aligned16(o_part) || !aligned16(o_lat) || !aligned16(workspace)) return MLA_ERR_MISALIGNED;
+  return cuda_status(launch_combine(o_part, lse_part, static_cast<const WsHeader*>(workspace), o_lat,
+                                    lse, d->B, d->Lq, d->H, d->G, static_cast<cudaStream_t>(stream)));
+}
+
+int mla_get_device_status(const void* workspace, void* stream) {
+  if (!workspace) return MLA_ERR_INVALID_ARG;
+  auto st = static_cast<cudaStream_t>(stream);
+  int status = 0;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MLA_ERR_CUDA;
+  if (cudaMemcpy(&status, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  return status;
+}
+
+}  // extern "C"

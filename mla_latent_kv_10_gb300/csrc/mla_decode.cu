@@ -1,0 +1,623 @@
+// mla_decode.cu — split-KV flash-decoding of MLA over the paged latent cache
+// (plan kernel, decode kernel, log-sum-exp combine kernel).
+//
+// Method: MLA operator write-up (nxmr.cn/news/151634) §1 (cache row = 512-d
+// latent + 64-d RoPE key), §3 (64-token pages, a tile of 64 tokens, a
+// multi-stage copy pipeline) and §4 (matrix absorption: scores are
+// q_abs . c_KV + q_R . k_R, so attention runs in the 576-d latent space and
+// the cache is never decompressed).
+//
+// GB300 design of the decode kernel
+//   * Query rows (l, h) form the M = 128 dimension of tcgen05 MMAs; a page
+//     of 64 tokens is the N (scores) or K (values) dimension.
+//   * An fp32 accumulator O of 128 rows x 512 latents would fill all 512
+//     tensor-memory columns of an SM, so each 128-row block runs on a CTA
+//     PAIR (cluster rank bit 0 = r): CTA r owns latent half r (256 columns of
+//     O) and loads only its half of each page (CTA 0 also loads the RoPE
+//     columns).  Each CTA computes a partial score tile over its columns;
+//     the two partials are swapped through distributed shared memory and
+//     summed, so both CTAs hold the same fp32 scores and run the same online
+//     softmax, bit for bit.
+//   * Tensor memory per CTA: O (256 cols) | Q (<=160 cols, bf16 pairs, the
+//     MMA A operand) | S (64 cols) | P (32 cols, bf16 pairs, A operand of
+//     the P.V MMA).  The page tile in shared memory is used twice: K-major as
+//     B for S = Q.K^T and MN-major as B for O += P.V.
+//   * Pages arrive by TMA (64 x 64 bf16 boxes, 128-byte swizzle) into a
+//     4-stage mbarrier ring; one thread issues MMAs, one thread issues copies,
+//     four warps (one TMEM lane quadrant each, one thread per query row) do
+//     the exchange, masking, online softmax and epilogue.
+//   * Split-KV: the pages of all sequences, in order, are cut into equal
+//     contiguous ranges, one per cluster; a range that covers parts of several
+//     sequences yields one partial (o, lse) per sequence, stored in slot
+//     b + unit.  The combine kernel merges them.
+//   * Every wait is bounded (wall clock); on expiry the kernel records
+//     MLA_ERR_TIMEOUT in the workspace status word, stops, waits for its own
+//     copies and MMAs, frees tensor memory and returns.
+#include <cmath>
+
+#include "mla_internal.h"
+#include "ptx.cuh"
+
+namespace mla {
+
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kBoxBytes = kPage * 64 * 2;       // 64 tokens x 64 bf16 = 8 KiB
+constexpr int kStageBytes = 5 * kBoxBytes;      // latent half (4 boxes) + RoPE box
+constexpr int kXBytes = kRowsPerCta * 64 * 4;   // one fp32 score tile, 32 KiB
+constexpr int kDecodeSmem = 1024 + kStages * kStageBytes + 2 * kXBytes;
+constexpr int kDecodeThreads = 192;             // 4 softmax warps, TMA warp, MMA warp
+constexpr uint32_t kColO = 0, kColQ = 256, kColS = 416, kColP = 480, kTmemCols = 512;
+constexpr float kRescaleThreshold = 8.0f;       // log2 units: defer O rescaling up to 2^8
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float lg2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ void set_status(WsHeader* ws, int code) {
+  atomicCAS(&ws->status, 0, code);
+}
+
+// Shared state of one decode CTA (static shared memory).
+struct DecodeShared {
+  uint64_t full[kStages], empty[kStages];
+  uint64_t q_full, s_full, s_free, p_full, o_done, drain;
+  uint64_t xfull[2], xfree[2];
+  uint32_t tmem;
+  int abort;
+};
+
+// Walks the (sequence, page range) segments of one work unit.
+struct SegIter {
+  const int* off;
+  int B, start, end, b;
+  __device__ void init(const WsHeader* ws, int unit) {
+    off = reinterpret_cast<const int*>(ws + 1);
+    B = ws->B;
+    const int total = ws->total, chunk = ws->chunk;
+    start = min(unit * chunk, total);
+    end = min(start + chunk, total);
+    // largest b with off[b] <= start
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (off[mid] <= start) lo = mid; else hi = mid - 1;
+    }
+    b = lo;
+  }
+  // Next non-empty segment: sequence b, pages [pa, pb) of that sequence.
+  __device__ bool next(int& sb, int& pa, int& pb) {
+    while (b < B && start < end) {
+      const int o0 = off[b], o1 = off[b + 1];
+      const int a = max(start, o0), e = min(end, o1);
+      const int cur = b++;
+      if (a < e) {
+        sb = cur;
+        pa = a - o0;
+        pb = e - o0;
+        return true;
+      }
+      if (o0 >= end) break;
+    }
+    return false;
+  }
+};
+
+__global__ void __launch_bounds__(kDecodeThreads, 1)
+    decode_kernel(const __grid_constant__ CUtensorMap tm_cache, const DecodeArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ DecodeShared sh;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* stages = smem;
+  float* xbuf = reinterpret_cast<float*>(smem + kStages * kStageBytes);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t crank = cluster_ctarank();
+  const uint32_t r = crank & 1u;         // latent half owned by this CTA
+  const uint32_t rg = crank >> 1;        // 128-row block of the query rows
+  const uint32_t peer = crank ^ 1u;
+  const int unit = (int)cluster_id_x();
+  WsHeader* ws = a.ws;
+  const int* nlen = reinterpret_cast<const int*>(ws + 1) + a.B + 1;
+
+  auto bar = [](uint64_t& x) { return smem_u32(&x); };
+
+  if (threadIdx.x == 0) {
+    sh.abort = 0;
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar(sh.full[s]), 1);
+      mbar_init(bar(sh.empty[s]), 1);
+    }
+    mbar_init(bar(sh.q_full), 128);
+    mbar_init(bar(sh.s_full), 1);
+    mbar_init(bar(sh.s_free), 128);
+    mbar_init(bar(sh.p_full), 128);
+    mbar_init(bar(sh.o_done), 1);
+    mbar_init(bar(sh.drain), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(sh.xfull[s]), 128);
+      mbar_init(bar(sh.xfree[s]), 128);
+    }
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_cache);
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(&sh.tmem), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // peer barriers initialised before any remote arrive
+  tc_fence_after();
+  const uint32_t tmem = sh.tmem;
+  volatile int* abort = &sh.abort;
+
+  auto fail = [&]() {
+    *abort = 1;
+    set_status(ws, MLA_ERR_TIMEOUT);
+  };
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const int nbox = (r == 0) ? 5 : 4;
+      const uint32_t bytes = nbox * kBoxBytes;
+      const uint64_t policy = l2_policy_evict_first();
+      SegIter it;
+      it.init(ws, unit);
+      int sb, pa, pb;
+      uint32_t pc = 0;
+      bool ok = true;
+      while (ok && it.next(sb, pa, pb)) {
+        const int32_t* bt = a.block_table + (size_t)sb * a.max_pages;
+        for (int i = pa; i < pb; ++i, ++pc) {
+          const int st = pc % kStages;
+          if (pc >= (uint32_t)kStages && !(ok = mbar_wait(bar(sh.empty[st]), ((pc / kStages) - 1) & 1, abort))) {
+            fail();
+            break;
+          }
+          int page = bt[i];
+          if (page < 0 || page >= a.num_pages) page = 0;  // reported by the plan kernel
+          const uint32_t dst = smem_u32(stages + st * kStageBytes);
+          mbar_arrive_expect_tx(bar(sh.full[st]), bytes);
+          for (int j = 0; j < 4; ++j)
+            tma_load_2d_hint(dst + j * kBoxBytes, &tm_cache, bar(sh.full[st]), (int)(r * 256 + j * 64),
+                             page * kPage, policy);
+          if (r == 0)
+            tma_load_2d_hint(dst + 4 * kBoxBytes, &tm_cache, bar(sh.full[st]), kDc, page * kPage, policy);
+        }
+      }
+      // Copies still in flight must land before this CTA may exit.
+      if (!ok) {
+        for (uint32_t k = (pc > (uint32_t)kStages ? pc - kStages : 0); k < pc; ++k)
+          mbar_wait(bar(sh.full[k % kStages]), (k / kStages) & 1, abort, 100000000ull);
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const int nk = (r == 0) ? 20 : 16;  // K steps of 16 for the score MMA
+      constexpr uint32_t idesc_qk = idesc_bf16(128, 64, false, false);
+      constexpr uint32_t idesc_pv = idesc_bf16(128, 256, false, true);
+      SegIter it;
+      it.init(ws, unit);
+      int sb, pa, pb;
+      uint32_t pc = 0, qc = 0;
+      bool ok = true;
+      auto issue_pv = [&](uint32_t q, bool acc) -> bool {
+        if (!mbar_wait(bar(sh.p_full), q & 1, abort)) return false;
+        tc_fence_after();
+        const uint32_t base = smem_u32(stages + (q % kStages) * kStageBytes);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {  // 64 tokens = 4 K steps
+          const uint64_t vd = sdesc_sw128(base + kk * 2048, kBoxBytes, 1024);
+          mma_ts(tmem + kColO, tmem + kColP + kk * 8, vd, idesc_pv, (acc || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(bar(sh.empty[q % kStages]));
+        mma_commit(bar(sh.o_done));
+        return true;
+      };
+      while (ok && it.next(sb, pa, pb)) {
+        if (!(ok = mbar_wait(bar(sh.q_full), qc & 1, abort))) break;
+        ++qc;
+        tc_fence_after();
+        for (int i = pa; i < pb; ++i, ++pc) {
+          const int st = pc % kStages;
+          if (!(ok = mbar_wait(bar(sh.full[st]), (pc / kStages) & 1, abort))) break;
+          if (pc > 0 && !(ok = mbar_wait(bar(sh.s_free), (pc - 1) & 1, abort))) break;
+          tc_fence_after();
+          const uint32_t base = smem_u32(stages + st * kStageBytes);
+          for (int kk = 0; kk < nk; ++kk) {
+            const uint64_t kd = sdesc_sw128(base + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024);
+            mma_ts(tmem + kColS, tmem + kColQ + kk * 8, kd, idesc_qk, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(bar(sh.s_full));
+          if (i > pa && !(ok = issue_pv(pc - 1, i - 1 > pa))) break;
+        }
+        if (!ok) break;
+        if (!(ok = issue_pv(pc - 1, pb - 1 > pa))) break;
+      }
+      if (!ok) fail();
+    }
+  } else {
+    // ------------------------------------------------------------ softmax warps
+    const int row = threadIdx.x;                 // TMEM lane = query row in this block
+    const int grow = (int)rg * kRowsPerCta + row;  // row of the (l, h) list
+    const bool valid = grow < a.rows;
+    const int l = valid ? grow / a.H : 0;
+    const int h = valid ? grow % a.H : 0;
+    const int g = (h * a.G) / a.H;
+    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    const uint32_t peer_x = mapa(smem_u32(xbuf), peer);
+    const uint32_t peer_xfull0 = mapa(bar(sh.xfull[0]), peer), peer_xfull1 = mapa(bar(sh.xfull[1]), peer);
+    const uint32_t peer_xfree0 = mapa(bar(sh.xfree[0]), peer), peer_xfree1 = mapa(bar(sh.xfree[1]), peer);
+    const int d_q = a.d_g + kDr;
+    SegIter it;
+    it.init(ws, unit);
+    int sb, pa, pb;
+    uint32_t pc = 0, od = 0;
+    bool ok = true;
+    while (ok && it.next(sb, pa, pb)) {
+      const int seg = sb + unit;
+      const int n = nlen[sb];
+      const int limit = a.causal ? n - a.Lq + l + 1 : n;  // keys [0, limit) visible
+
+      // ---- load this CTA's slice of the query row into tensor memory
+      {
+        const __nv_bfloat16* qrow = a.q_cat + ((size_t)(sb * a.Lq + l) * a.H + h) * d_q;
+        const uint4* lat = nullptr;
+        if (valid) {
+          if (a.G == 1) lat = reinterpret_cast<const uint4*>(qrow + r * 256);
+          else if ((uint32_t)g == r) lat = reinterpret_cast<const uint4*>(qrow);
+        }
+        const uint4* rope = valid ? reinterpret_cast<const uint4*>(qrow + a.d_g) : nullptr;
+        const int nchunk = (r == 0) ? 5 : 4;
+        for (int c = 0; c < nchunk; ++c) {
+          const uint4* src = (c < 4) ? (lat ? lat + c * 8 : nullptr) : rope;
+          uint32_t w[32];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            uint4 v = src ? src[q] : make_uint4(0, 0, 0, 0);
+            w[4 * q + 0] = v.x; w[4 * q + 1] = v.y; w[4 * q + 2] = v.z; w[4 * q + 3] = v.w;
+          }
+          tmem_st32(lane_base + kColQ + c * 32, w);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(sh.q_full));
+      }
+
+      float m_used = -INFINITY, l_sum = 0.f;
+      for (int i = pa; i < pb; ++i, ++pc) {
+        // ---- partial scores of this CTA's columns
+        ok = mbar_wait(bar(sh.s_full), pc & 1, abort);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        tc_fence_after();
+        float s[64];
+        {
+          uint32_t v[32];
+          tmem_ld32(lane_base + kColS, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) s[j] = __uint_as_float(v[j]);
+          tmem_ld32(lane_base + kColS + 32, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) s[32 + j] = __uint_as_float(v[j]);
+        }
+        tc_fence_before();
+        mbar_arrive(bar(sh.s_free));
+
+        // ---- swap partials with the peer CTA (slot alternates per page)
+        const uint32_t slot = pc & 1, use = pc >> 1;
+        if (use > 0) {
+          ok = mbar_wait<true>(bar(sh.xfree[slot]), (use - 1) & 1, abort);
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        }
+        const uint32_t xrow = slot * kXBytes + row * 256;
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          st_cluster_v4(peer_x + xrow + ((c ^ (row & 15)) << 4),
+                        make_float4(s[4 * c], s[4 * c + 1], s[4 * c + 2], s[4 * c + 3]));
+        mbar_arrive_remote(slot ? peer_xfull1 : peer_xfull0);
+        ok = mbar_wait<true>(bar(sh.xfull[slot]), use & 1, abort);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        {
+          const float* mine = reinterpret_cast<const float*>(reinterpret_cast<const uint8_t*>(xbuf) + xrow);
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const float4 t = *reinterpret_cast<const float4*>(mine + 4 * (c ^ (row & 15)));
+            s[4 * c] += t.x; s[4 * c + 1] += t.y; s[4 * c + 2] += t.z; s[4 * c + 3] += t.w;
+          }
+        }
+        mbar_arrive_remote(slot ? peer_xfree1 : peer_xfree0);
+
+        // ---- mask, scale to log2 units, tile max
+        const int key0 = i * kPage;
+        float mt = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 64; ++j) {
+          const float v = (key0 + j < limit) ? s[j] * a.scale_log2 : -INFINITY;
+          s[j] = v;
+          mt = fmaxf(mt, v);
+        }
+        const bool need = mt > m_used + kRescaleThreshold;
+        const bool first = (i == pa);
+        if (!first) {  // P.V of the previous page done: P and O are ours
+          ok = mbar_wait(bar(sh.o_done), od & 1, abort);
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+          ++od;
+          tc_fence_after();
+          if (__any_sync(0xffffffffu, need)) {
+            const float f = need ? ex2(m_used - mt) : 1.0f;
+            for (int c = 0; c < 8; ++c) {
+              uint32_t v[32];
+              tmem_ld32(lane_base + kColO + c * 32, v);
+              tmem_wait_ld();
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * f);
+              tmem_st32(lane_base + kColO + c * 32, v);
+            }
+            l_sum *= f;
+          }
+        }
+        if (need) m_used = mt;
+        const float base = (m_used == -INFINITY) ? 0.f : m_used;
+        uint32_t pk[32];
+        float psum = 0.f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const uint32_t w = pack_bf16x2(ex2(s[2 * j] - base), ex2(s[2 * j + 1] - base));
+          psum += bf16_lo(w) + bf16_hi(w);
+          pk[j] = w;
+        }
+        l_sum += psum;
+        tmem_st32(lane_base + kColP, pk);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(sh.p_full));
+      }
+      if (!ok) break;
+
+      // ---- epilogue: normalised latent partial and log-sum-exp
+      ok = mbar_wait(bar(sh.o_done), od & 1, abort);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      ++od;
+      tc_fence_after();
+      const float inv = l_sum > 0.f ? 1.0f / l_sum : 0.f;
+      float* dst = a.o_part + ((size_t)seg * a.rows + grow) * kDc + r * 256;
+      for (int c = 0; c < 8; ++c) {
+        uint32_t v[32];
+        tmem_ld32(lane_base + kColO + c * 32, v);
+        tmem_wait_ld();
+        if (valid) {
+          float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            d4[q] = make_float4(__uint_as_float(v[4 * q]) * inv, __uint_as_float(v[4 * q + 1]) * inv,
+                                __uint_as_float(v[4 * q + 2]) * inv, __uint_as_float(v[4 * q + 3]) * inv);
+        }
+      }
+      if (valid && r == 0)
+        a.lse_part[(size_t)seg * a.rows + grow] =
+            l_sum > 0.f ? (m_used + lg2(l_sum)) * 0.69314718055994531f : -INFINITY;
+      tc_fence_before();
+    }
+    if (!ok) fail();
+  }
+
+  // ------------------------------------------------------------ teardown
+  __syncthreads();
+  if (warp == 5) {
+    if (*abort) {  // let MMAs already issued finish before freeing their memory
+      if (lane == 0) {
+        mma_commit(bar(sh.drain));
+        mbar_wait(bar(sh.drain), 0, abort, 100000000ull);
+      }
+      __syncwarp();
+    }
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+  cluster_sync();  // the peer may still write into this CTA's exchange buffer until here
+}
+
+// ---------------------------------------------------------------- plan
+// One CTA: validates lengths and table entries, prefix-sums pages per
+// sequence, cuts the flattened page list into `units` equal ranges.
+__global__ void __launch_bounds__(1024)
+    plan_kernel(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ block_table,
+                WsHeader* ws, int B, int Lq, int max_pages, int num_pages, int units) {
+  __shared__ int scan[1024];
+  __shared__ int carry;
+  int* off = reinterpret_cast<int*>(ws + 1);
+  int* nlen = off + B + 1;
+  const int tid = threadIdx.x;
+  if (tid == 0) carry = 0;
+  __syncthreads();
+  const int lo = Lq > 1 ? Lq : 1, hi = max_pages * kPage;
+  for (int base = 0; base < B; base += 1024) {
+    const int b = base + tid;
+    int np = 0;
+    if (b < B) {
+      int n = seq_lens[b];
+      if (n < lo || n > hi) {
+        set_status(ws, MLA_ERR_BAD_SEQLEN);
+        n = n < lo ? lo : hi;
+      }
+      nlen[b] = n;
+      np = (n + kPage - 1) / kPage;
+    }
+    scan[tid] = np;
+    __syncthreads();
+    for (int d = 1; d < 1024; d <<= 1) {
+      const int v = tid >= d ? scan[tid - d] : 0;
+      __syncthreads();
+      scan[tid] += v;
+      __syncthreads();
+    }
+    if (b < B) off[b] = carry + scan[tid] - np;
+    __syncthreads();
+    if (tid == 1023) carry += scan[1023];
+    __syncthreads();
+  }
+  if (tid == 0) {
+    off[B] = carry;
+    ws->total = carry;
+    ws->chunk = carry > 0 ? (carry + units - 1) / units : 1;
+    ws->units = units;
+    ws->B = B;
+  }
+  __syncthreads();
+  // table entries actually used must name a real page
+  const long long entries = (long long)B * max_pages;
+  for (long long e = tid; e < entries; e += 1024) {
+    const int b = (int)(e / max_pages), i = (int)(e % max_pages);
+    if (i * kPage < nlen[b]) {
+      const int pg = block_table[e];
+      if (pg < 0 || pg >= num_pages) set_status(ws, MLA_ERR_BAD_TABLE);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- combine
+// One warp per (sequence, query row): log-sum-exp over the row's partials
+// (warp-shuffle max and sum), then the weighted sum of its latent slice.
+template <int DG>
+__global__ void __launch_bounds__(256)
+    combine_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part,
+                   const WsHeader* __restrict__ ws, __nv_bfloat16* __restrict__ o_lat,
+                   float* __restrict__ lse_out, int B, int Lq, int H, int G) {
+  const int rows = Lq * H;
+  const int gw = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (gw >= B * rows) return;
+  const int b = gw / rows, row = gw % rows;
+  const int h = row % H, g = (h * G) / H;
+  const int* off = reinterpret_cast<const int*>(ws + 1);
+  const int chunk = ws->chunk;
+  const int o0 = off[b], np = off[b + 1] - o0;
+  const int kf = o0 / chunk, kl = (o0 + np - 1) / chunk;
+  const int nseg = kl - kf + 1;
+  const size_t seg0 = (size_t)b + kf;
+
+  float mx = -INFINITY;
+  for (int j = lane; j < nseg; j += 32) mx = fmaxf(mx, lse_part[(seg0 + j) * rows + row]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  float sum = 0.f;
+  if (mx != -INFINITY)
+    for (int j = lane; j < nseg; j += 32) sum += expf(lse_part[(seg0 + j) * rows + row] - mx);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  const float L = (mx == -INFINITY) ? -INFINITY : mx + logf(sum);
+
+  constexpr int kQ = DG / 128;  // float4 per lane
+  float4 acc[kQ];
+#pragma unroll
+  for (int q = 0; q < kQ; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (L != -INFINITY) {
+    for (int j = 0; j < nseg; ++j) {
+      const float w = expf(lse_part[(seg0 + j) * rows + row] - L);
+      if (w == 0.f) continue;
+      const float4* src = reinterpret_cast<const float4*>(o_part + ((seg0 + j) * rows + row) * kDc + g * DG);
+#pragma unroll
+      for (int q = 0; q < kQ; ++q) {
+        const float4 v = src[q * 32 + lane];
+        acc[q].x += w * v.x; acc[q].y += w * v.y; acc[q].z += w * v.z; acc[q].w += w * v.w;
+      }
+    }
+  }
+  __nv_bfloat16* dst = o_lat + ((size_t)b * rows + row) * DG;
+#pragma unroll
+  for (int q = 0; q < kQ; ++q) {
+    uint2 v;
+    v.x = pack_bf16x2(acc[q].x, acc[q].y);
+    v.y = pack_bf16x2(acc[q].z, acc[q].w);
+    reinterpret_cast<uint2*>(dst)[q * 32 + lane] = v;
+  }
+  if (lse_out && lane == 0) lse_out[(size_t)b * rows + row] = L;
+}
+
+}  // namespace
+
+cudaError_t launch_plan(const int32_t* seq_lens, const int32_t* block_table, WsHeader* ws, int B,
+                        int Lq, int max_pages, int num_pages, int units, cudaStream_t st) {
+  plan_kernel<<<1, 1024, 0, st>>>(seq_lens, block_table, ws, B, Lq, max_pages, num_pages, units);
+  return cudaGetLastError();
+}
+
+static cudaError_t decode_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, int units,
+                                 int csize, cudaStream_t st) {
+  static int configured_dev = -1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (configured_dev != dev) {  // attribute is per device; set it again on a new one
+    e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecodeSmem);
+    if (e != cudaSuccess) return e;
+    configured_dev = dev;
+  }
+  cfg = cudaLaunchConfig_t{};
+  cfg.gridDim = dim3(units * csize);
+  cfg.blockDim = dim3(kDecodeThreads);
+  cfg.dynamicSmemBytes = kDecodeSmem;
+  cfg.stream = st;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = csize;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaSuccess;
+}
+
+int decode_max_units(int csize, int* units) {
+  static int cache_dev[2] = {-1, -1}, cache_val[2] = {0, 0};
+  const int slot = csize == 2 ? 0 : 1;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_CUDA;
+  if (cache_dev[slot] == dev) {
+    *units = cache_val[slot];
+    return MLA_OK;
+  }
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[1];
+  if (decode_config(cfg, attr, 1, csize, nullptr) != cudaSuccess) return MLA_ERR_CUDA;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, decode_kernel, &cfg) != cudaSuccess || n < 1) return MLA_ERR_CUDA;
+  cache_dev[slot] = dev;
+  cache_val[slot] = n;
+  *units = n;
+  return MLA_OK;
+}
+
+cudaError_t launch_decode(const CUtensorMap& tm_cache, const DecodeArgs& a, int units, int csize,
+                          cudaStream_t st) {
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[1];
+  cudaError_t e = decode_config(cfg, attr, units, csize, st);
+  if (e != cudaSuccess) return e;
+  return cudaLaunchKernelEx(&cfg, decode_kernel, tm_cache, a);
+}
+
+cudaError_t launch_combine(const float* o_part, const float* lse_part, const WsHeader* ws, void* o_lat,
+                           float* lse, int B, int Lq, int H, int G, cudaStream_t st) {
+  const int warps = B * Lq * H;
+  dim3 grid((warps + 7) / 8), block(256);
+  auto* ol = static_cast<__nv_bfloat16*>(o_lat);
+  if (G == 1) combine_kernel<512><<<grid, block, 0, st>>>(o_part, lse_part, ws, ol, lse, B, Lq, H, G);
+  else combine_kernel<256><<<grid, block, 0, st>>>(o_part, lse_part, ws, ol, lse, B, Lq, H, G);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

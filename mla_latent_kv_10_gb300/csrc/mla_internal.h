@@ -1,0 +1,61 @@
+// mla_internal.h — declarations shared by the kernels and the C-ABI layer.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "../../include/mla.h"
+
+namespace mla {
+
+constexpr int kPage = 64;      // tokens per cache page
+constexpr int kDc = 512;       // latent width (all groups)
+constexpr int kDr = 64;        // RoPE key width
+constexpr int kRow = kDc + kDr;  // 576 elements per cache row
+constexpr int kDhc = 128;      // content head dim
+constexpr int kRowsPerCta = 128;  // query rows (l, h) per CTA = MMA M
+
+// Decode workspace: header, then int off[B+1] (page offsets of each sequence
+// in the flattened page order, off[B] = total pages) and int nlen[B] (the
+// validated sequence lengths).
+struct WsHeader {
+  int status;    // sticky device status (mla_status), 0 = ok
+  int total;     // total pages over all sequences
+  int chunk;     // pages per work unit
+  int units;     // work units (CTA clusters) of the last launch
+  int B;
+  int pad[3];
+};
+static_assert(sizeof(WsHeader) == 32, "header layout");
+
+inline size_t ws_bytes_for(int B) {
+  size_t b = sizeof(WsHeader) + sizeof(int) * (size_t)(2 * B + 1);
+  return (b + 255) & ~(size_t)255;
+}
+
+struct DecodeArgs {
+  const __nv_bfloat16* q_cat;
+  const int32_t* block_table;
+  float* o_part;
+  float* lse_part;
+  WsHeader* ws;
+  int B, Lq, H, G, d_g, max_pages, num_pages, causal, rows;  // rows = Lq*H
+  float scale_log2;   // scale * log2(e)
+};
+
+// launchers (return cudaError_t of the launch)
+cudaError_t launch_absorb(const CUtensorMap& tmA, const CUtensorMap& tmB, const void* q_rope,
+                          void* q_cat, int M, int H, int d_g, cudaStream_t st);
+cudaError_t launch_project(const CUtensorMap& tmA, const CUtensorMap& tmB, void* out, int M, int H,
+                           int d_g, cudaStream_t st);
+cudaError_t launch_plan(const int32_t* seq_lens, const int32_t* block_table, WsHeader* ws, int B,
+                        int Lq, int max_pages, int num_pages, int units, cudaStream_t st);
+cudaError_t launch_decode(const CUtensorMap& tm_cache, const DecodeArgs& a, int units, int csize,
+                          cudaStream_t st);
+cudaError_t launch_combine(const float* o_part, const float* lse_part, const WsHeader* ws,
+                           void* o_lat, float* lse, int B, int Lq, int H, int G, cudaStream_t st);
+int decode_max_units(int csize, int* units);  // clusters of csize CTAs resident at once
+
+}  // namespace mla

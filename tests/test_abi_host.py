@@ -1,0 +1,113 @@
+"""Host-only checks of the C ABI: the library builds, loads without a GPU,
+exports every function include/mla.h declares, and rejects bad arguments
+with the documented status codes before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import mla_latent_kv_10_gb300 as mla
+from mla_latent_kv_10_gb300 import _build
+from mla_latent_kv_10_gb300.inputs import workload
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mla.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return mla.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mla_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("mla_absorb_q", "mla_decode_paged", "mla_combine_splits", "mla_project_uv",
+              "mla_decode_workspace_size", "mla_get_device_status", "mla_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    assert mla.mla_status_string(0) == "MLA_OK"
+    assert mla.mla_status_string(-7) == "MLA_ERR_TIMEOUT"
+    assert mla.mla_status_string(-6) == "MLA_ERR_BAD_TABLE"
+    assert mla.mla_status_string(123) == "MLA_ERR_UNKNOWN"
+
+
+def dims(**kw):
+    d = dict(workload("tiny").dims)
+    d.update(kw)
+    return mla.make_dims(d)
+
+
+P = ctypes.c_void_p
+A16 = P(0x10000)      # aligned fake device addresses (never dereferenced)
+A8 = P(0x10008)
+
+
+def decode(lib, d, q=A16, cache=A16, bt=A16, sl=A16, splits=0, op=A16, lp=A16, ws=A16, wsb=4096):
+    return lib.mla_decode_paged(ctypes.byref(d), q, cache, bt, sl, splits, op, lp, ws, wsb, None)
+
+
+def test_decode_rejects_bad_arguments(lib):
+    d = dims()
+    assert lib.mla_decode_paged(None, A16, A16, A16, A16, 0, A16, A16, A16, 4096, None) == -1
+    assert decode(lib, d, q=None) == -1
+    assert decode(lib, d, bt=None) == -1
+    assert decode(lib, d, splits=-1) == -1
+    assert decode(lib, d, ws=None) == -4
+    assert decode(lib, d, wsb=8) == -4
+    assert decode(lib, d, cache=A8) == -3
+    assert decode(lib, d, q=A8) == -3
+    assert decode(lib, d, op=A8) == -3
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("d_hc", 64, -2), ("d_c", 256, -2), ("d_R", 32, -2), ("page_size", 16, -2),
+    ("G", 4, -2), ("Lq", 3, -2), ("H", 24, -2), ("H", 256, -2),
+    ("B", 0, -1), ("num_pages", 0, -1), ("scale", 0.0, -1), ("scale", float("nan"), -1),
+    ("max_pages_per_seq", 0, -1)])
+def test_unsupported_or_invalid_dims(lib, field, value, code):
+    d = dims()
+    setattr(d, field, value)
+    assert decode(lib, d) == code
+    assert lib.mla_absorb_q(ctypes.byref(d), A16, A16, A16, A16, None) == code
+    assert lib.mla_project_uv(ctypes.byref(d), A16, A16, A16, None) == code
+    n = ctypes.c_size_t()
+    assert lib.mla_decode_workspace_size(ctypes.byref(d), ctypes.byref(n)) == code
+
+
+def test_gemm_entry_points_check_pointers(lib):
+    d = dims()
+    assert lib.mla_absorb_q(ctypes.byref(d), None, A16, A16, A16, None) == -1
+    assert lib.mla_absorb_q(ctypes.byref(d), A16, A16, A8, A16, None) == -3
+    assert lib.mla_project_uv(ctypes.byref(d), A16, None, A16, None) == -1
+    assert lib.mla_project_uv(ctypes.byref(d), A16, A16, A8, None) == -3
+    assert lib.mla_combine_splits(ctypes.byref(d), A16, A16, None, 4096, A16, None, None) == -4
+    assert lib.mla_combine_splits(ctypes.byref(d), None, A16, A16, 4096, A16, None, None) == -1
+    assert lib.mla_get_device_status(None, None) == -1
+
+
+def test_workspace_size_grows_with_batch(lib):
+    a = mla.mla_decode_workspace_size(dims(B=2))
+    b = mla.mla_decode_workspace_size(dims(B=5000))
+    assert a >= 32 + 4 * 5 and a % 256 == 0
+    assert b >= 32 + 4 * 10001 and b > a
+
+
+def test_python_binding_raises_mla_error(lib):
+    with pytest.raises(mla.MLAError) as e:
+        mla.mla_decode_workspace_size(dims(G=3))
+    assert e.value.code == -2
