@@ -14,10 +14,13 @@
 //     tensor-memory columns of an SM, so each 128-row block runs on a CTA
 //     PAIR (cluster rank bit 0 = r): CTA r owns latent half r (256 columns of
 //     O) and loads only its half of each page (CTA 0 also loads the RoPE
-//     columns).  Each CTA computes a partial score tile over its columns;
-//     the two partials are swapped through distributed shared memory and
-//     summed, so both CTAs hold the same fp32 scores and run the same online
-//     softmax, bit for bit.
+//     columns).  Each CTA computes a partial score tile over its columns, in
+//     log2 units, rounds it to fp16 and sends it to the peer with one bulk
+//     shared-to-shared copy (16 KiB per page); both CTAs add the same two
+//     fp16 partials, so they hold bit-identical scores and run the same
+//     online softmax.  The exchange is double-buffered and the softmax warps
+//     run one page behind the exchange, so the copy of page q overlaps the
+//     softmax of page q-1.
 //   * Tensor memory per CTA: O (256 cols) | Q (<=160 cols, bf16 pairs, the
 //     MMA A operand) | S (64 cols) | P (32 cols, bf16 pairs, A operand of
 //     the P.V MMA).  The page tile in shared memory is used twice: K-major as
@@ -25,7 +28,9 @@
 //   * Pages arrive by TMA (64 x 64 bf16 boxes, 128-byte swizzle) into a
 //     4-stage mbarrier ring; one thread issues MMAs, one thread issues copies,
 //     four warps (one TMEM lane quadrant each, one thread per query row) do
-//     the exchange, masking, online softmax and epilogue.
+//     the exchange, masking, online softmax and epilogue.  Rescaling of O
+//     after a new row maximum is deferred until the maximum has grown by
+//     2^8 (log2 units), so it is rare.
 //   * Split-KV: the pages of all sequences, in order, are cut into equal
 //     contiguous ranges, one per cluster; a range that covers parts of several
 //     sequences yields one partial (o, lse) per sequence, stored in slot
@@ -45,10 +50,12 @@ namespace {
 constexpr int kStages = 4;
 constexpr int kBoxBytes = kPage * 64 * 2;       // 64 tokens x 64 bf16 = 8 KiB
 constexpr int kStageBytes = 5 * kBoxBytes;      // latent half (4 boxes) + RoPE box
-constexpr int kXBytes = kRowsPerCta * 64 * 4;   // one fp32 score tile, 32 KiB
-constexpr int kDecodeSmem = 1024 + kStages * kStageBytes + 2 * kXBytes;
-constexpr int kDecodeThreads = 192;             // 4 softmax warps, TMA warp, MMA warp
-constexpr uint32_t kColO = 0, kColQ = 256, kColS = 416, kColP = 480, kTmemCols = 512;
+constexpr int kXSlot = kRowsPerCta * 64 * 2;    // one fp16 partial-score tile, 16 KiB
+constexpr int kSmemShared = kStages * kStageBytes + 4 * kXSlot;  // offset of DecodeShared (2 send + 2 receive slots before it)
+constexpr int kSoftmaxThreads = 256;            // 8 softmax warps, two per TMEM lane quadrant
+constexpr int kTmaWarp = 8, kMmaWarp = 9;
+constexpr int kDecodeThreads = kSoftmaxThreads + 64;
+constexpr uint32_t kColO = 0, kColQ = 256, kColS = 416, kColP = 480, kTmemCols = 512;  // Q uses 144 columns
 constexpr float kRescaleThreshold = 8.0f;       // log2 units: defer O rescaling up to 2^8
 
 __device__ __forceinline__ float ex2(float x) {
@@ -64,6 +71,41 @@ __device__ __forceinline__ float lg2(float x) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+__device__ __forceinline__ uint32_t pack_f16x2_sat(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ float2 unpack_f16x2(uint32_t w) {
+  float2 f;
+  asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
+      : "=f"(f.x), "=f"(f.y) : "r"(w));
+  return f;
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+__device__ __forceinline__ void ld_shared_v4(uint32_t addr, uint32_t& a, uint32_t& b, uint32_t& c, uint32_t& d) {
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(a), "=r"(b), "=r"(c), "=r"(d) : "r"(addr) : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// Copy `bytes` of this CTA's shared memory into another CTA of the cluster;
+// completion is counted in bytes on the destination CTA's mbarrier.
+__device__ __forceinline__ void bulk_s2s(uint32_t dst_cluster, uint32_t src, uint32_t bytes, uint32_t bar_cluster) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(dst_cluster), "r"(src), "r"(bytes), "r"(bar_cluster) : "memory");
+}
+// Named barrier `id` over `n` threads with an AND vote: every thread learns
+// whether all of them are still ok (so none is left waiting alone).
+__device__ __forceinline__ bool bar_red_and_n(bool ok, uint32_t id, uint32_t n) {
+  uint32_t r;
+  asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\tbar.red.and.pred p, %2, %3, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+               : "=r"(r) : "r"((uint32_t)ok), "r"(id), "r"(n) : "memory");
+  return r != 0;
+}
+
 __device__ __forceinline__ void set_status(WsHeader* ws, int code) {
   atomicCAS(&ws->status, 0, code);
 }
@@ -73,9 +115,15 @@ struct DecodeShared {
   uint64_t full[kStages], empty[kStages];
   uint64_t q_full, s_full, s_free, p_full, o_done, drain;
   uint64_t xfull[2], xfree[2];
+  float pmax[2][kRowsPerCta];   // [column half][row]: half-row maxima of the current page
+  float lpart[2][kRowsPerCta];  // [column half][row]: half-row sums at the epilogue
   uint32_t tmem;
   int abort;
 };
+
+// All shared memory is dynamic: stage ring, exchange slots, then the small state.
+constexpr int kDecodeSmem = kSmemShared + (int)((sizeof(DecodeShared) + 15) & ~size_t(15));
+static_assert(kDecodeSmem <= 232448, "decode kernel exceeds 227 KiB of shared memory");
 
 // Walks the (sequence, page range) segments of one work unit.
 struct SegIter {
@@ -115,13 +163,18 @@ struct SegIter {
 
 __global__ void __launch_bounds__(kDecodeThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tm_cache, const DecodeArgs a) {
-  extern __shared__ uint8_t smem_raw[];
-  __shared__ DecodeShared sh;
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* stages = smem;
-  float* xbuf = reinterpret_cast<float*>(smem + kStages * kStageBytes);
+  uint8_t* xbuf = smem + kStages * kStageBytes;  // [send 2][receive 2] x 16 KiB
+  DecodeShared& sh = *reinterpret_cast<DecodeShared*>(smem + kSmemShared);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // 128-byte-swizzled tiles need a 1024-byte aligned base; the whole cluster
+  // sees the same layout, so every CTA takes this exit together.
+  if (smem_u32(smem) & 1023u) {
+    if (threadIdx.x == 0) set_status(a.ws, MLA_ERR_UNSUPPORTED);
+    return;
+  }
   const uint32_t crank = cluster_ctarank();
   const uint32_t r = crank & 1u;         // latent half owned by this CTA
   const uint32_t rg = crank >> 1;        // 128-row block of the query rows
@@ -138,20 +191,21 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       mbar_init(bar(sh.full[s]), 1);
       mbar_init(bar(sh.empty[s]), 1);
     }
-    mbar_init(bar(sh.q_full), 128);
+    mbar_init(bar(sh.q_full), kSoftmaxThreads);
     mbar_init(bar(sh.s_full), 1);
-    mbar_init(bar(sh.s_free), 128);
-    mbar_init(bar(sh.p_full), 128);
+    mbar_init(bar(sh.s_free), kSoftmaxThreads);
+    mbar_init(bar(sh.p_full), kSoftmaxThreads);
     mbar_init(bar(sh.o_done), 1);
     mbar_init(bar(sh.drain), 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(sh.xfull[s]), 128);
-      mbar_init(bar(sh.xfree[s]), 128);
+      mbar_init(bar(sh.xfull[s]), 1);                  // armed with the expected bytes, completed by the peer's copy
+      mbar_init(bar(sh.xfree[s]), kSoftmaxThreads / 32);  // every softmax warp of the peer consumed its part
     }
     fence_mbar_init();
+    for (int s = 0; s < 2; ++s) mbar_arrive_expect_tx(bar(sh.xfull[s]), kXSlot);
     tma_prefetch_desc(&tm_cache);
   }
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(&sh.tmem), kTmemCols);
     tmem_relinquish();
   }
@@ -167,11 +221,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     set_status(ws, MLA_ERR_TIMEOUT);
   };
 
-  if (warp == 4) {
+  if (warp == kTmaWarp) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      const int nbox = (r == 0) ? 5 : 4;
-      const uint32_t bytes = nbox * kBoxBytes;
+      const uint32_t bytes = 5 * kBoxBytes;
       const uint64_t policy = l2_policy_evict_first();
       SegIter it;
       it.init(ws, unit);
@@ -190,11 +243,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           if (page < 0 || page >= a.num_pages) page = 0;  // reported by the plan kernel
           const uint32_t dst = smem_u32(stages + st * kStageBytes);
           mbar_arrive_expect_tx(bar(sh.full[st]), bytes);
-          for (int j = 0; j < 4; ++j)
+          for (int j = 0; j < 4; ++j)  // this CTA's latent half
             tma_load_2d_hint(dst + j * kBoxBytes, &tm_cache, bar(sh.full[st]), (int)(r * 256 + j * 64),
                              page * kPage, policy);
-          if (r == 0)
-            tma_load_2d_hint(dst + 4 * kBoxBytes, &tm_cache, bar(sh.full[st]), kDc, page * kPage, policy);
+          // RoPE box (each CTA uses 32 of its 64 columns)
+          tma_load_2d_hint(dst + 4 * kBoxBytes, &tm_cache, bar(sh.full[st]), kDc, page * kPage, policy);
         }
       }
       // Copies still in flight must land before this CTA may exit.
@@ -203,10 +256,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           mbar_wait(bar(sh.full[k % kStages]), (k / kStages) & 1, abort, 100000000ull);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const int nk = (r == 0) ? 20 : 16;  // K steps of 16 for the score MMA
+      constexpr int nk = 18;  // K steps of 16: 16 over the latent half + 2 over half the RoPE columns
       constexpr uint32_t idesc_qk = idesc_bf16(128, 64, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16(128, 256, false, true);
       SegIter it;
@@ -217,62 +270,210 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       auto issue_pv = [&](uint32_t q, bool acc) -> bool {
         if (!mbar_wait(bar(sh.p_full), q & 1, abort)) return false;
         tc_fence_after();
-        const uint32_t base = smem_u32(stages + (q % kStages) * kStageBytes);
+        const uint64_t vd0 = sdesc_sw128(smem_u32(stages + (q % kStages) * kStageBytes), kBoxBytes, 1024);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {  // 64 tokens = 4 K steps
-          const uint64_t vd = sdesc_sw128(base + kk * 2048, kBoxBytes, 1024);
+          const uint64_t vd = vd0 + (uint64_t)((kk * 2048) >> 4);
           mma_ts(tmem + kColO, tmem + kColP + kk * 8, vd, idesc_pv, (acc || kk > 0) ? 1u : 0u);
         }
         mma_commit(bar(sh.empty[q % kStages]));
         mma_commit(bar(sh.o_done));
         return true;
       };
+      // Issue order QK(q), PV(q-2): the softmax warps work one page behind
+      // the score MMAs, so P(q-2) is ready once S(q) may be overwritten.
       while (ok && it.next(sb, pa, pb)) {
         if (!(ok = mbar_wait(bar(sh.q_full), qc & 1, abort))) break;
         ++qc;
         tc_fence_after();
+        const uint32_t p0 = pc;  // global index of page pa
         for (int i = pa; i < pb; ++i, ++pc) {
           const int st = pc % kStages;
           if (!(ok = mbar_wait(bar(sh.full[st]), (pc / kStages) & 1, abort))) break;
           if (pc > 0 && !(ok = mbar_wait(bar(sh.s_free), (pc - 1) & 1, abort))) break;
           tc_fence_after();
-          const uint32_t base = smem_u32(stages + st * kStageBytes);
+          const uint64_t kd0 = sdesc_sw128(smem_u32(stages + st * kStageBytes), 16, 1024);
+#pragma unroll
           for (int kk = 0; kk < nk; ++kk) {
-            const uint64_t kd = sdesc_sw128(base + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024);
-            mma_ts(tmem + kColS, tmem + kColQ + kk * 8, kd, idesc_qk, kk > 0 ? 1u : 0u);
+            // latent K steps walk boxes 0..3; the last two take this CTA's
+            // 32 RoPE columns from box 4
+            const uint32_t off = kk < 16 ? (kk >> 2) * kBoxBytes + (kk & 3) * 32
+                                         : 4 * kBoxBytes + (r * 2 + (kk - 16)) * 32;
+            mma_ts(tmem + kColS, tmem + kColQ + kk * 8, kd0 + (uint64_t)(off >> 4), idesc_qk, kk > 0 ? 1u : 0u);
           }
           mma_commit(bar(sh.s_full));
-          if (i > pa && !(ok = issue_pv(pc - 1, i - 1 > pa))) break;
+          if (i - 2 >= pa && !(ok = issue_pv(pc - 2, i - 2 > pa))) break;
         }
         if (!ok) break;
-        if (!(ok = issue_pv(pc - 1, pb - 1 > pa))) break;
+        for (int i = max(pa, pb - 2); i < pb; ++i)
+          if (!(ok = issue_pv(p0 + (uint32_t)(i - pa), i > pa))) break;
       }
       if (!ok) fail();
     }
   } else {
     // ------------------------------------------------------------ softmax warps
-    const int row = threadIdx.x;                 // TMEM lane = query row in this block
+    // Two warps per TMEM lane quadrant: warp w and w+4 share query rows and
+    // split each page's 64 key columns (half = warp / 4).  Software-pipelined
+    // by one page: while the partial scores of page q travel to the peer, the
+    // softmax of page q-1 runs.
+    const int quad = warp & 3, half = warp >> 2;
+    const int row = quad * 32 + lane;              // TMEM lane = query row in this block
     const int grow = (int)rg * kRowsPerCta + row;  // row of the (l, h) list
     const bool valid = grow < a.rows;
     const int l = valid ? grow / a.H : 0;
     const int h = valid ? grow % a.H : 0;
     const int g = (h * a.G) / a.H;
-    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-    const uint32_t peer_x = mapa(smem_u32(xbuf), peer);
+    const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+    const uint32_t xsrc = smem_u32(xbuf), xrecv = xsrc + 2 * kXSlot;
+    const uint32_t peer_recv = mapa(xrecv, peer);
     const uint32_t peer_xfull0 = mapa(bar(sh.xfull[0]), peer), peer_xfull1 = mapa(bar(sh.xfull[1]), peer);
     const uint32_t peer_xfree0 = mapa(bar(sh.xfree[0]), peer), peer_xfree1 = mapa(bar(sh.xfree[1]), peer);
+    const uint32_t xrow = row * 128;
+    const uint32_t pair_bar = 2 + quad;  // named barrier of warps quad and quad+4
     const int d_q = a.d_g + kDr;
+    const bool sender = threadIdx.x == 32 * 4 + 1;  // issues the bulk copies, no remote arrives
     SegIter it;
     it.init(ws, unit);
     int sb, pa, pb;
     uint32_t pc = 0, od = 0;
     bool ok = true;
-    while (ok && it.next(sb, pa, pb)) {
+    float m_used = -INFINITY, l_part = 0.f;
+    int limit = 0;
+
+    // (a) page q: this thread's 32 partial scores TMEM -> fp16 (log2 units)
+    // -> local send slot
+    auto stage_a = [&](uint32_t q) {
+      if (ok) ok = mbar_wait(bar(sh.s_full), q & 1, abort);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) return;
+      tc_fence_after();
+      uint32_t w[16];
+      {
+        uint32_t v[32];
+        tmem_ld32(lane_base + kColS + 32 * half, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          w[j] = pack_f16x2_sat(__uint_as_float(v[2 * j]) * a.scale_log2, __uint_as_float(v[2 * j + 1]) * a.scale_log2);
+      }
+      tc_fence_before();
+      mbar_arrive(bar(sh.s_free));
+      const uint32_t slot = q & 1, use = q >> 1;
+      if (use > 0) ok = mbar_wait<true>(bar(sh.xfree[slot]), (use - 1) & 1, abort);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) return;
+      const uint32_t dst = xsrc + slot * kXSlot + xrow;
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        st_shared_v4(dst + (((4 * half + c) ^ (row & 7)) << 4), w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+      fence_proxy_async();
+    };
+
+    // wait until the peer's partial of page q has landed in our receive slot
+    auto recv_wait = [&](uint32_t q) {
+      if (ok) ok = mbar_wait<true>(bar(sh.xfull[q & 1]), (q >> 1) & 1, abort);
+      ok = __all_sync(0xffffffffu, ok);
+    };
+
+    // (b) page q (= page i of the sequence): scores = own + peer partial
+    // (both fp16-rounded, so the two CTAs add identical values), mask,
+    // online softmax over this thread's 32 columns (row maximum shared with
+    // the partner warp), P -> tensor memory
+    auto stage_b = [&](uint32_t q, int i, bool first) {
+      if (!ok) return;
+      float s[32];
+      {
+        const uint32_t off = (q & 1) * kXSlot + xrow;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o[4], p[4];
+          const uint32_t sw = ((4 * half + c) ^ (row & 7)) << 4;
+          ld_shared_v4(xsrc + off + sw, o[0], o[1], o[2], o[3]);
+          ld_shared_v4(xrecv + off + sw, p[0], p[1], p[2], p[3]);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float2 x = unpack_f16x2(o[k]), y = unpack_f16x2(p[k]);
+            s[8 * c + 2 * k] = x.x + y.x;
+            s[8 * c + 2 * k + 1] = x.y + y.y;
+          }
+        }
+      }
+      // this warp's part of the receive slot is read (every loaded value is
+      // already consumed above): hand it back, after re-arming the slot for
+      // its next use (once per CTA)
+      __syncwarp();
+      if (lane == 0) {
+        if (warp == 0) mbar_arrive_expect_tx(bar(sh.xfull[q & 1]), kXSlot);
+        mbar_arrive_remote_relaxed((q & 1) ? peer_xfree1 : peer_xfree0);
+      }
+      const int key0 = i * kPage + 32 * half;
+      float mt = -INFINITY;
+      if (limit < i * kPage + kPage) {  // page holds keys this row may not see
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float v = (key0 + j < limit) ? s[j] : -INFINITY;
+          s[j] = v;
+          mt = fmaxf(mt, v);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) mt = fmaxf(mt, s[j]);
+      }
+      sh.pmax[half][row] = mt;
+      ok = bar_red_and_n(ok, pair_bar, 64);
+      if (!ok) return;
+      mt = fmaxf(mt, sh.pmax[half ^ 1][row]);
+      const bool need = mt > m_used + kRescaleThreshold;
+      if (!first) {  // P.V of the previous page done: P and O are ours
+        ok = mbar_wait(bar(sh.o_done), od & 1, abort);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) return;
+        ++od;
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, need)) {
+          const float f = need ? ex2(m_used - mt) : 1.0f;
+          for (int c = 0; c < 4; ++c) {
+            uint32_t v[32];
+            const uint32_t col = lane_base + kColO + 128 * half + c * 32;
+            tmem_ld32(col, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * f);
+            tmem_st32(col, v);
+          }
+          l_part *= f;
+        }
+      }
+      if (need) m_used = mt;
+      const float base = (m_used == -INFINITY) ? 0.f : m_used;
+      uint32_t pk[16];
+      float psum = 0.f;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const uint32_t w = pack_bf16x2(ex2(s[2 * j] - base), ex2(s[2 * j + 1] - base));
+        psum += bf16_lo(w) + bf16_hi(w);
+        pk[j] = w;
+      }
+      l_part += psum;
+      tmem_st16(lane_base + kColP + 16 * half, pk);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(sh.p_full));
+    };
+
+    // Control flow leaves this loop only right after a vote of all softmax
+    // threads (bar_red_and_n), so no thread is ever left waiting at a named
+    // barrier for a warp that gave up.
+    while (it.next(sb, pa, pb)) {
       const int seg = sb + unit;
       const int n = nlen[sb];
-      const int limit = a.causal ? n - a.Lq + l + 1 : n;  // keys [0, limit) visible
+      limit = a.causal ? n - a.Lq + l + 1 : n;  // keys [0, limit) visible
+      m_used = -INFINITY;
+      l_part = 0.f;
 
-      // ---- load this CTA's slice of the query row into tensor memory
+      // ---- load this CTA's slice of the query row into tensor memory:
+      // 4 chunks of 64 latent columns (half 0: chunks 0-1 and the 32 RoPE
+      // columns this CTA multiplies; half 1: chunks 2-3)
       {
         const __nv_bfloat16* qrow = a.q_cat + ((size_t)(sb * a.Lq + l) * a.H + h) * d_q;
         const uint4* lat = nullptr;
@@ -280,10 +481,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           if (a.G == 1) lat = reinterpret_cast<const uint4*>(qrow + r * 256);
           else if ((uint32_t)g == r) lat = reinterpret_cast<const uint4*>(qrow);
         }
-        const uint4* rope = valid ? reinterpret_cast<const uint4*>(qrow + a.d_g) : nullptr;
-        const int nchunk = (r == 0) ? 5 : 4;
-        for (int c = 0; c < nchunk; ++c) {
-          const uint4* src = (c < 4) ? (lat ? lat + c * 8 : nullptr) : rope;
+        for (int c = 2 * half; c < 2 * half + 2; ++c) {
+          const uint4* src = lat ? lat + c * 8 : nullptr;
           uint32_t w[32];
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
@@ -292,133 +491,81 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           }
           tmem_st32(lane_base + kColQ + c * 32, w);
         }
+        if (half == 0) {
+          const uint4* rope = valid ? reinterpret_cast<const uint4*>(qrow + a.d_g + 32 * r) : nullptr;
+          uint32_t w[16];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4 v = rope ? rope[q] : make_uint4(0, 0, 0, 0);
+            w[4 * q + 0] = v.x; w[4 * q + 1] = v.y; w[4 * q + 2] = v.z; w[4 * q + 3] = v.w;
+          }
+          tmem_st16(lane_base + kColQ + 128, w);
+        }
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar(sh.q_full));
       }
 
-      float m_used = -INFINITY, l_sum = 0.f;
-      for (int i = pa; i < pb; ++i, ++pc) {
-        // ---- partial scores of this CTA's columns
-        ok = mbar_wait(bar(sh.s_full), pc & 1, abort);
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        tc_fence_after();
-        float s[64];
-        {
-          uint32_t v[32];
-          tmem_ld32(lane_base + kColS, v);
-          tmem_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 32; ++j) s[j] = __uint_as_float(v[j]);
-          tmem_ld32(lane_base + kColS + 32, v);
-          tmem_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 32; ++j) s[32 + j] = __uint_as_float(v[j]);
-        }
-        tc_fence_before();
-        mbar_arrive(bar(sh.s_free));
-
-        // ---- swap partials with the peer CTA (slot alternates per page)
-        const uint32_t slot = pc & 1, use = pc >> 1;
-        if (use > 0) {
-          ok = mbar_wait<true>(bar(sh.xfree[slot]), (use - 1) & 1, abort);
-          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        }
-        const uint32_t xrow = slot * kXBytes + row * 256;
-#pragma unroll
-        for (int c = 0; c < 16; ++c)
-          st_cluster_v4(peer_x + xrow + ((c ^ (row & 15)) << 4),
-                        make_float4(s[4 * c], s[4 * c + 1], s[4 * c + 2], s[4 * c + 3]));
-        mbar_arrive_remote(slot ? peer_xfull1 : peer_xfull0);
-        ok = mbar_wait<true>(bar(sh.xfull[slot]), use & 1, abort);
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        {
-          const float* mine = reinterpret_cast<const float*>(reinterpret_cast<const uint8_t*>(xbuf) + xrow);
-#pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const float4 t = *reinterpret_cast<const float4*>(mine + 4 * (c ^ (row & 15)));
-            s[4 * c] += t.x; s[4 * c + 1] += t.y; s[4 * c + 2] += t.z; s[4 * c + 3] += t.w;
-          }
-        }
-        mbar_arrive_remote(slot ? peer_xfree1 : peer_xfree0);
-
-        // ---- mask, scale to log2 units, tile max
-        const int key0 = i * kPage;
-        float mt = -INFINITY;
-#pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          const float v = (key0 + j < limit) ? s[j] * a.scale_log2 : -INFINITY;
-          s[j] = v;
-          mt = fmaxf(mt, v);
-        }
-        const bool need = mt > m_used + kRescaleThreshold;
-        const bool first = (i == pa);
-        if (!first) {  // P.V of the previous page done: P and O are ours
-          ok = mbar_wait(bar(sh.o_done), od & 1, abort);
-          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-          ++od;
-          tc_fence_after();
-          if (__any_sync(0xffffffffu, need)) {
-            const float f = need ? ex2(m_used - mt) : 1.0f;
-            for (int c = 0; c < 8; ++c) {
-              uint32_t v[32];
-              tmem_ld32(lane_base + kColO + c * 32, v);
-              tmem_wait_ld();
-#pragma unroll
-              for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * f);
-              tmem_st32(lane_base + kColO + c * 32, v);
-            }
-            l_sum *= f;
-          }
-        }
-        if (need) m_used = mt;
-        const float base = (m_used == -INFINITY) ? 0.f : m_used;
-        uint32_t pk[32];
-        float psum = 0.f;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const uint32_t w = pack_bf16x2(ex2(s[2 * j] - base), ex2(s[2 * j + 1] - base));
-          psum += bf16_lo(w) + bf16_hi(w);
-          pk[j] = w;
-        }
-        l_sum += psum;
-        tmem_st32(lane_base + kColP, pk);
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(bar(sh.p_full));
-      }
+      // ---- pages, one-page software pipeline
+      stage_a(pc);
+      ok = bar_red_and_n(ok, 1, kSoftmaxThreads);
       if (!ok) break;
+      if (sender) bulk_s2s(peer_recv + (pc & 1) * kXSlot, xsrc + (pc & 1) * kXSlot, kXSlot, (pc & 1) ? peer_xfull1 : peer_xfull0);
+      bool go = true;
+      for (int i = pa + 1; i < pb; ++i) {
+        const uint32_t q = pc + (uint32_t)(i - pa);
+        stage_a(q);
+        ok = bar_red_and_n(ok, 1, kSoftmaxThreads);
+        if (!ok) { go = false; break; }
+        if (sender) bulk_s2s(peer_recv + (q & 1) * kXSlot, xsrc + (q & 1) * kXSlot, kXSlot, (q & 1) ? peer_xfull1 : peer_xfull0);
+        recv_wait(q - 1);
+        stage_b(q - 1, i - 1, i - 1 == pa);
+        ok = bar_red_and_n(ok, pair_bar, 64);  // partner done with pmax; pair in step on failure
+        if (!ok) { go = false; break; }
+      }
+      if (!go) break;
+      const uint32_t qe = pc + (uint32_t)(pb - 1 - pa);
+      recv_wait(qe);
+      stage_b(qe, pb - 1, pb - 1 == pa);
+      pc += (uint32_t)(pb - pa);
 
       // ---- epilogue: normalised latent partial and log-sum-exp
-      ok = mbar_wait(bar(sh.o_done), od & 1, abort);
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      if (ok) ok = mbar_wait(bar(sh.o_done), od & 1, abort);
+      ok = __all_sync(0xffffffffu, ok);
       ++od;
-      tc_fence_after();
-      const float inv = l_sum > 0.f ? 1.0f / l_sum : 0.f;
-      float* dst = a.o_part + ((size_t)seg * a.rows + grow) * kDc + r * 256;
-      for (int c = 0; c < 8; ++c) {
-        uint32_t v[32];
-        tmem_ld32(lane_base + kColO + c * 32, v);
-        tmem_wait_ld();
-        if (valid) {
-          float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
+      sh.lpart[half][row] = l_part;
+      ok = bar_red_and_n(ok, pair_bar, 64);
+      if (ok) {
+        tc_fence_after();
+        const float l_sum = l_part + sh.lpart[half ^ 1][row];
+        const float inv = l_sum > 0.f ? 1.0f / l_sum : 0.f;
+        float* dst = a.o_part + ((size_t)seg * a.rows + grow) * kDc + r * 256 + half * 128;
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tmem_ld32(lane_base + kColO + 128 * half + c * 32, v);
+          tmem_wait_ld();
+          if (valid) {
+            float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
 #pragma unroll
-          for (int q = 0; q < 8; ++q)
-            d4[q] = make_float4(__uint_as_float(v[4 * q]) * inv, __uint_as_float(v[4 * q + 1]) * inv,
-                                __uint_as_float(v[4 * q + 2]) * inv, __uint_as_float(v[4 * q + 3]) * inv);
+            for (int q = 0; q < 8; ++q)
+              d4[q] = make_float4(__uint_as_float(v[4 * q]) * inv, __uint_as_float(v[4 * q + 1]) * inv,
+                                  __uint_as_float(v[4 * q + 2]) * inv, __uint_as_float(v[4 * q + 3]) * inv);
+          }
         }
+        if (valid && r == 0 && half == 0)
+          a.lse_part[(size_t)seg * a.rows + grow] =
+              l_sum > 0.f ? (m_used + lg2(l_sum)) * 0.69314718055994531f : -INFINITY;
+        tc_fence_before();
       }
-      if (valid && r == 0)
-        a.lse_part[(size_t)seg * a.rows + grow] =
-            l_sum > 0.f ? (m_used + lg2(l_sum)) * 0.69314718055994531f : -INFINITY;
-      tc_fence_before();
+      ok = bar_red_and_n(ok, 1, kSoftmaxThreads);
+      if (!ok) break;
     }
     if (!ok) fail();
   }
 
   // ------------------------------------------------------------ teardown
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     if (*abort) {  // let MMAs already issued finish before freeing their memory
       if (lane == 0) {
         mma_commit(bar(sh.drain));

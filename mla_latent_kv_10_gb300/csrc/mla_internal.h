@@ -6,7 +6,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
-#include "../../include/mla.h"
+#include "mla.h"
 
 namespace mla {
 
