@@ -130,7 +130,8 @@ int mla_decode_workspace_size(const mla_dims* dims, size_t* bytes);
  * kv_cache bf16 [num_pages, P, d_c+d_R], 16-byte aligned
  * block_table int32 [B, max_pages_per_seq]; entries past ceil(n/P) unused
  * seq_lens int32 [B]
- * o_part  fp32 [slots, Lq*H, d_c]   (scratch for mla_combine_splits)
+ * o_part  fp32 scratch of slots * Lq*H * d_c floats for mla_combine_splits
+ *         (its layout is private to the library), 16-byte aligned
  * lse_part fp32 [slots, Lq*H]
  * workspace / ws_bytes: see mla_decode_workspace_size.
  * num_splits: 0 = automatic (all SMs busy); otherwise the number of

@@ -539,17 +539,20 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         tc_fence_after();
         const float l_sum = l_part + sh.lpart[half ^ 1][row];
         const float inv = l_sum > 0.f ? 1.0f / l_sum : 0.f;
-        float* dst = a.o_part + ((size_t)seg * a.rows + grow) * kDc + r * 256 + half * 128;
+        // o_part is chunk-major, [slot][column/4][row][4]: consecutive rows
+        // of a warp write consecutive 16-byte chunks.
+        float4* dst = reinterpret_cast<float4*>(a.o_part) +
+                      ((size_t)seg * (kDc / 4) + r * 64 + half * 32) * a.rows + grow;
         for (int c = 0; c < 4; ++c) {
           uint32_t v[32];
           tmem_ld32(lane_base + kColO + 128 * half + c * 32, v);
           tmem_wait_ld();
           if (valid) {
-            float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
 #pragma unroll
             for (int q = 0; q < 8; ++q)
-              d4[q] = make_float4(__uint_as_float(v[4 * q]) * inv, __uint_as_float(v[4 * q + 1]) * inv,
-                                  __uint_as_float(v[4 * q + 2]) * inv, __uint_as_float(v[4 * q + 3]) * inv);
+              dst[(size_t)(c * 8 + q) * a.rows] =
+                  make_float4(__uint_as_float(v[4 * q]) * inv, __uint_as_float(v[4 * q + 1]) * inv,
+                              __uint_as_float(v[4 * q + 2]) * inv, __uint_as_float(v[4 * q + 3]) * inv);
           }
         }
         if (valid && r == 0 && half == 0)
@@ -638,61 +641,90 @@ __global__ void __launch_bounds__(1024)
 }
 
 // ---------------------------------------------------------------- combine
-// One warp per (sequence, query row): log-sum-exp over the row's partials
-// (warp-shuffle max and sum), then the weighted sum of its latent slice.
+// One CTA per (sequence, 32 query rows, quarter of the latent slice).  The
+// log-sum-exp of each row's partials is reduced with warp shuffles over the
+// partial index and turned into per-partial weights in shared memory; the
+// weighted sum then reads the chunk-major partials coalesced (32
+// consecutive rows per warp access).  The bf16 result is staged in shared
+// memory and written out as contiguous row pieces.
+constexpr int kCombineRows = 32, kCombineSplit = 4, kCombineMaxSeg = 64;
 template <int DG>
 __global__ void __launch_bounds__(256)
     combine_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part,
                    const WsHeader* __restrict__ ws, __nv_bfloat16* __restrict__ o_lat,
                    float* __restrict__ lse_out, int B, int Lq, int H, int G) {
+  constexpr int kCols = DG / kCombineSplit;  // columns of this CTA
+  __shared__ __align__(16) __nv_bfloat16 tile[kCombineRows][kCols + 8];
+  __shared__ float wts[kCombineMaxSeg][kCombineRows];
+  __shared__ float lrow[kCombineRows];
   const int rows = Lq * H;
-  const int gw = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-  if (gw >= B * rows) return;
-  const int b = gw / rows, row = gw % rows;
-  const int h = row % H, g = (h * G) / H;
+  const int b = blockIdx.x, r0 = blockIdx.y * kCombineRows, cz = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int* off = reinterpret_cast<const int*>(ws + 1);
   const int chunk = ws->chunk;
   const int o0 = off[b], np = off[b + 1] - o0;
   const int kf = o0 / chunk, kl = (o0 + np - 1) / chunk;
   const int nseg = kl - kf + 1;
   const size_t seg0 = (size_t)b + kf;
+  const bool table = nseg <= kCombineMaxSeg;
 
-  float mx = -INFINITY;
-  for (int j = lane; j < nseg; j += 32) mx = fmaxf(mx, lse_part[(seg0 + j) * rows + row]);
+  // log-sum-exp per row (warp w: rows w, w+8, w+16, w+24), then weights
+  for (int rr = warp; rr < kCombineRows; rr += 8) {
+    const int row = r0 + rr;
+    float L = -INFINITY;
+    if (row < rows) {
+      float mx = -INFINITY;
+      for (int j = lane; j < nseg; j += 32) mx = fmaxf(mx, lse_part[(seg0 + j) * rows + row]);
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  float sum = 0.f;
-  if (mx != -INFINITY)
-    for (int j = lane; j < nseg; j += 32) sum += expf(lse_part[(seg0 + j) * rows + row] - mx);
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      float sum = 0.f;
+      if (mx != -INFINITY)
+        for (int j = lane; j < nseg; j += 32) sum += expf(lse_part[(seg0 + j) * rows + row] - mx);
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-  const float L = (mx == -INFINITY) ? -INFINITY : mx + logf(sum);
-
-  constexpr int kQ = DG / 128;  // float4 per lane
-  float4 acc[kQ];
-#pragma unroll
-  for (int q = 0; q < kQ; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (L != -INFINITY) {
-    for (int j = 0; j < nseg; ++j) {
-      const float w = expf(lse_part[(seg0 + j) * rows + row] - L);
-      if (w == 0.f) continue;
-      const float4* src = reinterpret_cast<const float4*>(o_part + ((seg0 + j) * rows + row) * kDc + g * DG);
-#pragma unroll
-      for (int q = 0; q < kQ; ++q) {
-        const float4 v = src[q * 32 + lane];
-        acc[q].x += w * v.x; acc[q].y += w * v.y; acc[q].z += w * v.z; acc[q].w += w * v.w;
-      }
+      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      L = (mx == -INFINITY) ? -INFINITY : mx + logf(sum);
+      if (table)
+        for (int j = lane; j < nseg; j += 32)
+          wts[j][rr] = (L == -INFINITY) ? 0.f : expf(lse_part[(seg0 + j) * rows + row] - L);
+    }
+    if (lane == 0) {
+      lrow[rr] = L;
+      if (row < rows && lse_out && cz == 0) lse_out[(size_t)b * rows + row] = L;
     }
   }
-  __nv_bfloat16* dst = o_lat + ((size_t)b * rows + row) * DG;
-#pragma unroll
-  for (int q = 0; q < kQ; ++q) {
-    uint2 v;
-    v.x = pack_bf16x2(acc[q].x, acc[q].y);
-    v.y = pack_bf16x2(acc[q].z, acc[q].w);
-    reinterpret_cast<uint2*>(dst)[q * 32 + lane] = v;
+  __syncthreads();
+
+  // weighted sum: thread = (row lane, chunk group warp)
+  const int row = r0 + lane;
+  const bool valid = row < rows;
+  const int h = valid ? row % H : 0, g = (h * G) / H;
+  const float L = lrow[lane];
+  constexpr int kChunks = kCols / 4;
+  for (int c = warp; c < kChunks; c += 8) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (valid && L != -INFINITY) {
+      const int c4 = g * (DG / 4) + cz * kChunks + c;  // 4-column chunk of the full latent
+      const float4* src = reinterpret_cast<const float4*>(o_part) + (size_t)c4 * rows + row;
+      for (int j = 0; j < nseg; ++j) {
+        const float w = table ? wts[j][lane] : expf(lse_part[(seg0 + j) * rows + row] - L);
+        if (w == 0.f) continue;
+        const float4 v = src[(seg0 + j) * (size_t)(kDc / 4) * rows];
+        acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
+      }
+    }
+    uint2 pk;
+    pk.x = pack_bf16x2(acc.x, acc.y);
+    pk.y = pack_bf16x2(acc.z, acc.w);
+    *reinterpret_cast<uint2*>(&tile[lane][c * 4]) = pk;
   }
-  if (lse_out && lane == 0) lse_out[(size_t)b * rows + row] = L;
+  __syncthreads();
+  constexpr int kPieces = kCols * 2 / 16;  // 16-byte pieces per row
+  for (int i = threadIdx.x; i < kCombineRows * kPieces; i += 256) {
+    const int rr = i / kPieces, pc = i % kPieces;
+    if (r0 + rr < rows)
+      reinterpret_cast<uint4*>(o_lat + ((size_t)b * rows + r0 + rr) * DG + cz * kCols)[pc] =
+          *reinterpret_cast<const uint4*>(&tile[rr][pc * 8]);
+  }
 }
 
 }  // namespace
@@ -759,8 +791,7 @@ cudaError_t launch_decode(const CUtensorMap& tm_cache, const DecodeArgs& a, int 
 
 cudaError_t launch_combine(const float* o_part, const float* lse_part, const WsHeader* ws, void* o_lat,
                            float* lse, int B, int Lq, int H, int G, cudaStream_t st) {
-  const int warps = B * Lq * H;
-  dim3 grid((warps + 7) / 8), block(256);
+  dim3 grid(B, (Lq * H + kCombineRows - 1) / kCombineRows, kCombineSplit), block(256);
   auto* ol = static_cast<__nv_bfloat16*>(o_lat);
   if (G == 1) combine_kernel<512><<<grid, block, 0, st>>>(o_part, lse_part, ws, ol, lse, B, Lq, H, G);
   else combine_kernel<256><<<grid, block, 0, st>>>(o_part, lse_part, ws, ol, lse, B, Lq, H, G);
