@@ -176,6 +176,39 @@ int mla_project_uv(const mla_dims* dims, const void* o_lat, const void* W_UV,
  */
 int mla_get_device_status(const void* workspace, void* stream);
 
+/*
+ * mla_decode_attend_noalloc — mla_decode_paged followed by
+ * mla_combine_splits, for callers that cannot allocate device memory.
+ * This is a library convenience with no counterpart in the source pages.
+ *
+ * Who it is for: callers that cannot hand the library scratch memory, e.g.
+ * an engine whose memory planner has already given out all of the GPU, a
+ * plugin inside a host program that owns every allocation, or a decode loop
+ * recorded into a CUDA graph (where a cudaMalloc would break the capture).
+ * They pass only inputs and outputs; the split plan, the status word and the
+ * split partials live in one fixed 32 MiB array that the library reserves on
+ * every GPU where it is loaded, until the process exits.
+ *
+ * q_cat, kv_cache, block_table, seq_lens: as for mla_decode_paged.
+ * o_lat bf16 [B,Lq,H,d_g], lse fp32 [B,Lq,H] (may be NULL): as for
+ * mla_combine_splits.  device_status (device int, may be NULL): receives this
+ * call's device status (MLA_OK, MLA_ERR_BAD_TABLE, MLA_ERR_BAD_SEQLEN or
+ * MLA_ERR_TIMEOUT) when the call's work has run.
+ *
+ * Limit: the scratch of one call is about (B + clusters - 1) * Lq*H * 2 KiB
+ * (clusters = CTA pairs that fit on the GPU, e.g. 76 on a GB300 at Lq*H <=
+ * 128); if that exceeds 32 MiB the call returns MLA_ERR_WORKSPACE and does
+ * nothing.  The first call on a device looks up the array's device address;
+ * make that first call before any stream capture.  All calls on a device
+ * share the array (each call clears and rewrites what it uses), so calls that
+ * may overlap on the GPU — unordered streams, several host threads — race.
+ * Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ */
+int mla_decode_attend_noalloc(const mla_dims* dims, const void* q_cat,
+                              const void* kv_cache, const int32_t* block_table,
+                              const int32_t* seq_lens, void* o_lat, float* lse,
+                              int* device_status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
