@@ -46,6 +46,20 @@ WORKLOAD_TEXT = {
 }
 
 
+def decode_traffic(workload):
+    """DRAM bytes per decode launch from the committed ncu summary of this
+    workload, if it was taken on the current decode source (else None)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "decode_kernel_%s.json" % workload)
+    if not os.path.exists(path):
+        return None
+    rec = json.load(open(path))
+    src = os.path.join(ROOT, rec["source"])
+    if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest() != rec["source_sha256"]:
+        return None
+    return rec["dram_bytes_per_launch"]
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -372,7 +386,7 @@ def main():
                           "tensor_frac": tflops_dec / peaks["bf16_tflops"],
                           "bytes": dec_bytes, "flops": dec_flops},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "traffic": None, "peak_source": peak_src,
+                     "frac": achieved / hbm, "traffic": decode_traffic(args.workload), "peak_source": peak_src,
                      "kernel": "mla_decode_paged (plan + decode)"},
         "e2e": {"value": world * step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
