@@ -52,9 +52,15 @@ constexpr int kBoxBytes = kPage * 64 * 2;       // 64 tokens x 64 bf16 = 8 KiB
 constexpr int kStageBytes = 5 * kBoxBytes;      // latent half (4 boxes) + RoPE box
 constexpr int kXSlot = kRowsPerCta * 64 * 2;    // one fp16 partial-score tile, 16 KiB
 constexpr int kSmemShared = kStages * kStageBytes + 4 * kXSlot;  // offset of DecodeShared (2 send + 2 receive slots before it)
-constexpr int kSoftmaxThreads = 256;            // 8 softmax warps, two per TMEM lane quadrant
-constexpr int kTmaWarp = 8, kMmaWarp = 9;
-constexpr int kDecodeThreads = kSoftmaxThreads + 64;
+// warps 0-3: exchange warps (one per TMEM lane quadrant); warps 4-11: softmax
+// warps (two per quadrant); warp 12: TMA producer; warp 13: MMA issuer
+constexpr int kXWarps = 4, kSWarps = 8;
+constexpr int kXThreads = 32 * kXWarps, kSoftmaxThreads = 32 * kSWarps;
+constexpr int kTmaWarp = kXWarps + kSWarps, kMmaWarp = kTmaWarp + 1;
+constexpr int kDecodeThreads = 32 * (kMmaWarp + 1);
+// named barriers: 1 = exchange warps, 2..5 = softmax warp pair of a quadrant,
+// 6 = all softmax warps
+constexpr uint32_t kBarX = 1, kBarPair0 = 2, kBarS = 6;
 constexpr uint32_t kColO = 0, kColQ = 256, kColS = 416, kColP = 480, kTmemCols = 512;  // Q uses 144 columns
 constexpr float kRescaleThreshold = 8.0f;       // log2 units: defer O rescaling up to 2^8
 
@@ -114,9 +120,10 @@ __device__ __forceinline__ void set_status(WsHeader* ws, int code) {
 struct DecodeShared {
   uint64_t full[kStages], empty[kStages];
   uint64_t q_full, s_full, s_free, p_full, o_done, drain;
-  uint64_t xfull[2], xfree[2];
-  float pmax[2][kRowsPerCta];   // [column half][row]: half-row maxima of the current page
-  float lpart[2][kRowsPerCta];  // [column half][row]: half-row sums at the epilogue
+  uint64_t xfull[2], xfree[2], own_ready[2], src_free[2];
+  // [page parity][column half][row]: half-row maxima (half-row sums at the
+  // epilogue use the parity after the segment's last page)
+  float red[2][2][kRowsPerCta];
   uint32_t tmem;
   int abort;
 };
@@ -193,13 +200,15 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     }
     mbar_init(bar(sh.q_full), kSoftmaxThreads);
     mbar_init(bar(sh.s_full), 1);
-    mbar_init(bar(sh.s_free), kSoftmaxThreads);
+    mbar_init(bar(sh.s_free), kXThreads);
     mbar_init(bar(sh.p_full), kSoftmaxThreads);
     mbar_init(bar(sh.o_done), 1);
     mbar_init(bar(sh.drain), 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(sh.xfull[s]), 1);                  // armed with the expected bytes, completed by the peer's copy
-      mbar_init(bar(sh.xfree[s]), kSoftmaxThreads / 32);  // every softmax warp of the peer consumed its part
+      mbar_init(bar(sh.xfull[s]), 1);         // armed with the expected bytes, completed by the peer's copy
+      mbar_init(bar(sh.xfree[s]), kSWarps);   // the peer's softmax warps consumed what we sent
+      mbar_init(bar(sh.own_ready[s]), 1);     // our exchange warps wrote our partial into the send slot
+      mbar_init(bar(sh.src_free[s]), kSWarps);  // our softmax warps read our partial from the send slot
     }
     fence_mbar_init();
     for (int s = 0; s < 2; ++s) mbar_arrive_expect_tx(bar(sh.xfull[s]), kXSlot);
@@ -220,6 +229,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     *abort = 1;
     set_status(ws, MLA_ERR_TIMEOUT);
   };
+  const uint32_t xsrc = smem_u32(xbuf), xrecv = xsrc + 2 * kXSlot;
 
   if (warp == kTmaWarp) {
     // ------------------------------------------------------------ TMA producer
@@ -256,6 +266,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           mbar_wait(bar(sh.full[k % kStages]), (k / kStages) & 1, abort, 100000000ull);
       }
     }
+    __syncwarp();  // reconverge before the CTA-wide barrier of the teardown
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -281,7 +292,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         return true;
       };
       // Issue order QK(q), PV(q-2): the softmax warps work one page behind
-      // the score MMAs, so P(q-2) is ready once S(q) may be overwritten.
+      // the exchange warps, so P(q-2) is ready once S(q) may be overwritten.
       while (ok && it.next(sb, pa, pb)) {
         if (!(ok = mbar_wait(bar(sh.q_full), qc & 1, abort))) break;
         ++qc;
@@ -310,13 +321,75 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       }
       if (!ok) fail();
     }
-  } else {
+    __syncwarp();  // reconverge before the CTA-wide barrier of the teardown
+  } else if (warp < kXWarps) {
+    // ------------------------------------------------------------ exchange warps
+    // Page q: this CTA's partial scores (TMEM) -> fp16 in log2 units -> send
+    // slot q&1 -> one bulk copy into the peer's receive slot.  After a
+    // failure the loop keeps running without work, so every named barrier
+    // still sees all four warps.
+    const int row = warp * 32 + lane;
+    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    const uint32_t peer_recv = mapa(xrecv, peer);
+    const uint32_t peer_xfull0 = mapa(bar(sh.xfull[0]), peer), peer_xfull1 = mapa(bar(sh.xfull[1]), peer);
+    SegIter it;
+    it.init(ws, unit);
+    const int npages = it.end - it.start;
+    bool ok = true;
+    for (int q = 0; q < npages; ++q) {
+      const uint32_t slot = q & 1, use = q >> 1;
+      if (ok) ok = mbar_wait(bar(sh.s_full), q & 1, abort);
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok) {
+        tc_fence_after();
+        uint32_t w[32];
+        {
+          uint32_t v[32];
+          tmem_ld32(lane_base + kColS, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            w[j] = pack_f16x2_sat(__uint_as_float(v[2 * j]) * a.scale_log2, __uint_as_float(v[2 * j + 1]) * a.scale_log2);
+          tmem_ld32(lane_base + kColS + 32, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            w[16 + j] = pack_f16x2_sat(__uint_as_float(v[2 * j]) * a.scale_log2,
+                                       __uint_as_float(v[2 * j + 1]) * a.scale_log2);
+        }
+        tc_fence_before();
+        mbar_arrive(bar(sh.s_free));
+        if (use > 0) {  // the peer and our softmax warps are done with this slot's last use
+          ok = mbar_wait(bar(sh.xfree[slot]), (use - 1) & 1, abort);
+          if (ok) ok = mbar_wait(bar(sh.src_free[slot]), (use - 1) & 1, abort);
+        }
+        ok = __all_sync(0xffffffffu, ok);
+        if (ok) {
+          const uint32_t dst = xsrc + slot * kXSlot + row * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            st_shared_v4(dst + ((c ^ (row & 7)) << 4), w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+          fence_proxy_async();
+        }
+      }
+      ok = bar_red_and_n(ok, kBarX, kXThreads);
+      if (ok && threadIdx.x == 0) {
+        bulk_s2s(peer_recv + slot * kXSlot, xsrc + slot * kXSlot, kXSlot, slot ? peer_xfull1 : peer_xfull0);
+        mbar_arrive(bar(sh.own_ready[slot]));
+      }
+      __syncwarp();
+    }
+    if (!ok) fail();
+  } else if (warp < kXWarps + kSWarps) {
     // ------------------------------------------------------------ softmax warps
-    // Two warps per TMEM lane quadrant: warp w and w+4 share query rows and
-    // split each page's 64 key columns (half = warp / 4).  Software-pipelined
-    // by one page: while the partial scores of page q travel to the peer, the
-    // softmax of page q-1 runs.
-    const int quad = warp & 3, half = warp >> 2;
+    // Two warps per TMEM lane quadrant share its 32 query rows and split each
+    // page's 64 key columns (half).  Page q: scores = own + peer fp16
+    // partials (the two CTAs add the same two values), mask, online softmax
+    // (row maximum shared with the partner warp), P -> tensor memory.  After a
+    // failure the loops keep running without work, so every named barrier
+    // still sees all its warps.
+    const int sw = warp - kXWarps;
+    const int quad = warp & 3, half = sw >> 2;
     const int row = quad * 32 + lane;              // TMEM lane = query row in this block
     const int grow = (int)rg * kRowsPerCta + row;  // row of the (l, h) list
     const bool valid = grow < a.rows;
@@ -324,220 +397,184 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     const int h = valid ? grow % a.H : 0;
     const int g = (h * a.G) / a.H;
     const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
-    const uint32_t xsrc = smem_u32(xbuf), xrecv = xsrc + 2 * kXSlot;
-    const uint32_t peer_recv = mapa(xrecv, peer);
-    const uint32_t peer_xfull0 = mapa(bar(sh.xfull[0]), peer), peer_xfull1 = mapa(bar(sh.xfull[1]), peer);
     const uint32_t peer_xfree0 = mapa(bar(sh.xfree[0]), peer), peer_xfree1 = mapa(bar(sh.xfree[1]), peer);
     const uint32_t xrow = row * 128;
-    const uint32_t pair_bar = 2 + quad;  // named barrier of warps quad and quad+4
+    const uint32_t pair_bar = kBarPair0 + quad;
     const int d_q = a.d_g + kDr;
-    const bool sender = threadIdx.x == 32 * 4 + 1;  // issues the bulk copies, no remote arrives
     SegIter it;
     it.init(ws, unit);
     int sb, pa, pb;
-    uint32_t pc = 0, od = 0;
+    uint32_t q = 0, od = 0;
     bool ok = true;
-    float m_used = -INFINITY, l_part = 0.f;
-    int limit = 0;
 
-    // (a) page q: this thread's 32 partial scores TMEM -> fp16 (log2 units)
-    // -> local send slot
-    auto stage_a = [&](uint32_t q) {
-      if (ok) ok = mbar_wait(bar(sh.s_full), q & 1, abort);
-      ok = __all_sync(0xffffffffu, ok);
+    // this CTA's slice of query row (sequence b) -> tensor memory: 4 chunks
+    // of 64 latent columns (half 0: chunks 0-1 and the 32 RoPE columns this
+    // CTA multiplies; half 1: chunks 2-3)
+    auto qrow_of = [&](int b) { return a.q_cat + ((size_t)(b * a.Lq + l) * a.H + h) * d_q; };
+    auto load_q = [&](int b) {
       if (!ok) return;
-      tc_fence_after();
-      uint32_t w[16];
-      {
-        uint32_t v[32];
-        tmem_ld32(lane_base + kColS + 32 * half, v);
-        tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-          w[j] = pack_f16x2_sat(__uint_as_float(v[2 * j]) * a.scale_log2, __uint_as_float(v[2 * j + 1]) * a.scale_log2);
+      const __nv_bfloat16* qrow = qrow_of(b);
+      const uint4* lat = nullptr;
+      if (valid) {
+        if (a.G == 1) lat = reinterpret_cast<const uint4*>(qrow + r * 256);
+        else if ((uint32_t)g == r) lat = reinterpret_cast<const uint4*>(qrow);
       }
-      tc_fence_before();
-      mbar_arrive(bar(sh.s_free));
-      const uint32_t slot = q & 1, use = q >> 1;
-      if (use > 0) ok = mbar_wait<true>(bar(sh.xfree[slot]), (use - 1) & 1, abort);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) return;
-      const uint32_t dst = xsrc + slot * kXSlot + xrow;
+      for (int c = 2 * half; c < 2 * half + 2; ++c) {
+        const uint4* src = lat ? lat + c * 8 : nullptr;
+        uint32_t w[32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
-        st_shared_v4(dst + (((4 * half + c) ^ (row & 7)) << 4), w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
-      fence_proxy_async();
-    };
-
-    // wait until the peer's partial of page q has landed in our receive slot
-    auto recv_wait = [&](uint32_t q) {
-      if (ok) ok = mbar_wait<true>(bar(sh.xfull[q & 1]), (q >> 1) & 1, abort);
-      ok = __all_sync(0xffffffffu, ok);
-    };
-
-    // (b) page q (= page i of the sequence): scores = own + peer partial
-    // (both fp16-rounded, so the two CTAs add identical values), mask,
-    // online softmax over this thread's 32 columns (row maximum shared with
-    // the partner warp), P -> tensor memory
-    auto stage_b = [&](uint32_t q, int i, bool first) {
-      if (!ok) return;
-      float s[32];
-      {
-        const uint32_t off = (q & 1) * kXSlot + xrow;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t o[4], p[4];
-          const uint32_t sw = ((4 * half + c) ^ (row & 7)) << 4;
-          ld_shared_v4(xsrc + off + sw, o[0], o[1], o[2], o[3]);
-          ld_shared_v4(xrecv + off + sw, p[0], p[1], p[2], p[3]);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float2 x = unpack_f16x2(o[k]), y = unpack_f16x2(p[k]);
-            s[8 * c + 2 * k] = x.x + y.x;
-            s[8 * c + 2 * k + 1] = x.y + y.y;
-          }
+        for (int k = 0; k < 8; ++k) {
+          uint4 v = src ? src[k] : make_uint4(0, 0, 0, 0);
+          w[4 * k + 0] = v.x; w[4 * k + 1] = v.y; w[4 * k + 2] = v.z; w[4 * k + 3] = v.w;
         }
+        tmem_st32(lane_base + kColQ + c * 32, w);
       }
-      // this warp's part of the receive slot is read (every loaded value is
-      // already consumed above): hand it back, after re-arming the slot for
-      // its next use (once per CTA)
-      __syncwarp();
-      if (lane == 0) {
-        if (warp == 0) mbar_arrive_expect_tx(bar(sh.xfull[q & 1]), kXSlot);
-        mbar_arrive_remote_relaxed((q & 1) ? peer_xfree1 : peer_xfree0);
-      }
-      const int key0 = i * kPage + 32 * half;
-      float mt = -INFINITY;
-      if (limit < i * kPage + kPage) {  // page holds keys this row may not see
+      if (half == 0) {
+        const uint4* rope = valid ? reinterpret_cast<const uint4*>(qrow + a.d_g + 32 * r) : nullptr;
+        uint32_t w[16];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float v = (key0 + j < limit) ? s[j] : -INFINITY;
-          s[j] = v;
-          mt = fmaxf(mt, v);
+        for (int k = 0; k < 4; ++k) {
+          uint4 v = rope ? rope[k] : make_uint4(0, 0, 0, 0);
+          w[4 * k + 0] = v.x; w[4 * k + 1] = v.y; w[4 * k + 2] = v.z; w[4 * k + 3] = v.w;
         }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) mt = fmaxf(mt, s[j]);
+        tmem_st16(lane_base + kColQ + 128, w);
       }
-      sh.pmax[half][row] = mt;
-      ok = bar_red_and_n(ok, pair_bar, 64);
-      if (!ok) return;
-      mt = fmaxf(mt, sh.pmax[half ^ 1][row]);
-      const bool need = mt > m_used + kRescaleThreshold;
-      if (!first) {  // P.V of the previous page done: P and O are ours
-        ok = mbar_wait(bar(sh.o_done), od & 1, abort);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) return;
-        ++od;
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, need)) {
-          const float f = need ? ex2(m_used - mt) : 1.0f;
-          for (int c = 0; c < 4; ++c) {
-            uint32_t v[32];
-            const uint32_t col = lane_base + kColO + 128 * half + c * 32;
-            tmem_ld32(col, v);
-            tmem_wait_ld();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * f);
-            tmem_st32(col, v);
-          }
-          l_part *= f;
-        }
-      }
-      if (need) m_used = mt;
-      const float base = (m_used == -INFINITY) ? 0.f : m_used;
-      uint32_t pk[16];
-      float psum = 0.f;
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const uint32_t w = pack_bf16x2(ex2(s[2 * j] - base), ex2(s[2 * j + 1] - base));
-        psum += bf16_lo(w) + bf16_hi(w);
-        pk[j] = w;
-      }
-      l_part += psum;
-      tmem_st16(lane_base + kColP + 16 * half, pk);
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar(sh.p_full));
+      mbar_arrive(bar(sh.q_full));
+    };
+    // pull the rows this thread will load for sequence b into L2 ahead of use
+    auto prefetch_q = [&](int b) {
+      if (!valid) return;
+      const char* qrow = reinterpret_cast<const char*>(qrow_of(b));
+      const char* lat = a.G == 1 ? qrow + r * 512 : qrow;
+      if (a.G == 1 || (uint32_t)g == r) {
+        asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(lat + half * 256));
+        asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(lat + half * 256 + 128));
+      }
+      if (half == 0) asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(qrow + a.d_g * 2 + 64 * r));
     };
 
-    // Control flow leaves this loop only right after a vote of all softmax
-    // threads (bar_red_and_n), so no thread is ever left waiting at a named
-    // barrier for a warp that gave up.
-    while (it.next(sb, pa, pb)) {
+    bool have = it.next(sb, pa, pb);
+    if (have) load_q(sb);
+    while (have) {
       const int seg = sb + unit;
       const int n = nlen[sb];
-      limit = a.causal ? n - a.Lq + l + 1 : n;  // keys [0, limit) visible
-      m_used = -INFINITY;
-      l_part = 0.f;
+      const int limit = a.causal ? n - a.Lq + l + 1 : n;  // keys [0, limit) visible
+      float m_used = -INFINITY, l_part = 0.f;
+      SegIter peek = it;
+      int nsb, npa, npb;
+      const bool nhave = peek.next(nsb, npa, npb);
+      if (nhave) prefetch_q(nsb);
 
-      // ---- load this CTA's slice of the query row into tensor memory:
-      // 4 chunks of 64 latent columns (half 0: chunks 0-1 and the 32 RoPE
-      // columns this CTA multiplies; half 1: chunks 2-3)
-      {
-        const __nv_bfloat16* qrow = a.q_cat + ((size_t)(sb * a.Lq + l) * a.H + h) * d_q;
-        const uint4* lat = nullptr;
-        if (valid) {
-          if (a.G == 1) lat = reinterpret_cast<const uint4*>(qrow + r * 256);
-          else if ((uint32_t)g == r) lat = reinterpret_cast<const uint4*>(qrow);
-        }
-        for (int c = 2 * half; c < 2 * half + 2; ++c) {
-          const uint4* src = lat ? lat + c * 8 : nullptr;
-          uint32_t w[32];
+      // ---- pages
+      for (int i = pa; i < pb; ++i, ++q) {
+        const uint32_t slot = q & 1, use = q >> 1;
+        const bool first = (i == pa);
+        float s[32];
+        float mt = -INFINITY;
+        if (ok) ok = mbar_wait(bar(sh.own_ready[slot]), use & 1, abort);
+        if (ok) ok = mbar_wait(bar(sh.xfull[slot]), use & 1, abort);
+        ok = __all_sync(0xffffffffu, ok);
+        if (ok) {
+          const uint32_t off = slot * kXSlot + xrow;
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            uint4 v = src ? src[q] : make_uint4(0, 0, 0, 0);
-            w[4 * q + 0] = v.x; w[4 * q + 1] = v.y; w[4 * q + 2] = v.z; w[4 * q + 3] = v.w;
-          }
-          tmem_st32(lane_base + kColQ + c * 32, w);
-        }
-        if (half == 0) {
-          const uint4* rope = valid ? reinterpret_cast<const uint4*>(qrow + a.d_g + 32 * r) : nullptr;
-          uint32_t w[16];
+          for (int c = 0; c < 4; ++c) {
+            uint32_t o[4], p[4];
+            const uint32_t swz = ((4 * half + c) ^ (row & 7)) << 4;
+            ld_shared_v4(xsrc + off + swz, o[0], o[1], o[2], o[3]);
+            ld_shared_v4(xrecv + off + swz, p[0], p[1], p[2], p[3]);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint4 v = rope ? rope[q] : make_uint4(0, 0, 0, 0);
-            w[4 * q + 0] = v.x; w[4 * q + 1] = v.y; w[4 * q + 2] = v.z; w[4 * q + 3] = v.w;
+            for (int k = 0; k < 4; ++k) {
+              const float2 x = unpack_f16x2(o[k]), y = unpack_f16x2(p[k]);
+              s[8 * c + 2 * k] = x.x + y.x;
+              s[8 * c + 2 * k + 1] = x.y + y.y;
+            }
           }
-          tmem_st16(lane_base + kColQ + 128, w);
+          // both slots read by this warp (values consumed above): hand the
+          // receive slot back to the peer (re-armed first, once per CTA) and
+          // the send slot back to our exchange warps
+          __syncwarp();
+          if (lane == 0) {
+            if (sw == 0) mbar_arrive_expect_tx(bar(sh.xfull[slot]), kXSlot);
+            mbar_arrive_remote_relaxed(slot ? peer_xfree1 : peer_xfree0);
+            mbar_arrive(bar(sh.src_free[slot]));
+          }
+          __syncwarp();  // reconverge: the aligned barrier and TMEM ops below need the whole warp
+          const int key0 = i * kPage + 32 * half;
+          if (limit < i * kPage + kPage) {  // page holds keys this row may not see
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float v = (key0 + j < limit) ? s[j] : -INFINITY;
+              s[j] = v;
+              mt = fmaxf(mt, v);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) mt = fmaxf(mt, s[j]);
+          }
+          sh.red[slot][half][row] = mt;
         }
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(bar(sh.q_full));
+        ok = bar_red_and_n(ok, pair_bar, 64);
+        if (ok) {
+          mt = fmaxf(mt, sh.red[slot][half ^ 1][row]);
+          const bool need = mt > m_used + kRescaleThreshold;
+          if (!first) {  // P.V of the previous page done: P and O are ours
+            ok = mbar_wait(bar(sh.o_done), od & 1, abort);
+            ok = __all_sync(0xffffffffu, ok);
+            ++od;
+            if (ok) {
+              tc_fence_after();
+              if (__any_sync(0xffffffffu, need)) {
+                const float f = need ? ex2(m_used - mt) : 1.0f;
+                for (int c = 0; c < 4; ++c) {
+                  uint32_t v[32];
+                  const uint32_t col = lane_base + kColO + 128 * half + c * 32;
+                  tmem_ld32(col, v);
+                  tmem_wait_ld();
+#pragma unroll
+                  for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * f);
+                  tmem_st32(col, v);
+                }
+                l_part *= f;
+              }
+            }
+          }
+          if (ok) {
+            if (need) m_used = mt;
+            const float base = (m_used == -INFINITY) ? 0.f : m_used;
+            uint32_t pk[16];
+            float psum = 0.f;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const uint32_t w = pack_bf16x2(ex2(s[2 * j] - base), ex2(s[2 * j + 1] - base));
+              psum += bf16_lo(w) + bf16_hi(w);
+              pk[j] = w;
+            }
+            l_part += psum;
+            tmem_st16(lane_base + kColP + 16 * half, pk);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bar(sh.p_full));
+          }
+        }
       }
 
-      // ---- pages, one-page software pipeline
-      stage_a(pc);
-      ok = bar_red_and_n(ok, 1, kSoftmaxThreads);
-      if (!ok) break;
-      if (sender) bulk_s2s(peer_recv + (pc & 1) * kXSlot, xsrc + (pc & 1) * kXSlot, kXSlot, (pc & 1) ? peer_xfull1 : peer_xfull0);
-      bool go = true;
-      for (int i = pa + 1; i < pb; ++i) {
-        const uint32_t q = pc + (uint32_t)(i - pa);
-        stage_a(q);
-        ok = bar_red_and_n(ok, 1, kSoftmaxThreads);
-        if (!ok) { go = false; break; }
-        if (sender) bulk_s2s(peer_recv + (q & 1) * kXSlot, xsrc + (q & 1) * kXSlot, kXSlot, (q & 1) ? peer_xfull1 : peer_xfull0);
-        recv_wait(q - 1);
-        stage_b(q - 1, i - 1, i - 1 == pa);
-        ok = bar_red_and_n(ok, pair_bar, 64);  // partner done with pmax; pair in step on failure
-        if (!ok) { go = false; break; }
-      }
-      if (!go) break;
-      const uint32_t qe = pc + (uint32_t)(pb - 1 - pa);
-      recv_wait(qe);
-      stage_b(qe, pb - 1, pb - 1 == pa);
-      pc += (uint32_t)(pb - pa);
-
-      // ---- epilogue: normalised latent partial and log-sum-exp
+      // ---- end of segment: once the last P.V is done, first hand the next
+      // segment's query to the MMA issuer, then write this segment's
+      // normalised latent partial and log-sum-exp while the next segment's
+      // first scores are computed (its first P.V needs our P, which comes
+      // after this epilogue, so O is read before it is overwritten).
       if (ok) ok = mbar_wait(bar(sh.o_done), od & 1, abort);
       ok = __all_sync(0xffffffffu, ok);
       ++od;
-      sh.lpart[half][row] = l_part;
+      if (ok) tc_fence_after();
+      it = peek;
+      if (nhave) load_q(nsb);
+      sh.red[q & 1][half][row] = l_part;  // parity after the last page: free (see red)
       ok = bar_red_and_n(ok, pair_bar, 64);
       if (ok) {
-        tc_fence_after();
-        const float l_sum = l_part + sh.lpart[half ^ 1][row];
+        const float l_sum = l_part + sh.red[q & 1][half ^ 1][row];
         const float inv = l_sum > 0.f ? 1.0f / l_sum : 0.f;
         // o_part is chunk-major, [slot][column/4][row][4]: consecutive rows
         // of a warp write consecutive 16-byte chunks.
@@ -549,10 +586,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           tmem_wait_ld();
           if (valid) {
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-              dst[(size_t)(c * 8 + q) * a.rows] =
-                  make_float4(__uint_as_float(v[4 * q]) * inv, __uint_as_float(v[4 * q + 1]) * inv,
-                              __uint_as_float(v[4 * q + 2]) * inv, __uint_as_float(v[4 * q + 3]) * inv);
+            for (int k = 0; k < 8; ++k)
+              dst[(size_t)(c * 8 + k) * a.rows] =
+                  make_float4(__uint_as_float(v[4 * k]) * inv, __uint_as_float(v[4 * k + 1]) * inv,
+                              __uint_as_float(v[4 * k + 2]) * inv, __uint_as_float(v[4 * k + 3]) * inv);
           }
         }
         if (valid && r == 0 && half == 0)
@@ -560,8 +597,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
               l_sum > 0.f ? (m_used + lg2(l_sum)) * 0.69314718055994531f : -INFINITY;
         tc_fence_before();
       }
-      ok = bar_red_and_n(ok, 1, kSoftmaxThreads);
-      if (!ok) break;
+      ok = bar_red_and_n(ok, kBarS, kSoftmaxThreads);
+      sb = nsb; pa = npa; pb = npb;
+      have = nhave;
     }
     if (!ok) fail();
   }

@@ -92,7 +92,8 @@ __global__ void __launch_bounds__(128, 1)
       abort_flag = 1;
     }
   }
-  const bool ok = mbar_wait(done, 0, &abort_flag);
+  __syncwarp();  // warp 0 reconverges before the aligned TMEM loads below
+  const bool ok = __all_sync(0xffffffffu, mbar_wait(done, 0, &abort_flag));
   tc_fence_after();
   if (ok) {
     const int row = warp * 32 + lane, m = m0 + row;
@@ -189,7 +190,8 @@ __global__ void __launch_bounds__(128, 1)
     if (ok) mma_commit(done);
     else abort_flag = 1;
   }
-  const bool ok = mbar_wait(done, 0, &abort_flag);
+  __syncwarp();  // warp 0 reconverges before the aligned TMEM loads below
+  const bool ok = __all_sync(0xffffffffu, mbar_wait(done, 0, &abort_flag));
   tc_fence_after();
   if (ok) {
     const int row = warp * 32 + lane, m = m0 + row;
