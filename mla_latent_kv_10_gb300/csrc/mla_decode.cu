@@ -38,6 +38,7 @@
 //   * Every wait is bounded (wall clock); on expiry the kernel records
 //     MLA_ERR_TIMEOUT in the workspace status word, stops, waits for its own
 //     copies and MMAs, frees tensor memory and returns.
+#include <climits>
 #include <cmath>
 
 #include "mla_internal.h"
@@ -134,11 +135,19 @@ static_assert(kDecodeSmem <= 232448, "decode kernel exceeds 227 KiB of shared me
 
 // Walks the (sequence, page range) segments of one work unit.
 struct SegIter {
-  const int* off;
-  int B, start, end, b;
-  __device__ void init(const WsHeader* ws, int unit) {
-    off = reinterpret_cast<const int*>(ws + 1);
+  WsView v;
+  int B, unit, mode, start, end, b;
+  __device__ void init(const WsHeader* ws, int u) {
     B = ws->B;
+    unit = u;
+    mode = ws->mode;
+    v = ws_view(ws, B);
+    if (mode == 1) {  // sequence-aligned: at most one segment
+      b = v.ub[unit];
+      start = b >= 0 ? v.upa[unit] : 0;
+      end = b >= 0 ? v.upb[unit] : 0;
+      return;
+    }
     const int total = ws->total, chunk = ws->chunk;
     start = min(unit * chunk, total);
     end = min(start + chunk, total);
@@ -146,14 +155,25 @@ struct SegIter {
     int lo = 0, hi = B - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if (off[mid] <= start) lo = mid; else hi = mid - 1;
+      if (v.off[mid] <= start) lo = mid; else hi = mid - 1;
     }
     b = lo;
   }
-  // Next non-empty segment: sequence b, pages [pa, pb) of that sequence.
+  __device__ int total_pages() const { return end - start; }
+  // partial-output slot of a segment of sequence sb
+  __device__ int slot(int sb) const { return mode == 1 ? unit : sb + unit; }
+  // Next non-empty segment: sequence sb, pages [pa, pb) of that sequence.
   __device__ bool next(int& sb, int& pa, int& pb) {
+    if (mode == 1) {
+      if (b < 0 || start >= end) return false;
+      sb = b;
+      pa = start;
+      pb = end;
+      b = -1;
+      return true;
+    }
     while (b < B && start < end) {
-      const int o0 = off[b], o1 = off[b + 1];
+      const int o0 = v.off[b], o1 = v.off[b + 1];
       const int a = max(start, o0), e = min(end, o1);
       const int cur = b++;
       if (a < e) {
@@ -188,7 +208,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   const uint32_t peer = crank ^ 1u;
   const int unit = (int)cluster_id_x();
   WsHeader* ws = a.ws;
-  const int* nlen = reinterpret_cast<const int*>(ws + 1) + a.B + 1;
+  const int* nlen = ws_view(ws, a.B).nlen;
 
   auto bar = [](uint64_t& x) { return smem_u32(&x); };
 
@@ -258,6 +278,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                              page * kPage, policy);
           // RoPE box (each CTA uses 32 of its 64 columns)
           tma_load_2d_hint(dst + 4 * kBoxBytes, &tm_cache, bar(sh.full[st]), kDc, page * kPage, policy);
+          // At start-up every CTA of the grid asks for its pages at once; let
+          // the first page land before queueing the rest so compute starts
+          // as early as possible instead of after the whole initial burst.
+          if (pc == 0 && !(ok = mbar_wait(bar(sh.full[0]), 0, abort))) {
+            fail();
+            ++pc;
+            break;
+          }
         }
       }
       // Copies still in flight must land before this CTA may exit.
@@ -458,7 +486,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     bool have = it.next(sb, pa, pb);
     if (have) load_q(sb);
     while (have) {
-      const int seg = sb + unit;
+      const int seg = it.slot(sb);
       const int n = nlen[sb];
       const int limit = a.causal ? n - a.Lq + l + 1 : n;  // keys [0, limit) visible
       float m_used = -INFINITY, l_part = 0.f;
@@ -622,16 +650,53 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 
 // ---------------------------------------------------------------- plan
 // One CTA: validates lengths and table entries, prefix-sums pages per
-// sequence, cuts the flattened page list into `units` equal ranges.
+// sequence and splits the work over `units` clusters.  Two splits are
+// costed (in pages, a switch between sequences inside a unit counting
+// kSwitchPages) and the cheaper one is written:
+//   balanced  — the flattened page list cut into equal contiguous ranges;
+//   aligned   — each sequence gets max(1, floor(units * pages_b / total))
+//               whole units, at most one per page (needs B <= units), and
+//               splits its pages evenly over them.
+constexpr int kSwitchPages = 4;
+__device__ __forceinline__ int block_reduce_max(int v, int* scratch) {
+  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+  if ((threadIdx.x & 31) == 0) scratch[threadIdx.x >> 5] = v;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    int w = threadIdx.x < (blockDim.x >> 5) ? scratch[threadIdx.x] : INT_MIN;
+    for (int o = 16; o > 0; o >>= 1) w = max(w, __shfl_xor_sync(0xffffffffu, w, o));
+    if (threadIdx.x == 0) scratch[32] = w;
+  }
+  __syncthreads();
+  const int r = scratch[32];
+  __syncthreads();
+  return r;
+}
+// inclusive block scan of one value per thread (1024 threads)
+__device__ __forceinline__ int block_scan(int v, int* scan) {
+  const int tid = threadIdx.x;
+  scan[tid] = v;
+  __syncthreads();
+  for (int d = 1; d < 1024; d <<= 1) {
+    const int x = tid >= d ? scan[tid - d] : 0;
+    __syncthreads();
+    scan[tid] += x;
+    __syncthreads();
+  }
+  const int r = scan[tid];
+  __syncthreads();
+  return r;
+}
+
 __global__ void __launch_bounds__(1024)
     plan_kernel(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ block_table,
                 WsHeader* ws, int B, int Lq, int max_pages, int num_pages, int units) {
   __shared__ int scan[1024];
-  __shared__ int carry;
-  int* off = reinterpret_cast<int*>(ws + 1);
-  int* nlen = off + B + 1;
+  __shared__ int red[33];
+  __shared__ int carry, carry2;
+  const WsView v = ws_view(ws, B);
   const int tid = threadIdx.x;
-  if (tid == 0) carry = 0;
+  if (tid == 0) carry = carry2 = 0;
   __syncthreads();
   const int lo = Lq > 1 ? Lq : 1, hi = max_pages * kPage;
   for (int base = 0; base < B; base += 1024) {
@@ -643,35 +708,90 @@ __global__ void __launch_bounds__(1024)
         set_status(ws, MLA_ERR_BAD_SEQLEN);
         n = n < lo ? lo : hi;
       }
-      nlen[b] = n;
+      v.nlen[b] = n;
       np = (n + kPage - 1) / kPage;
     }
-    scan[tid] = np;
+    const int incl = block_scan(np, scan);
+    if (b < B) v.off[b] = carry + incl - np;
     __syncthreads();
-    for (int d = 1; d < 1024; d <<= 1) {
-      const int v = tid >= d ? scan[tid - d] : 0;
-      __syncthreads();
-      scan[tid] += v;
-      __syncthreads();
-    }
-    if (b < B) off[b] = carry + scan[tid] - np;
-    __syncthreads();
-    if (tid == 1023) carry += scan[1023];
+    if (tid == 1023) carry += incl;
     __syncthreads();
   }
+  const int total = carry;
+  const int chunk = total > 0 ? (total + units - 1) / units : 1;
+  if (tid == 0) v.off[B] = total;  // read below by every thread
+  __syncthreads();
+
+  // cost of the balanced split: pages per unit + switches inside a unit
+  int segs = 0;
+  for (int k = tid; k < units; k += 1024) {
+    const int st = min(k * chunk, total), en = min(st + chunk, total);
+    if (st < en) {
+      int l0 = 0, h0 = B - 1, l1 = 0, h1 = B - 1;
+      while (l0 < h0) { const int m = (l0 + h0 + 1) >> 1; if (v.off[m] <= st) l0 = m; else h0 = m - 1; }
+      while (l1 < h1) { const int m = (l1 + h1 + 1) >> 1; if (v.off[m] <= en - 1) l1 = m; else h1 = m - 1; }
+      segs = max(segs, l1 - l0 + 1);
+    }
+  }
+  segs = block_reduce_max(segs, red);
+  const int cost_bal = chunk + kSwitchPages * (segs - 1);
+
+  // cost of the sequence-aligned split
+  int cost_al = INT_MAX, used = 0;
+  if (B <= units && total > 0) {
+    int worst = 0;
+    for (int base = 0; base < B; base += 1024) {
+      const int b = base + tid;
+      int u = 0;
+      if (b < B) {
+        const int np = v.off[b + 1] - v.off[b];
+        u = min(np, max(1, (int)(((long long)units * np) / total)));
+        worst = max(worst, (np + u - 1) / u);
+      }
+      const int incl = block_scan(u, scan);
+      if (b < B) v.slot0[b] = carry2 + incl - u;  // first unit of b (kept if aligned wins)
+      __syncthreads();
+      if (tid == 1023) carry2 += incl;
+      __syncthreads();
+    }
+    used = carry2;
+    worst = block_reduce_max(worst, red);
+    if (used <= units) cost_al = worst;
+  }
+  const int mode = cost_al <= cost_bal ? 1 : 0;
+
+  for (int b = tid; b < B; b += 1024) {
+    const int o0 = v.off[b], np = v.off[b + 1] - o0;
+    if (mode == 1) {
+      const int u = min(np, max(1, (int)(((long long)units * np) / total)));
+      const int k0 = v.slot0[b];
+      v.nslot[b] = u;
+      for (int j = 0; j < u; ++j) {
+        v.ub[k0 + j] = b;
+        v.upa[k0 + j] = (int)(((long long)j * np) / u);
+        v.upb[k0 + j] = (int)(((long long)(j + 1) * np) / u);
+      }
+    } else {
+      const int kf = o0 / chunk, kl = (o0 + np - 1) / chunk;
+      v.slot0[b] = b + kf;
+      v.nslot[b] = kl - kf + 1;
+    }
+  }
+  if (mode == 1)
+    for (int k = used + tid; k < units; k += 1024) v.ub[k] = -1;
   if (tid == 0) {
-    off[B] = carry;
-    ws->total = carry;
-    ws->chunk = carry > 0 ? (carry + units - 1) / units : 1;
+    ws->total = total;
+    ws->chunk = chunk;
     ws->units = units;
     ws->B = B;
+    ws->mode = mode;
   }
   __syncthreads();
   // table entries actually used must name a real page
   const long long entries = (long long)B * max_pages;
   for (long long e = tid; e < entries; e += 1024) {
     const int b = (int)(e / max_pages), i = (int)(e % max_pages);
-    if (i * kPage < nlen[b]) {
+    if (i * kPage < v.nlen[b]) {
       const int pg = block_table[e];
       if (pg < 0 || pg >= num_pages) set_status(ws, MLA_ERR_BAD_TABLE);
     }
@@ -698,12 +818,9 @@ __global__ void __launch_bounds__(256)
   const int rows = Lq * H;
   const int b = blockIdx.x, r0 = blockIdx.y * kCombineRows, cz = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int* off = reinterpret_cast<const int*>(ws + 1);
-  const int chunk = ws->chunk;
-  const int o0 = off[b], np = off[b + 1] - o0;
-  const int kf = o0 / chunk, kl = (o0 + np - 1) / chunk;
-  const int nseg = kl - kf + 1;
-  const size_t seg0 = (size_t)b + kf;
+  const WsView v = ws_view(ws, B);
+  const int nseg = v.nslot[b];
+  const size_t seg0 = (size_t)v.slot0[b];
   const bool table = nseg <= kCombineMaxSeg;
 
   // log-sum-exp per row (warp w: rows w, w+8, w+16, w+24), then weights
@@ -812,6 +929,7 @@ int decode_max_units(int csize, int* units) {
   if (decode_config(cfg, attr, 1, csize, nullptr) != cudaSuccess) return MLA_ERR_CUDA;
   int n = 0;
   if (cudaOccupancyMaxActiveClusters(&n, decode_kernel, &cfg) != cudaSuccess || n < 1) return MLA_ERR_CUDA;
+  if (n > kMaxUnits) n = kMaxUnits;  // the workspace holds per-unit records for at most this many
   cache_dev[slot] = dev;
   cache_val[slot] = n;
   *units = n;

@@ -17,21 +17,48 @@ constexpr int kRow = kDc + kDr;  // 576 elements per cache row
 constexpr int kDhc = 128;      // content head dim
 constexpr int kRowsPerCta = 128;  // query rows (l, h) per CTA = MMA M
 
-// Decode workspace: header, then int off[B+1] (page offsets of each sequence
-// in the flattened page order, off[B] = total pages) and int nlen[B] (the
-// validated sequence lengths).
+// Decode workspace: a 32-byte header, then int arrays
+//   off[B+1]   page offset of each sequence in the flattened page order
+//              (off[B] = total pages)
+//   nlen[B]    validated sequence lengths
+//   slot0[B]   first partial-output slot of sequence b
+//   nslot[B]   number of partial-output slots of sequence b
+//   ub[kMaxUnits], upa[kMaxUnits], upb[kMaxUnits]
+//              sequence-aligned split only: the one (sequence, page range)
+//              each work unit decodes (ub = -1: idle unit)
+// Split modes: 0 = balanced (the flattened page list cut into equal
+// contiguous ranges, a range may cover several sequences; slot = b + unit),
+// 1 = sequence-aligned (every unit inside one sequence; slot = unit).
+constexpr int kMaxUnits = 256;
 struct WsHeader {
   int status;    // sticky device status (mla_status), 0 = ok
   int total;     // total pages over all sequences
-  int chunk;     // pages per work unit
+  int chunk;     // pages per work unit (balanced split)
   int units;     // work units (CTA clusters) of the last launch
   int B;
-  int pad[3];
+  int mode;      // 0 balanced, 1 sequence-aligned
+  int pad[2];
 };
 static_assert(sizeof(WsHeader) == 32, "header layout");
 
+struct WsView {
+  int *off, *nlen, *slot0, *nslot, *ub, *upa, *upb;
+};
+__host__ __device__ inline WsView ws_view(const WsHeader* ws, int B) {
+  int* p = const_cast<int*>(reinterpret_cast<const int*>(ws + 1));
+  WsView v;
+  v.off = p;
+  v.nlen = v.off + B + 1;
+  v.slot0 = v.nlen + B;
+  v.nslot = v.slot0 + B;
+  v.ub = v.nslot + B;
+  v.upa = v.ub + kMaxUnits;
+  v.upb = v.upa + kMaxUnits;
+  return v;
+}
+
 inline size_t ws_bytes_for(int B) {
-  size_t b = sizeof(WsHeader) + sizeof(int) * (size_t)(2 * B + 1);
+  size_t b = sizeof(WsHeader) + sizeof(int) * ((size_t)4 * B + 1 + 3 * kMaxUnits);
   return (b + 255) & ~(size_t)255;
 }
 
