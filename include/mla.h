@@ -106,6 +106,13 @@ int mla_absorb_q(const mla_dims* dims, const void* q_nope, const void* q_rope,
 int mla_decode_num_slots(const mla_dims* dims, int* slots);
 
 /*
+ * Number of kernels one mla_decode_paged call with these dims launches: 1
+ * when B <= 448 (the decode kernel computes its own split of the work), 2
+ * above that (a plan kernel runs first).  Host-only, launches nothing.
+ */
+int mla_decode_kernel_launches(const mla_dims* dims, int* launches);
+
+/*
  * Bytes of workspace mla_decode_paged needs (split plan + sticky status
  * word).  The caller allocates it, zero-fills it ONCE (that clears the status
  * word) and may reuse it for any number of calls with the same or smaller

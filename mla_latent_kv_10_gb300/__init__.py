@@ -14,7 +14,8 @@ import os
 __all__ = [
     "MLAError", "Dims", "load_library", "library_path",
     "mla_absorb_q", "mla_decode_paged", "mla_combine_splits", "mla_project_uv",
-    "mla_decode_workspace_size", "mla_decode_num_slots", "mla_get_device_status",
+    "mla_decode_workspace_size", "mla_decode_num_slots", "mla_decode_kernel_launches",
+    "launches_per_step", "mla_get_device_status",
     "mla_status_string", "make_dims", "DecodeBuffers", "decode_step",
 ]
 
@@ -55,6 +56,7 @@ def load_library():
     sig = {
         "mla_absorb_q": [DP, P, P, P, P, P],
         "mla_decode_num_slots": [DP, ctypes.POINTER(I)],
+        "mla_decode_kernel_launches": [DP, ctypes.POINTER(I)],
         "mla_decode_workspace_size": [DP, ctypes.POINTER(S)],
         "mla_decode_paged": [DP, P, P, P, P, I, P, P, P, S, P],
         "mla_combine_splits": [DP, P, P, P, S, P, P, P],
@@ -123,6 +125,19 @@ def mla_decode_num_slots(dims) -> int:
     n = ctypes.c_int(0)
     _check(load_library().mla_decode_num_slots(_dims(dims), ctypes.byref(n)), "mla_decode_num_slots")
     return n.value
+
+
+def mla_decode_kernel_launches(dims) -> int:
+    n = ctypes.c_int(0)
+    _check(load_library().mla_decode_kernel_launches(_dims(dims), ctypes.byref(n)),
+           "mla_decode_kernel_launches")
+    return n.value
+
+
+def launches_per_step(dims) -> int:
+    """Kernel launches of one decode_step: absorb, decode (+ plan), combine,
+    project."""
+    return 3 + mla_decode_kernel_launches(dims)
 
 
 def mla_decode_paged(dims, q_cat, kv_cache, block_table, seq_lens, num_splits, o_part, lse_part,

@@ -145,6 +145,14 @@ int mla_decode_num_slots(const mla_dims* d, int* slots) {
   return MLA_OK;
 }
 
+int mla_decode_kernel_launches(const mla_dims* d, int* launches) {
+  int rc = check_dims(d);
+  if (rc != MLA_OK) return rc;
+  if (!launches) return MLA_ERR_INVALID_ARG;
+  *launches = d->B <= kPlanInKernelMaxB ? 1 : 2;
+  return MLA_OK;
+}
+
 int mla_decode_paged(const mla_dims* d, const void* q_cat, const void* kv_cache,
                      const int32_t* block_table, const int32_t* seq_lens, int num_splits,
                      float* o_part, float* lse_part, void* workspace, size_t ws_bytes, void* stream) {
@@ -170,9 +178,14 @@ int mla_decode_paged(const mla_dims* d, const void* q_cat, const void* kv_cache,
     if ((rc = make_map(&tm, kv_cache, 2, dims, strides, box)) != MLA_OK) return rc;
   }
   auto* ws = static_cast<WsHeader*>(workspace);
-  cudaError_t e = launch_plan(seq_lens, block_table, ws, d->B, d->Lq, d->max_pages_per_seq,
-                              d->num_pages, units, st);
-  if (e != cudaSuccess) return MLA_ERR_CUDA;
+  // Small batches are split by the decode kernel itself (one launch);
+  // larger ones by the separate plan kernel.
+  const bool in_kernel = d->B <= kPlanInKernelMaxB;
+  if (!in_kernel) {
+    cudaError_t e = launch_plan(seq_lens, block_table, ws, d->B, d->Lq, d->max_pages_per_seq,
+                                d->num_pages, units, st);
+    if (e != cudaSuccess) return MLA_ERR_CUDA;
+  }
   DecodeArgs a;
   a.q_cat = static_cast<const __nv_bfloat16*>(q_cat);
   a.block_table = block_table;
@@ -189,6 +202,9 @@ int mla_decode_paged(const mla_dims* d, const void* q_cat, const void* kv_cache,
   a.causal = d->causal ? 1 : 0;
   a.rows = d->Lq * d->H;
   a.scale_log2 = d->scale * 1.4426950408889634f;
+  a.plan_in_kernel = in_kernel ? 1 : 0;
+  a.units = units;
+  a.seq_lens = seq_lens;
   return cuda_status(launch_decode(tm, a, units, csize, st));
 }
 

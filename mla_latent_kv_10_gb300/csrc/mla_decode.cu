@@ -125,6 +125,7 @@ struct DecodeShared {
   // [page parity][column half][row]: half-row maxima (half-row sums at the
   // epilogue use the parity after the segment's last page)
   float red[2][2][kRowsPerCta];
+  UnitRec rec;  // this CTA's work unit
   uint32_t tmem;
   int abort;
 };
@@ -133,60 +134,183 @@ struct DecodeShared {
 constexpr int kDecodeSmem = kSmemShared + (int)((sizeof(DecodeShared) + 15) & ~size_t(15));
 static_assert(kDecodeSmem <= 232448, "decode kernel exceeds 227 KiB of shared memory");
 
-// Walks the (sequence, page range) segments of one work unit.
+__device__ __forceinline__ int clamp_len(int n, int lo, int hi) { return n < lo ? lo : (n > hi ? hi : n); }
+// units given to a sequence of np pages by the sequence-aligned split
+__device__ __forceinline__ int aligned_units(int np, int units, int total) {
+  return min(np, max(1, (int)(((long long)units * np) / total)));
+}
+
+// Walks the (sequence, page range) segments of one work unit from its
+// UnitRec, reading page counts from seq_lens (validated lengths).
 struct SegIter {
-  WsView v;
-  int B, unit, mode, start, end, b;
-  __device__ void init(const WsHeader* ws, int u) {
-    B = ws->B;
-    unit = u;
-    mode = ws->mode;
-    v = ws_view(ws, B);
-    if (mode == 1) {  // sequence-aligned: at most one segment
-      b = v.ub[unit];
-      start = b >= 0 ? v.upa[unit] : 0;
-      end = b >= 0 ? v.upb[unit] : 0;
-      return;
-    }
-    const int total = ws->total, chunk = ws->chunk;
-    start = min(unit * chunk, total);
-    end = min(start + chunk, total);
-    // largest b with off[b] <= start
-    int lo = 0, hi = B - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (v.off[mid] <= start) lo = mid; else hi = mid - 1;
-    }
-    b = lo;
+  const int32_t* sl;
+  int B, lo, hi, b, o, start, end, bias;
+  __device__ void init(const UnitRec& r, const DecodeArgs& a) {
+    sl = a.seq_lens;
+    B = a.B;
+    lo = a.Lq > 1 ? a.Lq : 1;
+    hi = a.max_pages * kPage;
+    b = r.b; o = r.o; start = r.start; end = r.end; bias = r.bias;
   }
   __device__ int total_pages() const { return end - start; }
-  // partial-output slot of a segment of sequence sb
-  __device__ int slot(int sb) const { return mode == 1 ? unit : sb + unit; }
+  __device__ int slot(int sb) const { return sb + bias; }
+  __device__ int len(int sb) const { return clamp_len(sl[sb], lo, hi); }
   // Next non-empty segment: sequence sb, pages [pa, pb) of that sequence.
   __device__ bool next(int& sb, int& pa, int& pb) {
-    if (mode == 1) {
-      if (b < 0 || start >= end) return false;
-      sb = b;
-      pa = start;
-      pb = end;
-      b = -1;
-      return true;
-    }
     while (b < B && start < end) {
-      const int o0 = v.off[b], o1 = v.off[b + 1];
-      const int a = max(start, o0), e = min(end, o1);
+      const int o0 = o;
+      if (o0 >= end) break;
+      const int o1 = o0 + (len(b) + kPage - 1) / kPage;
+      const int aa = max(start, o0), e = min(end, o1);
       const int cur = b++;
-      if (a < e) {
+      o = o1;
+      if (aa < e) {
         sb = cur;
-        pa = a - o0;
+        pa = aa - o0;
         pb = e - o0;
         return true;
       }
-      if (o0 >= end) break;
     }
     return false;
   }
 };
+
+// ---- small block-wide helpers (all threads of the block call them)
+__device__ __forceinline__ int block_reduce_max(int v, int* scratch) {
+  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+  if ((threadIdx.x & 31) == 0) scratch[threadIdx.x >> 5] = v;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    int w = threadIdx.x < (int)(blockDim.x >> 5) ? scratch[threadIdx.x] : INT_MIN;
+    for (int o = 16; o > 0; o >>= 1) w = max(w, __shfl_xor_sync(0xffffffffu, w, o));
+    if (threadIdx.x == 0) scratch[32] = w;
+  }
+  __syncthreads();
+  const int r = scratch[32];
+  __syncthreads();
+  return r;
+}
+// inclusive block scan of one value per thread; *total receives the sum
+__device__ __forceinline__ int block_scan_incl(int v, int* scratch, int* total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int x = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += x;
+  }
+  if (lane == 31) scratch[w] = v;
+  __syncthreads();
+  if (w == 0) {
+    int t = lane < nw ? scratch[lane] : 0;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int x = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += x;
+    }
+    if (lane < nw) scratch[lane] = t;
+    if (lane == nw - 1) scratch[32] = t;
+  }
+  __syncthreads();
+  if (w > 0) v += scratch[w - 1];
+  *total = scratch[32];
+  __syncthreads();
+  return v;
+}
+
+constexpr int kSwitchPages = 4;  // cost of a sequence switch inside a unit, in pages
+
+// The split of mla_decode_paged's work, computed by one block with one
+// thread per sequence (B <= blockDim.x): validated lengths, page prefix sums,
+// the cheaper of the balanced and sequence-aligned splits (see plan_kernel),
+// and this unit's UnitRec.  `writer` also stores the per-sequence slot
+// ranges and the header for the combine kernel.  scr: >= 3*B + 3 ints of
+// shared scratch; red: 33 ints.
+__device__ void plan_in_block(const DecodeArgs& a, int unit, bool writer, int* scr, int* red, UnitRec* out) {
+  const int B = a.B, units = a.units, tid = threadIdx.x;
+  const WsView v = ws_view(a.ws, B);
+  int* off_s = scr;            // [B+1]
+  int* u0_s = scr + B + 1;     // [B+1]
+  const int lo = a.Lq > 1 ? a.Lq : 1, hi = a.max_pages * kPage;
+  int np = 0;
+  if (tid < B) {
+    const int n0 = a.seq_lens[tid];
+    const int n = clamp_len(n0, lo, hi);
+    if (writer) {
+      if (n != n0) set_status(a.ws, MLA_ERR_BAD_SEQLEN);
+      v.nlen[tid] = n;
+    }
+    np = (n + kPage - 1) / kPage;
+  }
+  int total = 0;
+  const int incl = block_scan_incl(np, red, &total);
+  if (tid < B) off_s[tid] = incl - np;
+  if (tid == 0) off_s[B] = total;
+  __syncthreads();
+  const int chunk = total > 0 ? (total + units - 1) / units : 1;
+
+  int segs = 0;  // balanced split: most sequences one unit touches
+  for (int k = tid; k < units; k += blockDim.x) {
+    const int st = min(k * chunk, total), en = min(st + chunk, total);
+    if (st < en) {
+      int l0 = 0, h0 = B - 1, l1 = 0, h1 = B - 1;
+      while (l0 < h0) { const int m = (l0 + h0 + 1) >> 1; if (off_s[m] <= st) l0 = m; else h0 = m - 1; }
+      while (l1 < h1) { const int m = (l1 + h1 + 1) >> 1; if (off_s[m] <= en - 1) l1 = m; else h1 = m - 1; }
+      segs = max(segs, l1 - l0 + 1);
+    }
+  }
+  segs = block_reduce_max(segs, red);
+  const int cost_bal = chunk + kSwitchPages * (segs - 1);
+
+  const bool feasible = B <= units && total > 0;
+  int u = 0, worst = 0, used = 0;
+  if (feasible && tid < B) {
+    u = aligned_units(np, units, total);
+    worst = (np + u - 1) / u;
+  }
+  const int uincl = block_scan_incl(u, red, &used);
+  if (tid < B) u0_s[tid] = uincl - u;
+  worst = block_reduce_max(worst, red);
+  const int cost_al = (feasible && used <= units) ? worst : INT_MAX;
+  const int mode = cost_al <= cost_bal ? 1 : 0;
+
+  if (tid == 0) {
+    UnitRec rec{0, 0, 0, 0, 0};
+    if (mode == 1) {
+      if (unit < used) {
+        int l0 = 0, h0 = B - 1;
+        while (l0 < h0) { const int m = (l0 + h0 + 1) >> 1; if (u0_s[m] <= unit) l0 = m; else h0 = m - 1; }
+        const int nb = off_s[l0 + 1] - off_s[l0], ub = aligned_units(nb, units, total), j = unit - u0_s[l0];
+        rec = UnitRec{l0, 0, (int)(((long long)j * nb) / ub), (int)(((long long)(j + 1) * nb) / ub), unit - l0};
+      }
+    } else {
+      const int st = min(unit * chunk, total), en = min(st + chunk, total);
+      int l0 = 0, h0 = B - 1;
+      while (l0 < h0) { const int m = (l0 + h0 + 1) >> 1; if (off_s[m] <= st) l0 = m; else h0 = m - 1; }
+      rec = UnitRec{l0, off_s[l0], st, en, unit};
+    }
+    *out = rec;
+  }
+  if (writer) {
+    if (tid < B) {
+      v.off[tid] = off_s[tid];
+      if (mode == 1) {
+        v.slot0[tid] = u0_s[tid];
+        v.nslot[tid] = u;
+      } else {
+        const int o0 = off_s[tid], kf = o0 / chunk, kl = (o0 + np - 1) / chunk;
+        v.slot0[tid] = tid + kf;
+        v.nslot[tid] = kl - kf + 1;
+      }
+    }
+    if (tid == 0) {
+      v.off[B] = total;
+      a.ws->total = total;
+      a.ws->chunk = chunk;
+      a.ws->units = units;
+      a.ws->B = B;
+      a.ws->mode = mode;
+    }
+  }
+  __syncthreads();
+}
 
 __global__ void __launch_bounds__(kDecodeThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tm_cache, const DecodeArgs a) {
@@ -208,7 +332,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   const uint32_t peer = crank ^ 1u;
   const int unit = (int)cluster_id_x();
   WsHeader* ws = a.ws;
-  const int* nlen = ws_view(ws, a.B).nlen;
 
   auto bar = [](uint64_t& x) { return smem_u32(&x); };
 
@@ -245,6 +368,16 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   const uint32_t tmem = sh.tmem;
   volatile int* abort = &sh.abort;
 
+  // the work split: computed here (the exchange slots are still unused and
+  // serve as scratch), or read from the plan kernel's records
+  if (a.plan_in_kernel) {
+    plan_in_block(a, unit, unit == 0 && crank == 0, reinterpret_cast<int*>(xbuf),
+                  reinterpret_cast<int*>(xbuf) + 3 * a.B + 8, &sh.rec);
+  } else if (threadIdx.x == 0) {
+    sh.rec = ws_view(ws, a.B).rec[unit];
+  }
+  __syncthreads();
+
   auto fail = [&]() {
     *abort = 1;
     set_status(ws, MLA_ERR_TIMEOUT);
@@ -257,7 +390,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       const uint32_t bytes = 5 * kBoxBytes;
       const uint64_t policy = l2_policy_evict_first();
       SegIter it;
-      it.init(ws, unit);
+      it.init(sh.rec, a);
       int sb, pa, pb;
       uint32_t pc = 0;
       bool ok = true;
@@ -270,7 +403,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             break;
           }
           int page = bt[i];
-          if (page < 0 || page >= a.num_pages) page = 0;  // reported by the plan kernel
+          if (page < 0 || page >= a.num_pages) {  // never dereferenced: clamped and reported
+            set_status(ws, MLA_ERR_BAD_TABLE);
+            page = 0;
+          }
           const uint32_t dst = smem_u32(stages + st * kStageBytes);
           mbar_arrive_expect_tx(bar(sh.full[st]), bytes);
           for (int j = 0; j < 4; ++j)  // this CTA's latent half
@@ -302,7 +438,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       constexpr uint32_t idesc_qk = idesc_bf16(128, 64, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16(128, 256, false, true);
       SegIter it;
-      it.init(ws, unit);
+      it.init(sh.rec, a);
       int sb, pa, pb;
       uint32_t pc = 0, qc = 0;
       bool ok = true;
@@ -361,7 +497,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     const uint32_t peer_recv = mapa(xrecv, peer);
     const uint32_t peer_xfull0 = mapa(bar(sh.xfull[0]), peer), peer_xfull1 = mapa(bar(sh.xfull[1]), peer);
     SegIter it;
-    it.init(ws, unit);
+    it.init(sh.rec, a);
     const int npages = it.end - it.start;
     bool ok = true;
     for (int q = 0; q < npages; ++q) {
@@ -430,7 +566,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     const uint32_t pair_bar = kBarPair0 + quad;
     const int d_q = a.d_g + kDr;
     SegIter it;
-    it.init(ws, unit);
+    it.init(sh.rec, a);
     int sb, pa, pb;
     uint32_t q = 0, od = 0;
     bool ok = true;
@@ -487,7 +623,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     if (have) load_q(sb);
     while (have) {
       const int seg = it.slot(sb);
-      const int n = nlen[sb];
+      const int n = it.len(sb);
       const int limit = a.causal ? n - a.Lq + l + 1 : n;  // keys [0, limit) visible
       float m_used = -INFINITY, l_part = 0.f;
       SegIter peek = it;
@@ -649,49 +785,18 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 }
 
 // ---------------------------------------------------------------- plan
-// One CTA: validates lengths and table entries, prefix-sums pages per
-// sequence and splits the work over `units` clusters.  Two splits are
-// costed (in pages, a switch between sequences inside a unit counting
-// kSwitchPages) and the cheaper one is written:
+// One CTA; used when B is too large for the decode kernel to plan for
+// itself.  Validates lengths and table entries, prefix-sums pages per
+// sequence and splits the work over `units` clusters with the same rules as
+// plan_in_block: two splits are costed in pages (a switch between sequences
+// inside a unit counting kSwitchPages) and the cheaper one is written:
 //   balanced  — the flattened page list cut into equal contiguous ranges;
 //   aligned   — each sequence gets max(1, floor(units * pages_b / total))
 //               whole units, at most one per page (needs B <= units), and
 //               splits its pages evenly over them.
-constexpr int kSwitchPages = 4;
-__device__ __forceinline__ int block_reduce_max(int v, int* scratch) {
-  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
-  if ((threadIdx.x & 31) == 0) scratch[threadIdx.x >> 5] = v;
-  __syncthreads();
-  if (threadIdx.x < 32) {
-    int w = threadIdx.x < (blockDim.x >> 5) ? scratch[threadIdx.x] : INT_MIN;
-    for (int o = 16; o > 0; o >>= 1) w = max(w, __shfl_xor_sync(0xffffffffu, w, o));
-    if (threadIdx.x == 0) scratch[32] = w;
-  }
-  __syncthreads();
-  const int r = scratch[32];
-  __syncthreads();
-  return r;
-}
-// inclusive block scan of one value per thread (1024 threads)
-__device__ __forceinline__ int block_scan(int v, int* scan) {
-  const int tid = threadIdx.x;
-  scan[tid] = v;
-  __syncthreads();
-  for (int d = 1; d < 1024; d <<= 1) {
-    const int x = tid >= d ? scan[tid - d] : 0;
-    __syncthreads();
-    scan[tid] += x;
-    __syncthreads();
-  }
-  const int r = scan[tid];
-  __syncthreads();
-  return r;
-}
-
 __global__ void __launch_bounds__(1024)
     plan_kernel(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ block_table,
                 WsHeader* ws, int B, int Lq, int max_pages, int num_pages, int units) {
-  __shared__ int scan[1024];
   __shared__ int red[33];
   __shared__ int carry, carry2;
   const WsView v = ws_view(ws, B);
@@ -703,18 +808,16 @@ __global__ void __launch_bounds__(1024)
     const int b = base + tid;
     int np = 0;
     if (b < B) {
-      int n = seq_lens[b];
-      if (n < lo || n > hi) {
-        set_status(ws, MLA_ERR_BAD_SEQLEN);
-        n = n < lo ? lo : hi;
-      }
+      const int n0 = seq_lens[b], n = clamp_len(n0, lo, hi);
+      if (n != n0) set_status(ws, MLA_ERR_BAD_SEQLEN);
       v.nlen[b] = n;
       np = (n + kPage - 1) / kPage;
     }
-    const int incl = block_scan(np, scan);
+    int sum = 0;
+    const int incl = block_scan_incl(np, red, &sum);
     if (b < B) v.off[b] = carry + incl - np;
     __syncthreads();
-    if (tid == 1023) carry += incl;
+    if (tid == 0) carry += sum;
     __syncthreads();
   }
   const int total = carry;
@@ -722,7 +825,6 @@ __global__ void __launch_bounds__(1024)
   if (tid == 0) v.off[B] = total;  // read below by every thread
   __syncthreads();
 
-  // cost of the balanced split: pages per unit + switches inside a unit
   int segs = 0;
   for (int k = tid; k < units; k += 1024) {
     const int st = min(k * chunk, total), en = min(st + chunk, total);
@@ -736,7 +838,6 @@ __global__ void __launch_bounds__(1024)
   segs = block_reduce_max(segs, red);
   const int cost_bal = chunk + kSwitchPages * (segs - 1);
 
-  // cost of the sequence-aligned split
   int cost_al = INT_MAX, used = 0;
   if (B <= units && total > 0) {
     int worst = 0;
@@ -745,13 +846,14 @@ __global__ void __launch_bounds__(1024)
       int u = 0;
       if (b < B) {
         const int np = v.off[b + 1] - v.off[b];
-        u = min(np, max(1, (int)(((long long)units * np) / total)));
+        u = aligned_units(np, units, total);
         worst = max(worst, (np + u - 1) / u);
       }
-      const int incl = block_scan(u, scan);
+      int sum = 0;
+      const int incl = block_scan_incl(u, red, &sum);
       if (b < B) v.slot0[b] = carry2 + incl - u;  // first unit of b (kept if aligned wins)
       __syncthreads();
-      if (tid == 1023) carry2 += incl;
+      if (tid == 0) carry2 += sum;
       __syncthreads();
     }
     used = carry2;
@@ -763,22 +865,31 @@ __global__ void __launch_bounds__(1024)
   for (int b = tid; b < B; b += 1024) {
     const int o0 = v.off[b], np = v.off[b + 1] - o0;
     if (mode == 1) {
-      const int u = min(np, max(1, (int)(((long long)units * np) / total)));
-      const int k0 = v.slot0[b];
-      v.nslot[b] = u;
-      for (int j = 0; j < u; ++j) {
-        v.ub[k0 + j] = b;
-        v.upa[k0 + j] = (int)(((long long)j * np) / u);
-        v.upb[k0 + j] = (int)(((long long)(j + 1) * np) / u);
-      }
+      v.nslot[b] = aligned_units(np, units, total);
     } else {
       const int kf = o0 / chunk, kl = (o0 + np - 1) / chunk;
       v.slot0[b] = b + kf;
       v.nslot[b] = kl - kf + 1;
     }
   }
-  if (mode == 1)
-    for (int k = used + tid; k < units; k += 1024) v.ub[k] = -1;
+  __syncthreads();
+  for (int k = tid; k < units; k += 1024) {
+    UnitRec rec{0, 0, 0, 0, 0};
+    if (mode == 1) {
+      if (k < used) {
+        int l0 = 0, h0 = B - 1;
+        while (l0 < h0) { const int m = (l0 + h0 + 1) >> 1; if (v.slot0[m] <= k) l0 = m; else h0 = m - 1; }
+        const int nb = v.off[l0 + 1] - v.off[l0], ub = v.nslot[l0], j = k - v.slot0[l0];
+        rec = UnitRec{l0, 0, (int)(((long long)j * nb) / ub), (int)(((long long)(j + 1) * nb) / ub), k - l0};
+      }
+    } else {
+      const int st = min(k * chunk, total), en = min(st + chunk, total);
+      int l0 = 0, h0 = B - 1;
+      while (l0 < h0) { const int m = (l0 + h0 + 1) >> 1; if (v.off[m] <= st) l0 = m; else h0 = m - 1; }
+      rec = UnitRec{l0, v.off[l0], st, en, k};
+    }
+    v.rec[k] = rec;
+  }
   if (tid == 0) {
     ws->total = total;
     ws->chunk = chunk;

@@ -23,9 +23,8 @@ constexpr int kRowsPerCta = 128;  // query rows (l, h) per CTA = MMA M
 //   nlen[B]    validated sequence lengths
 //   slot0[B]   first partial-output slot of sequence b
 //   nslot[B]   number of partial-output slots of sequence b
-//   ub[kMaxUnits], upa[kMaxUnits], upb[kMaxUnits]
-//              sequence-aligned split only: the one (sequence, page range)
-//              each work unit decodes (ub = -1: idle unit)
+//   rec[kMaxUnits]  one UnitRec per work unit (written by the plan kernel
+//              when the decode kernel does not plan for itself)
 // Split modes: 0 = balanced (the flattened page list cut into equal
 // contiguous ranges, a range may cover several sequences; slot = b + unit),
 // 1 = sequence-aligned (every unit inside one sequence; slot = unit).
@@ -41,8 +40,17 @@ struct WsHeader {
 };
 static_assert(sizeof(WsHeader) == 32, "header layout");
 
+// The pages one work unit decodes: starting at sequence b, whose first page
+// sits at flattened offset o, the unit covers flattened pages [start, end)
+// (sequence-aligned split: o = 0 and [start, end) are pages of sequence b).
+// The partial of a segment of sequence sb goes to slot sb + bias.
+struct UnitRec {
+  int b, o, start, end, bias;
+};
+
 struct WsView {
-  int *off, *nlen, *slot0, *nslot, *ub, *upa, *upb;
+  int *off, *nlen, *slot0, *nslot;
+  UnitRec* rec;
 };
 __host__ __device__ inline WsView ws_view(const WsHeader* ws, int B) {
   int* p = const_cast<int*>(reinterpret_cast<const int*>(ws + 1));
@@ -51,14 +59,12 @@ __host__ __device__ inline WsView ws_view(const WsHeader* ws, int B) {
   v.nlen = v.off + B + 1;
   v.slot0 = v.nlen + B;
   v.nslot = v.slot0 + B;
-  v.ub = v.nslot + B;
-  v.upa = v.ub + kMaxUnits;
-  v.upb = v.upa + kMaxUnits;
+  v.rec = reinterpret_cast<UnitRec*>(v.nslot + B);
   return v;
 }
 
 inline size_t ws_bytes_for(int B) {
-  size_t b = sizeof(WsHeader) + sizeof(int) * ((size_t)4 * B + 1 + 3 * kMaxUnits);
+  size_t b = sizeof(WsHeader) + sizeof(int) * ((size_t)4 * B + 1) + sizeof(UnitRec) * kMaxUnits;
   return (b + 255) & ~(size_t)255;
 }
 
@@ -70,7 +76,11 @@ struct DecodeArgs {
   WsHeader* ws;
   int B, Lq, H, G, d_g, max_pages, num_pages, causal, rows;  // rows = Lq*H
   float scale_log2;   // scale * log2(e)
+  int plan_in_kernel; // 1: every CTA computes the split itself (B <= kPlanInKernelMaxB)
+  int units;
+  const int32_t* seq_lens;
 };
+constexpr int kPlanInKernelMaxB = 448;  // one sequence per decode-kernel thread
 
 // launchers (return cudaError_t of the launch)
 cudaError_t launch_absorb(const CUtensorMap& tmA, const CUtensorMap& tmB, const void* q_rope,

@@ -57,7 +57,7 @@ A16 = P(0x10000)      # aligned fake device addresses (never dereferenced)
 A8 = P(0x10008)
 
 
-def decode(lib, d, q=A16, cache=A16, bt=A16, sl=A16, splits=0, op=A16, lp=A16, ws=A16, wsb=4096):
+def decode(lib, d, q=A16, cache=A16, bt=A16, sl=A16, splits=0, op=A16, lp=A16, ws=A16, wsb=1 << 20):
     return lib.mla_decode_paged(ctypes.byref(d), q, cache, bt, sl, splits, op, lp, ws, wsb, None)
 
 

@@ -78,6 +78,21 @@ def test_decode_step_small(name):
     check_case(c, got, sample_pairs(c, heads))
 
 
+@pytest.mark.parametrize("B,Lq", [(448, 2), (600, 1)])
+def test_decode_large_batch(B, Lq):
+    """Batches at the largest size the decode kernel splits by itself (448)
+    and above it (600, split by the separate plan kernel): ragged lengths,
+    shuffled pages, every sequence checked on a few heads."""
+    rng = np.random.default_rng(B)
+    lens = [int(x) for x in rng.integers(Lq, 200, size=B)]
+    lens[0], lens[-1] = Lq, 64
+    c = make_case(B=B, Lq=Lq, H=16, seq_lens=lens, table="perm", seed=47 + B)
+    got = run_gpu(c)
+    assert got["status"] == 0
+    pairs = [(b, h) for b in range(B) for h in (0, 7, 15)]
+    check_case(c, got, pairs)
+
+
 @pytest.mark.parametrize("splits", [1, 3, 7])
 def test_split_count_invariance(splits):
     """Any number of work units gives the same result (fp32 merge order
