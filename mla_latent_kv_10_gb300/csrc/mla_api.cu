@@ -27,15 +27,16 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// bf16 tensor map with 128-byte swizzle; dims innermost first; strides in
-// bytes for dims 1..rank-1.
+// bf16 tensor map (128-byte swizzle unless told otherwise); dims innermost
+// first; strides in bytes for dims 1..rank-1.
 int make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
-             const cuuint64_t* strides, const cuuint32_t* box) {
+             const cuuint64_t* strides, const cuuint32_t* box,
+             CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
   auto fn = encode_fn();
   if (!fn) return MLA_ERR_CUDA;
   cuuint32_t elem[3] = {1, 1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides,
-                  box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_CUDA;
 }
@@ -170,12 +171,22 @@ int mla_decode_paged(const mla_dims* d, const void* q_cat, const void* kv_cache,
   if ((rc = decode_max_units(csize, &units)) != MLA_OK) return rc;
   if (num_splits > 0 && num_splits < units) units = num_splits;
   auto st = static_cast<cudaStream_t>(stream);
-  CUtensorMap tm;
+  CUtensorMap tm, tm_rope, tm_qrope;
   {
     cuuint64_t dims[2] = {(cuuint64_t)kRow, (cuuint64_t)d->num_pages * kPage};
     cuuint64_t strides[1] = {(cuuint64_t)kRow * 2};
     cuuint32_t box[2] = {64, kPage};
     if ((rc = make_map(&tm, kv_cache, 2, dims, strides, box)) != MLA_OK) return rc;
+    cuuint32_t rbox[2] = {32, kPage};
+    if ((rc = make_map(&tm_rope, kv_cache, 2, dims, strides, rbox, CU_TENSOR_MAP_SWIZZLE_64B)) != MLA_OK)
+      return rc;
+  }
+  {
+    const int d_q = kDc / d->G + kDr;
+    cuuint64_t dims[2] = {(cuuint64_t)d_q, (cuuint64_t)d->B * d->Lq * d->H};
+    cuuint64_t strides[1] = {(cuuint64_t)d_q * 2};
+    cuuint32_t box[2] = {32, kRowsPerCta};
+    if ((rc = make_map(&tm_qrope, q_cat, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B)) != MLA_OK) return rc;
   }
   auto* ws = static_cast<WsHeader*>(workspace);
   // Small batches are split by the decode kernel itself (one launch);
@@ -205,7 +216,7 @@ int mla_decode_paged(const mla_dims* d, const void* q_cat, const void* kv_cache,
   a.plan_in_kernel = in_kernel ? 1 : 0;
   a.units = units;
   a.seq_lens = seq_lens;
-  return cuda_status(launch_decode(tm, a, units, csize, st));
+  return cuda_status(launch_decode(tm, tm_rope, tm_qrope, a, units, csize, st));
 }
 
 int mla_combine_splits(const mla_dims* d, const float* o_part, const float* lse_part,

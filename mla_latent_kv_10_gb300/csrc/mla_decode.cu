@@ -13,24 +13,29 @@
 //   * An fp32 accumulator O of 128 rows x 512 latents would fill all 512
 //     tensor-memory columns of an SM, so each 128-row block runs on a CTA
 //     PAIR (cluster rank bit 0 = r): CTA r owns latent half r (256 columns of
-//     O) and loads only its half of each page (CTA 0 also loads the RoPE
-//     columns).  Each CTA computes a partial score tile over its columns, in
+//     O) and loads only its half of each page plus half of the 64 RoPE
+//     columns.  Each CTA computes a partial score tile over its columns, in
 //     log2 units, rounds it to fp16 and sends it to the peer with one bulk
 //     shared-to-shared copy (16 KiB per page); both CTAs add the same two
 //     fp16 partials, so they hold bit-identical scores and run the same
 //     online softmax.  The exchange is double-buffered and the softmax warps
 //     run one page behind the exchange, so the copy of page q overlaps the
 //     softmax of page q-1.
-//   * Tensor memory per CTA: O (256 cols) | Q (<=160 cols, bf16 pairs, the
-//     MMA A operand) | S (64 cols) | P (32 cols, bf16 pairs, A operand of
-//     the P.V MMA).  The page tile in shared memory is used twice: K-major as
-//     B for S = Q.K^T and MN-major as B for O += P.V.
-//   * Pages arrive by TMA (64 x 64 bf16 boxes, 128-byte swizzle) into a
-//     4-stage mbarrier ring; one thread issues MMAs, one thread issues copies,
-//     four warps (one TMEM lane quadrant each, one thread per query row) do
-//     the exchange, masking, online softmax and epilogue.  Rescaling of O
-//     after a new row maximum is deferred until the maximum has grown by
-//     2^8 (log2 units), so it is rare.
+//   * Tensor memory per CTA (all 512 columns): O (256) | Q latent half (128,
+//     bf16 pairs, the MMA A operand) | S (64) | two P buffers (32 each, bf16
+//     pairs, A operand of the P.V MMA).  The RoPE half of Q is a 64-byte
+//     swizzled tile in shared memory (A operand of the last two K steps).
+//     The page tile in shared memory is used twice: K-major as B for
+//     S = Q.K^T and MN-major as B for O += P.V.  With two P buffers the
+//     softmax of page q+1 never waits for P.V of page q.
+//   * Pages arrive by TMA (four 64 x 64 latent boxes with 128-byte swizzle,
+//     one 32 x 64 RoPE box with 64-byte swizzle) into a 4-stage mbarrier
+//     ring; one thread issues MMAs, one thread issues copies, four exchange
+//     warps move partial scores, eight softmax warps (two per TMEM lane
+//     quadrant, one query row and half the page's keys per thread) do the
+//     masking, online softmax and epilogue.  Rescaling of O after a new row
+//     maximum is deferred until the maximum has grown by 2^8 (log2 units),
+//     so it is rare.
 //   * Split-KV: the pages of all sequences, in order, are cut into equal
 //     contiguous ranges, one per cluster; a range that covers parts of several
 //     sequences yields one partial (o, lse) per sequence, stored in slot
@@ -49,20 +54,35 @@ namespace mla {
 namespace {
 
 constexpr int kStages = 4;
-constexpr int kBoxBytes = kPage * 64 * 2;       // 64 tokens x 64 bf16 = 8 KiB
-constexpr int kStageBytes = 5 * kBoxBytes;      // latent half (4 boxes) + RoPE box
-constexpr int kXSlot = kRowsPerCta * 64 * 2;    // one fp16 partial-score tile, 16 KiB
-constexpr int kSmemShared = kStages * kStageBytes + 4 * kXSlot;  // offset of DecodeShared (2 send + 2 receive slots before it)
-// warps 0-3: exchange warps (one per TMEM lane quadrant); warps 4-11: softmax
-// warps (two per quadrant); warp 12: TMA producer; warp 13: MMA issuer
-constexpr int kXWarps = 4, kSWarps = 8;
-constexpr int kXThreads = 32 * kXWarps, kSoftmaxThreads = 32 * kSWarps;
-constexpr int kTmaWarp = kXWarps + kSWarps, kMmaWarp = kTmaWarp + 1;
-constexpr int kDecodeThreads = 32 * (kMmaWarp + 1);
-// named barriers: 1 = exchange warps, 2..5 = softmax warp pair of a quadrant,
-// 6 = all softmax warps
-constexpr uint32_t kBarX = 1, kBarPair0 = 2, kBarS = 6;
-constexpr uint32_t kColO = 0, kColQ = 256, kColS = 416, kColP = 480, kTmemCols = 512;  // Q uses 144 columns
+constexpr int kBoxBytes = kPage * 64 * 2;       // 64 tokens x 64 bf16 = 8 KiB, 128-byte swizzle
+constexpr int kRopeBoxBytes = kPage * 32 * 2;   // 64 tokens x 32 bf16 = 4 KiB, 64-byte swizzle
+constexpr int kStageBytes = 4 * kBoxBytes + kRopeBoxBytes;  // latent half + this CTA's RoPE half
+constexpr int kXSlot = kRowsPerCta * 64 * 2;    // a 128 x 64 tile of 16-bit values, 16 KiB
+constexpr int kQRopeBytes = kRowsPerCta * 32 * 2;  // this CTA's 32 RoPE columns of 128 query rows
+constexpr int kIdentBytes = 64 * 64 * 2;        // 64 x 64 fp16 identity
+// shared memory: stage ring | send slots (2) | receive slots (2) | RoPE
+// query tile | identity | DecodeShared
+constexpr int kXOff = kStages * kStageBytes;
+constexpr int kRecvOff = kXOff + 2 * kXSlot;
+constexpr int kQRopeOff = kXOff + 4 * kXSlot;
+constexpr int kIdentOff = kQRopeOff + kQRopeBytes;
+constexpr int kSmemShared = kIdentOff + kIdentBytes;
+static_assert(kStageBytes % 1024 == 0 && kQRopeOff % 1024 == 0 && kIdentOff % 1024 == 0,
+              "swizzled tiles need aligned bases");
+// warps 0-7: softmax warps (TMEM lane quadrant w & 3, key half w >> 2: 32
+// keys of every page, 128 columns of O, 64 columns of Q); warps 8-11:
+// exchange warps (one per quadrant, a whole score row per thread); warp 12:
+// TMA producer; warps 13, 14, 15: QK, ID and P.V issuers
+constexpr int kSWarps = 8, kXWarps = 4;
+constexpr int kSoftmaxThreads = 32 * kSWarps, kXThreads = 32 * kXWarps;
+constexpr int kTmaWarp = kSWarps + kXWarps, kMmaWarp = kTmaWarp + 1, kIdWarp = kMmaWarp + 1, kPvWarp = kIdWarp + 1;
+constexpr int kDecodeThreads = 32 * (kPvWarp + 1);
+static_assert(kPlanInKernelMaxB <= kDecodeThreads, "the in-kernel plan takes one thread per sequence");
+// named barriers: 1..4 = the two softmax warps of a quadrant, 5 = exchange warps
+constexpr uint32_t kBarPair0 = 1, kBarX = 5;
+// tensor memory columns: O (256) | Q latent half (128, bf16 pairs) | two
+// score buffers (64 each)
+constexpr uint32_t kColO = 0, kColQ = 256, kColS = 384, kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;       // log2 units: defer O rescaling up to 2^8
 
 __device__ __forceinline__ float ex2(float x) {
@@ -75,25 +95,14 @@ __device__ __forceinline__ float lg2(float x) {
   asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 __device__ __forceinline__ uint32_t pack_f16x2_sat(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
-__device__ __forceinline__ float2 unpack_f16x2(uint32_t w) {
-  float2 f;
-  asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
-      : "=f"(f.x), "=f"(f.y) : "r"(w));
-  return f;
-}
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
-}
-__device__ __forceinline__ void ld_shared_v4(uint32_t addr, uint32_t& a, uint32_t& b, uint32_t& c, uint32_t& d) {
-  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(a), "=r"(b), "=r"(c), "=r"(d) : "r"(addr) : "memory");
 }
 __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -117,15 +126,23 @@ __device__ __forceinline__ void set_status(WsHeader* ws, int code) {
   atomicCAS(&ws->status, 0, code);
 }
 
-// Shared state of one decode CTA (static shared memory).
+// Shared state of one decode CTA (at the end of dynamic shared memory).
+// Per score buffer / exchange slot b (page parity):
+//   s_full   QK(p) wrote the own partial scores into S_b
+//   x_read   the exchange warps read S_b (it may now receive the peer's part)
+//   xfull    the peer's fp16 partial landed in receive slot b
+//   s_ready  S_b holds the full scores (own + peer)
+//   s_free   the softmax warps read S_b (the next QK may overwrite it)
+//   p_full   P(p) is in receive slot b
+//   o_done   P.V of page p is done
+//   can_send the peer's P.V of page p is done: its receive slot b and our
+//            send slot b are free again (arrives from the peer's MMA)
 struct DecodeShared {
   uint64_t full[kStages], empty[kStages];
-  uint64_t q_full, s_full, s_free, p_full, o_done, drain;
-  uint64_t xfull[2], xfree[2], own_ready[2], src_free[2];
-  // [page parity][column half][row]: half-row maxima (half-row sums at the
-  // epilogue use the parity after the segment's last page)
-  float red[2][2][kRowsPerCta];
-  UnitRec rec;  // this CTA's work unit
+  uint64_t q_full, drain;
+  uint64_t s_full[2], x_read[2], xfull[2], s_ready[2], s_free[2], p_full[2], o_done[2], can_send[2];
+  float red[2][2][kRowsPerCta];  // [parity][key half][row]: partial row maxima (row sums at a segment's end)
+  UnitRec rec;                   // this CTA's work unit
   uint32_t tmem;
   int abort;
 };
@@ -143,24 +160,20 @@ __device__ __forceinline__ int aligned_units(int np, int units, int total) {
 // Walks the (sequence, page range) segments of one work unit from its
 // UnitRec, reading page counts from seq_lens (validated lengths).
 struct SegIter {
-  const int32_t* sl;
-  int B, lo, hi, b, o, start, end, bias;
-  __device__ void init(const UnitRec& r, const DecodeArgs& a) {
-    sl = a.seq_lens;
-    B = a.B;
-    lo = a.Lq > 1 ? a.Lq : 1;
-    hi = a.max_pages * kPage;
+  int b, o, start, end, bias;
+  __device__ void init(const UnitRec& r) {
     b = r.b; o = r.o; start = r.start; end = r.end; bias = r.bias;
   }
-  __device__ int total_pages() const { return end - start; }
   __device__ int slot(int sb) const { return sb + bias; }
-  __device__ int len(int sb) const { return clamp_len(sl[sb], lo, hi); }
+  __device__ static int len(const DecodeArgs& a, int sb) {
+    return clamp_len(a.seq_lens[sb], a.Lq > 1 ? a.Lq : 1, a.max_pages * kPage);
+  }
   // Next non-empty segment: sequence sb, pages [pa, pb) of that sequence.
-  __device__ bool next(int& sb, int& pa, int& pb) {
-    while (b < B && start < end) {
+  __device__ bool next(const DecodeArgs& a, int& sb, int& pa, int& pb) {
+    while (b < a.B && start < end) {
       const int o0 = o;
       if (o0 >= end) break;
-      const int o1 = o0 + (len(b) + kPage - 1) / kPage;
+      const int o1 = o0 + (len(a, b) + kPage - 1) / kPage;
       const int aa = max(start, o0), e = min(end, o1);
       const int cur = b++;
       o = o1;
@@ -173,6 +186,26 @@ struct SegIter {
     }
     return false;
   }
+};
+
+// One unit's pages in order: page i of sequence sb, in the segment [pa, pb).
+struct PageCursor {
+  SegIter it;
+  int sb, pa, pb, i;
+  bool valid;
+  __device__ void init(const UnitRec& r, const DecodeArgs& a) {
+    it.init(r);
+    valid = it.next(a, sb, pa, pb);
+    i = pa;
+  }
+  __device__ void advance(const DecodeArgs& a) {
+    if (++i >= pb) {
+      valid = it.next(a, sb, pa, pb);
+      i = pa;
+    }
+  }
+  __device__ bool seg_first() const { return i == pa; }
+  __device__ bool seg_last() const { return i == pb - 1; }
 };
 
 // ---- small block-wide helpers (all threads of the block call them)
@@ -313,10 +346,13 @@ __device__ void plan_in_block(const DecodeArgs& a, int unit, bool writer, int* s
 }
 
 __global__ void __launch_bounds__(kDecodeThreads, 1)
-    decode_kernel(const __grid_constant__ CUtensorMap tm_cache, const DecodeArgs a) {
+    decode_kernel(const __grid_constant__ CUtensorMap tm_cache, const __grid_constant__ CUtensorMap tm_rope,
+                  const __grid_constant__ CUtensorMap tm_qrope, const DecodeArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* stages = smem;
-  uint8_t* xbuf = smem + kStages * kStageBytes;  // [send 2][receive 2] x 16 KiB
+  uint8_t* xbuf = smem + kXOff;  // [send 2][receive 2] x 16 KiB
+  const uint32_t qrope = smem_u32(smem + kQRopeOff);
+  const uint32_t ident = smem_u32(smem + kIdentOff);
   DecodeShared& sh = *reinterpret_cast<DecodeShared*>(smem + kSmemShared);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -342,21 +378,33 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       mbar_init(bar(sh.empty[s]), 1);
     }
     mbar_init(bar(sh.q_full), kSoftmaxThreads);
-    mbar_init(bar(sh.s_full), 1);
-    mbar_init(bar(sh.s_free), kXThreads);
-    mbar_init(bar(sh.p_full), kSoftmaxThreads);
-    mbar_init(bar(sh.o_done), 1);
     mbar_init(bar(sh.drain), 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(sh.xfull[s]), 1);         // armed with the expected bytes, completed by the peer's copy
-      mbar_init(bar(sh.xfree[s]), kSWarps);   // the peer's softmax warps consumed what we sent
-      mbar_init(bar(sh.own_ready[s]), 1);     // our exchange warps wrote our partial into the send slot
-      mbar_init(bar(sh.src_free[s]), kSWarps);  // our softmax warps read our partial from the send slot
+      mbar_init(bar(sh.s_full[s]), 1);
+      mbar_init(bar(sh.x_read[s]), kXThreads);
+      mbar_init(bar(sh.xfull[s]), 1);  // armed with the expected bytes, completed by the peer's copy
+      mbar_init(bar(sh.s_ready[s]), 1);
+      mbar_init(bar(sh.s_free[s]), kSoftmaxThreads);
+      mbar_init(bar(sh.p_full[s]), kSoftmaxThreads);
+      mbar_init(bar(sh.o_done[s]), 1);
+      mbar_init(bar(sh.can_send[s]), 1);  // one arrival from the peer's MMA completion
     }
     fence_mbar_init();
     for (int s = 0; s < 2; ++s) mbar_arrive_expect_tx(bar(sh.xfull[s]), kXSlot);
     tma_prefetch_desc(&tm_cache);
+    tma_prefetch_desc(&tm_rope);
+    tma_prefetch_desc(&tm_qrope);
   }
+  // 64 x 64 fp16 identity, K-major with 128-byte swizzle (B operand that adds
+  // the peer's partial scores into S)
+  for (int i = threadIdx.x; i < 64 * 8; i += kDecodeThreads) {
+    const int n = i >> 3, c = i & 7;
+    const uint32_t one = (c == (n >> 3)) ? 0x3C00u << (16 * (n & 1)) : 0u;  // element n of row n
+    const int k = (n & 7) >> 1;                                             // its 32-bit word
+    st_shared_v4(ident + n * 128 + ((c ^ (n & 7)) << 4), k == 0 ? one : 0u, k == 1 ? one : 0u,
+                 k == 2 ? one : 0u, k == 3 ? one : 0u);
+  }
+  fence_proxy_async();
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(&sh.tmem), kTmemCols);
     tmem_relinquish();
@@ -382,19 +430,19 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     *abort = 1;
     set_status(ws, MLA_ERR_TIMEOUT);
   };
-  const uint32_t xsrc = smem_u32(xbuf), xrecv = xsrc + 2 * kXSlot;
+  const uint32_t xsrc = smem_u32(xbuf), xrecv = smem_u32(smem + kRecvOff);
 
   if (warp == kTmaWarp) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      const uint32_t bytes = 5 * kBoxBytes;
+      const uint32_t bytes = kStageBytes;
       const uint64_t policy = l2_policy_evict_first();
       SegIter it;
-      it.init(sh.rec, a);
+      it.init(sh.rec);
       int sb, pa, pb;
       uint32_t pc = 0;
       bool ok = true;
-      while (ok && it.next(sb, pa, pb)) {
+      while (ok && it.next(a, sb, pa, pb)) {
         const int32_t* bt = a.block_table + (size_t)sb * a.max_pages;
         for (int i = pa; i < pb; ++i, ++pc) {
           const int st = pc % kStages;
@@ -412,8 +460,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           for (int j = 0; j < 4; ++j)  // this CTA's latent half
             tma_load_2d_hint(dst + j * kBoxBytes, &tm_cache, bar(sh.full[st]), (int)(r * 256 + j * 64),
                              page * kPage, policy);
-          // RoPE box (each CTA uses 32 of its 64 columns)
-          tma_load_2d_hint(dst + 4 * kBoxBytes, &tm_cache, bar(sh.full[st]), kDc, page * kPage, policy);
+          // this CTA's 32 RoPE columns
+          tma_load_2d_hint(dst + 4 * kBoxBytes, &tm_rope, bar(sh.full[st]), kDc + 32 * (int)r, page * kPage,
+                           policy);
           // At start-up every CTA of the grid asks for its pages at once; let
           // the first page land before queueing the rest so compute starts
           // as early as possible instead of after the whole initial burst.
@@ -432,104 +481,138 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     }
     __syncwarp();  // reconverge before the CTA-wide barrier of the teardown
   } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ QK issuer
+    // Per page p in score buffer b = p & 1:
+    //   QK(p):  S_b  = Q . K^T over this CTA's columns           (this warp)
+    //   ID(p):  S_b += peer partial (receive slot b) x identity    (next warp)
+    //   PV(p):  O   += P (receive slot b, written by the softmax) . V
+    // Three issuing threads keep the tensor pipe fed: QKs wait only for
+    // their page and score buffer, IDs for the exchange, P.Vs for the
+    // softmax.  Every dependence between the streams goes through an mbarrier
+    // that a consumer of the earlier stream's results arrives on.
     if (lane == 0) {
-      constexpr int nk = 18;  // K steps of 16: 16 over the latent half + 2 over half the RoPE columns
       constexpr uint32_t idesc_qk = idesc_bf16(128, 64, false, false);
-      constexpr uint32_t idesc_pv = idesc_bf16(128, 256, false, true);
-      SegIter it;
-      it.init(sh.rec, a);
-      int sb, pa, pb;
+      const uint64_t qr0 = sdesc_sw64(qrope, 512);
+      PageCursor c;
+      c.init(sh.rec, a);
       uint32_t pc = 0, qc = 0;
       bool ok = true;
-      auto issue_pv = [&](uint32_t q, bool acc) -> bool {
-        if (!mbar_wait(bar(sh.p_full), q & 1, abort)) return false;
-        tc_fence_after();
-        const uint64_t vd0 = sdesc_sw128(smem_u32(stages + (q % kStages) * kStageBytes), kBoxBytes, 1024);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {  // 64 tokens = 4 K steps
-          const uint64_t vd = vd0 + (uint64_t)((kk * 2048) >> 4);
-          mma_ts(tmem + kColO, tmem + kColP + kk * 8, vd, idesc_pv, (acc || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(bar(sh.empty[q % kStages]));
-        mma_commit(bar(sh.o_done));
-        return true;
-      };
-      // Issue order QK(q), PV(q-2): the softmax warps work one page behind
-      // the exchange warps, so P(q-2) is ready once S(q) may be overwritten.
-      while (ok && it.next(sb, pa, pb)) {
-        if (!(ok = mbar_wait(bar(sh.q_full), qc & 1, abort))) break;
-        ++qc;
-        tc_fence_after();
-        const uint32_t p0 = pc;  // global index of page pa
-        for (int i = pa; i < pb; ++i, ++pc) {
-          const int st = pc % kStages;
-          if (!(ok = mbar_wait(bar(sh.full[st]), (pc / kStages) & 1, abort))) break;
-          if (pc > 0 && !(ok = mbar_wait(bar(sh.s_free), (pc - 1) & 1, abort))) break;
+      while (ok && c.valid) {
+        if (c.seg_first()) {  // the segment's query (loaded after every QK before it finished)
+          if (!(ok = mbar_wait(bar(sh.q_full), qc & 1, abort))) break;
+          ++qc;
           tc_fence_after();
-          const uint64_t kd0 = sdesc_sw128(smem_u32(stages + st * kStageBytes), 16, 1024);
-#pragma unroll
-          for (int kk = 0; kk < nk; ++kk) {
-            // latent K steps walk boxes 0..3; the last two take this CTA's
-            // 32 RoPE columns from box 4
-            const uint32_t off = kk < 16 ? (kk >> 2) * kBoxBytes + (kk & 3) * 32
-                                         : 4 * kBoxBytes + (r * 2 + (kk - 16)) * 32;
-            mma_ts(tmem + kColS, tmem + kColQ + kk * 8, kd0 + (uint64_t)(off >> 4), idesc_qk, kk > 0 ? 1u : 0u);
-          }
-          mma_commit(bar(sh.s_full));
-          if (i - 2 >= pa && !(ok = issue_pv(pc - 2, i - 2 > pa))) break;
         }
-        if (!ok) break;
-        for (int i = max(pa, pb - 2); i < pb; ++i)
-          if (!(ok = issue_pv(p0 + (uint32_t)(i - pa), i > pa))) break;
+        const uint32_t b = pc & 1;
+        const int st = pc % kStages;
+        if (!(ok = mbar_wait(bar(sh.full[st]), (pc / kStages) & 1, abort))) break;
+        if (pc >= 2 && !(ok = mbar_wait(bar(sh.s_free[b]), ((pc - 2) >> 1) & 1, abort))) break;
+        tc_fence_after();
+        const uint32_t sbase = smem_u32(stages + st * kStageBytes);
+        const uint64_t kd0 = sdesc_sw128(sbase, 16, 1024);
+        const uint64_t kr0 = sdesc_sw64(sbase + 4 * kBoxBytes, 512);
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) {  // latent: boxes 0..3, 4 K steps each (A = Q in tensor memory)
+          const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+          mma_ts(tmem + kColS + 64 * b, tmem + kColQ + kk * 8, kd0 + (uint64_t)(off >> 4), idesc_qk,
+                 kk > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk)  // RoPE: 32 columns = 2 K steps (A = RoPE query tile)
+          mma_ss(tmem + kColS + 64 * b, qr0 + (uint64_t)(kk * 2), kr0 + (uint64_t)(kk * 2), idesc_qk, 1u);
+        mma_commit(bar(sh.s_full[b]));
+        ++pc;
+        c.advance(a);
       }
       if (!ok) fail();
     }
     __syncwarp();  // reconverge before the CTA-wide barrier of the teardown
-  } else if (warp < kXWarps) {
+  } else if (warp == kIdWarp) {
+    // ------------------------------------------------------------ ID issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_id = idesc_f16(128, 64);
+      const uint64_t id0 = sdesc_sw128(ident, 16, 1024);
+      const int npages = sh.rec.end - sh.rec.start;
+      bool ok = true;
+      for (int p = 0; ok && p < npages; ++p) {
+        const uint32_t b = p & 1;
+        if (!(ok = mbar_wait(bar(sh.x_read[b]), (p >> 1) & 1, abort))) break;
+        if (!(ok = mbar_wait(bar(sh.xfull[b]), (p >> 1) & 1, abort))) break;
+        mbar_arrive_expect_tx(bar(sh.xfull[b]), kXSlot);  // armed for page p+2 (sent after our PV(p))
+        tc_fence_after();
+        const uint64_t rd0 = sdesc_sw128(xrecv + b * kXSlot, 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)  // 64 keys = 4 K steps of 32 bytes
+          mma_ss(tmem + kColS + 64 * b, rd0 + (uint64_t)(kk * 2), id0 + (uint64_t)(kk * 2), idesc_id, 1u);
+        mma_commit(bar(sh.s_ready[b]));
+      }
+      if (!ok) fail();
+    }
+    __syncwarp();  // reconverge before the CTA-wide barrier of the teardown
+  } else if (warp == kPvWarp) {
+    // ------------------------------------------------------------ P.V issuer
+    // P.V of page p frees receive slot p&1 at the peer for its next send.
+    if (lane == 0) {
+      constexpr uint32_t idesc_pv = idesc_bf16(128, 256, false, true);
+      const uint16_t peer_mask = (uint16_t)(1u << peer);
+      PageCursor c;
+      c.init(sh.rec, a);
+      bool ok = true;
+      for (uint32_t p = 0; ok && c.valid; ++p) {
+        const uint32_t b = p & 1;
+        const bool acc = !c.seg_first();  // a segment's first P.V starts O afresh
+        if (!(ok = mbar_wait(bar(sh.p_full[b]), (p >> 1) & 1, abort))) break;
+        tc_fence_after();
+        const uint64_t pd0 = sdesc_sw128(xrecv + b * kXSlot, 16, 1024);
+        const uint64_t vd0 = sdesc_sw128(smem_u32(stages + (p % kStages) * kStageBytes), kBoxBytes, 1024);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)  // 64 tokens = 4 K steps
+          mma_ss(tmem + kColO, pd0 + (uint64_t)(kk * 2), vd0 + (uint64_t)((kk * 2048) >> 4), idesc_pv,
+                 (acc || kk > 0) ? 1u : 0u);
+        mma_commit(bar(sh.empty[p % kStages]));
+        mma_commit(bar(sh.o_done[b]));
+        mma_commit_multicast(bar(sh.can_send[b]), peer_mask);
+        c.advance(a);
+      }
+      if (!ok) fail();
+    }
+    __syncwarp();  // reconverge before the CTA-wide barrier of the teardown
+  } else if (warp >= kSWarps && warp < kSWarps + kXWarps) {
     // ------------------------------------------------------------ exchange warps
-    // Page q: this CTA's partial scores (TMEM) -> fp16 in log2 units -> send
-    // slot q&1 -> one bulk copy into the peer's receive slot.  After a
-    // failure the loop keeps running without work, so every named barrier
-    // still sees all four warps.
-    const int row = warp * 32 + lane;
-    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    // Page p: own partial scores (S_b, fp32) -> fp16 -> send slot b -> one
+    // bulk copy into the peer's receive slot b.  After a failure the loop
+    // keeps running without work, so the named barrier still sees all four
+    // warps.
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
     const uint32_t peer_recv = mapa(xrecv, peer);
     const uint32_t peer_xfull0 = mapa(bar(sh.xfull[0]), peer), peer_xfull1 = mapa(bar(sh.xfull[1]), peer);
-    SegIter it;
-    it.init(sh.rec, a);
-    const int npages = it.end - it.start;
+    const int npages = sh.rec.end - sh.rec.start;
     bool ok = true;
-    for (int q = 0; q < npages; ++q) {
-      const uint32_t slot = q & 1, use = q >> 1;
-      if (ok) ok = mbar_wait(bar(sh.s_full), q & 1, abort);
+    for (int p = 0; p < npages; ++p) {
+      const uint32_t b = p & 1;
+      if (ok) ok = mbar_wait(bar(sh.s_full[b]), (p >> 1) & 1, abort);
       ok = __all_sync(0xffffffffu, ok);
+      uint32_t w[32];
       if (ok) {
         tc_fence_after();
-        uint32_t w[32];
-        {
+#pragma unroll
+        for (int hlf = 0; hlf < 2; ++hlf) {
           uint32_t v[32];
-          tmem_ld32(lane_base + kColS, v);
+          tmem_ld32(lane_base + kColS + 64 * b + 32 * hlf, v);
           tmem_wait_ld();
 #pragma unroll
           for (int j = 0; j < 16; ++j)
-            w[j] = pack_f16x2_sat(__uint_as_float(v[2 * j]) * a.scale_log2, __uint_as_float(v[2 * j + 1]) * a.scale_log2);
-          tmem_ld32(lane_base + kColS + 32, v);
-          tmem_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 16; ++j)
-            w[16 + j] = pack_f16x2_sat(__uint_as_float(v[2 * j]) * a.scale_log2,
-                                       __uint_as_float(v[2 * j + 1]) * a.scale_log2);
+            w[16 * hlf + j] = pack_f16x2_sat(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
         }
         tc_fence_before();
-        mbar_arrive(bar(sh.s_free));
-        if (use > 0) {  // the peer and our softmax warps are done with this slot's last use
-          ok = mbar_wait(bar(sh.xfree[slot]), (use - 1) & 1, abort);
-          if (ok) ok = mbar_wait(bar(sh.src_free[slot]), (use - 1) & 1, abort);
-        }
+        mbar_arrive(bar(sh.x_read[b]));
+        // the peer's P.V two pages back freed its receive slot and our send slot
+        if (p >= 2) ok = mbar_wait<true>(bar(sh.can_send[b]), ((p - 2) >> 1) & 1, abort);
         ok = __all_sync(0xffffffffu, ok);
         if (ok) {
-          const uint32_t dst = xsrc + slot * kXSlot + row * 128;
+          const uint32_t dst = xsrc + b * kXSlot + row * 128;
 #pragma unroll
           for (int c = 0; c < 8; ++c)
             st_shared_v4(dst + ((c ^ (row & 7)) << 4), w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
@@ -537,23 +620,19 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         }
       }
       ok = bar_red_and_n(ok, kBarX, kXThreads);
-      if (ok && threadIdx.x == 0) {
-        bulk_s2s(peer_recv + slot * kXSlot, xsrc + slot * kXSlot, kXSlot, slot ? peer_xfull1 : peer_xfull0);
-        mbar_arrive(bar(sh.own_ready[slot]));
-      }
+      if (ok && threadIdx.x == 32 * kSWarps)
+        bulk_s2s(peer_recv + b * kXSlot, xsrc + b * kXSlot, kXSlot, b ? peer_xfull1 : peer_xfull0);
       __syncwarp();
     }
     if (!ok) fail();
-  } else if (warp < kXWarps + kSWarps) {
+  } else {
     // ------------------------------------------------------------ softmax warps
-    // Two warps per TMEM lane quadrant share its 32 query rows and split each
-    // page's 64 key columns (half).  Page q: scores = own + peer fp16
-    // partials (the two CTAs add the same two values), mask, online softmax
-    // (row maximum shared with the partner warp), P -> tensor memory.  After a
-    // failure the loops keep running without work, so every named barrier
-    // still sees all its warps.
-    const int sw = warp - kXWarps;
-    const int quad = warp & 3, half = sw >> 2;
+    // Thread = one query row (TMEM lane) and 32 of each page's 64 keys (key
+    // half).  Page q: full scores (S_b) -> mask -> row maximum shared with
+    // the partner warp -> online softmax -> P (bf16) into receive slot b, in
+    // the layout of an MMA operand.  After a failure the loops keep running
+    // without work, so every named barrier still sees both warps.
+    const int quad = warp & 3, half = warp >> 2;
     const int row = quad * 32 + lane;              // TMEM lane = query row in this block
     const int grow = (int)rg * kRowsPerCta + row;  // row of the (l, h) list
     const bool valid = grow < a.rows;
@@ -561,209 +640,196 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     const int h = valid ? grow % a.H : 0;
     const int g = (h * a.G) / a.H;
     const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
-    const uint32_t peer_xfree0 = mapa(bar(sh.xfree[0]), peer), peer_xfree1 = mapa(bar(sh.xfree[1]), peer);
-    const uint32_t xrow = row * 128;
     const uint32_t pair_bar = kBarPair0 + quad;
+    const bool leader = (threadIdx.x == 0);
     const int d_q = a.d_g + kDr;
-    SegIter it;
-    it.init(sh.rec, a);
-    int sb, pa, pb;
-    uint32_t q = 0, od = 0;
     bool ok = true;
 
-    // this CTA's slice of query row (sequence b) -> tensor memory: 4 chunks
-    // of 64 latent columns (half 0: chunks 0-1 and the 32 RoPE columns this
-    // CTA multiplies; half 1: chunks 2-3)
+    // this thread's 128 latent query columns of sequence b -> tensor memory;
+    // the 128 rows' RoPE half by TMA (rows past the end read as zero; rows
+    // of another sequence in a partial block give scores nobody reads)
     auto qrow_of = [&](int b) { return a.q_cat + ((size_t)(b * a.Lq + l) * a.H + h) * d_q; };
     auto load_q = [&](int b) {
       if (!ok) return;
-      const __nv_bfloat16* qrow = qrow_of(b);
+      if (leader)
+        tma_load_2d(qrope, &tm_qrope, bar(sh.q_full), a.d_g + 32 * (int)r,
+                    b * a.Lq * a.H + (int)rg * kRowsPerCta);
       const uint4* lat = nullptr;
       if (valid) {
-        if (a.G == 1) lat = reinterpret_cast<const uint4*>(qrow + r * 256);
-        else if ((uint32_t)g == r) lat = reinterpret_cast<const uint4*>(qrow);
+        const __nv_bfloat16* qrow = qrow_of(b);
+        if (a.G == 1) lat = reinterpret_cast<const uint4*>(qrow + r * 256 + 128 * half);
+        else if ((uint32_t)g == r) lat = reinterpret_cast<const uint4*>(qrow + 128 * half);
       }
-      for (int c = 2 * half; c < 2 * half + 2; ++c) {
-        const uint4* src = lat ? lat + c * 8 : nullptr;
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {  // 32 columns (64 bf16) per round trip
         uint32_t w[32];
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          uint4 v = src ? src[k] : make_uint4(0, 0, 0, 0);
+          const uint4 v = lat ? lat[8 * c + k] : make_uint4(0, 0, 0, 0);
           w[4 * k + 0] = v.x; w[4 * k + 1] = v.y; w[4 * k + 2] = v.z; w[4 * k + 3] = v.w;
         }
-        tmem_st32(lane_base + kColQ + c * 32, w);
-      }
-      if (half == 0) {
-        const uint4* rope = valid ? reinterpret_cast<const uint4*>(qrow + a.d_g + 32 * r) : nullptr;
-        uint32_t w[16];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          uint4 v = rope ? rope[k] : make_uint4(0, 0, 0, 0);
-          w[4 * k + 0] = v.x; w[4 * k + 1] = v.y; w[4 * k + 2] = v.z; w[4 * k + 3] = v.w;
-        }
-        tmem_st16(lane_base + kColQ + 128, w);
+        tmem_st32(lane_base + kColQ + 64 * half + 32 * c, w);
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar(sh.q_full));
+      if (leader) mbar_arrive_expect_tx(bar(sh.q_full), kQRopeBytes);
+      else mbar_arrive(bar(sh.q_full));
     };
-    // pull the rows this thread will load for sequence b into L2 ahead of use
+    // pull what this thread will load for sequence b into L2 ahead of use
     auto prefetch_q = [&](int b) {
       if (!valid) return;
       const char* qrow = reinterpret_cast<const char*>(qrow_of(b));
-      const char* lat = a.G == 1 ? qrow + r * 512 : qrow;
       if (a.G == 1 || (uint32_t)g == r) {
-        asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(lat + half * 256));
-        asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(lat + half * 256 + 128));
+        const char* lat = qrow + (a.G == 1 ? r * 512 : 0) + half * 256;
+        asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(lat));
+        asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(lat + 128));
       }
       if (half == 0) asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(qrow + a.d_g * 2 + 64 * r));
     };
+    auto prefetch_after = [&](const SegIter& at) {  // the sequence after the segment `at` just produced
+      SegIter t = at;
+      int b2, pa2, pb2;
+      if (t.next(a, b2, pa2, pb2)) prefetch_q(b2);
+    };
 
-    bool have = it.next(sb, pa, pb);
-    if (have) load_q(sb);
-    while (have) {
-      const int seg = it.slot(sb);
-      const int n = it.len(sb);
-      const int limit = a.causal ? n - a.Lq + l + 1 : n;  // keys [0, limit) visible
-      float m_used = -INFINITY, l_part = 0.f;
-      SegIter peek = it;
-      int nsb, npa, npb;
-      const bool nhave = peek.next(nsb, npa, npb);
-      if (nhave) prefetch_q(nsb);
-
-      // ---- pages
-      for (int i = pa; i < pb; ++i, ++q) {
-        const uint32_t slot = q & 1, use = q >> 1;
-        const bool first = (i == pa);
-        float s[32];
-        float mt = -INFINITY;
-        if (ok) ok = mbar_wait(bar(sh.own_ready[slot]), use & 1, abort);
-        if (ok) ok = mbar_wait(bar(sh.xfull[slot]), use & 1, abort);
-        ok = __all_sync(0xffffffffu, ok);
-        if (ok) {
-          const uint32_t off = slot * kXSlot + xrow;
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t o[4], p[4];
-            const uint32_t swz = ((4 * half + c) ^ (row & 7)) << 4;
-            ld_shared_v4(xsrc + off + swz, o[0], o[1], o[2], o[3]);
-            ld_shared_v4(xrecv + off + swz, p[0], p[1], p[2], p[3]);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const float2 x = unpack_f16x2(o[k]), y = unpack_f16x2(p[k]);
-              s[8 * c + 2 * k] = x.x + y.x;
-              s[8 * c + 2 * k + 1] = x.y + y.y;
-            }
-          }
-          // both slots read by this warp (values consumed above): hand the
-          // receive slot back to the peer (re-armed first, once per CTA) and
-          // the send slot back to our exchange warps
-          __syncwarp();
-          if (lane == 0) {
-            if (sw == 0) mbar_arrive_expect_tx(bar(sh.xfull[slot]), kXSlot);
-            mbar_arrive_remote_relaxed(slot ? peer_xfree1 : peer_xfree0);
-            mbar_arrive(bar(sh.src_free[slot]));
-          }
-          __syncwarp();  // reconverge: the aligned barrier and TMEM ops below need the whole warp
-          const int key0 = i * kPage + 32 * half;
-          if (limit < i * kPage + kPage) {  // page holds keys this row may not see
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const float v = (key0 + j < limit) ? s[j] : -INFINITY;
-              s[j] = v;
-              mt = fmaxf(mt, v);
-            }
-          } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) mt = fmaxf(mt, s[j]);
-          }
-          sh.red[slot][half][row] = mt;
-        }
-        ok = bar_red_and_n(ok, pair_bar, 64);
-        if (ok) {
-          mt = fmaxf(mt, sh.red[slot][half ^ 1][row]);
-          const bool need = mt > m_used + kRescaleThreshold;
-          if (!first) {  // P.V of the previous page done: P and O are ours
-            ok = mbar_wait(bar(sh.o_done), od & 1, abort);
-            ok = __all_sync(0xffffffffu, ok);
-            ++od;
-            if (ok) {
-              tc_fence_after();
-              if (__any_sync(0xffffffffu, need)) {
-                const float f = need ? ex2(m_used - mt) : 1.0f;
-                for (int c = 0; c < 4; ++c) {
-                  uint32_t v[32];
-                  const uint32_t col = lane_base + kColO + 128 * half + c * 32;
-                  tmem_ld32(col, v);
-                  tmem_wait_ld();
-#pragma unroll
-                  for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * f);
-                  tmem_st32(col, v);
-                }
-                l_part *= f;
-              }
-            }
-          }
-          if (ok) {
-            if (need) m_used = mt;
-            const float base = (m_used == -INFINITY) ? 0.f : m_used;
-            uint32_t pk[16];
-            float psum = 0.f;
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const uint32_t w = pack_bf16x2(ex2(s[2 * j] - base), ex2(s[2 * j + 1] - base));
-              psum += bf16_lo(w) + bf16_hi(w);
-              pk[j] = w;
-            }
-            l_part += psum;
-            tmem_st16(lane_base + kColP + 16 * half, pk);
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(bar(sh.p_full));
-          }
-        }
+    PageCursor cur;
+    cur.init(sh.rec, a);
+    if (cur.valid) {
+      load_q(cur.sb);
+      prefetch_after(cur.it);
+    }
+    float m_used = -INFINITY, l_part = 0.f;
+    int seg = 0, limit = 0;
+    uint32_t q = 0;
+    while (cur.valid) {
+      const uint32_t b = q & 1;
+      PageCursor nx = cur;
+      nx.advance(a);
+      if (cur.seg_first()) {
+        m_used = -INFINITY;
+        l_part = 0.f;
+        seg = cur.it.slot(cur.sb);
+        const int n = SegIter::len(a, cur.sb);
+        limit = a.causal ? n - a.Lq + l + 1 : n;  // keys [0, limit) visible
       }
-
-      // ---- end of segment: once the last P.V is done, first hand the next
-      // segment's query to the MMA issuer, then write this segment's
-      // normalised latent partial and log-sum-exp while the next segment's
-      // first scores are computed (its first P.V needs our P, which comes
-      // after this epilogue, so O is read before it is overwritten).
-      if (ok) ok = mbar_wait(bar(sh.o_done), od & 1, abort);
+      float s[32];  // raw scores (unscaled) of this thread's 32 keys
+      float mt = -INFINITY;
+      if (ok) ok = mbar_wait(bar(sh.s_ready[b]), (q >> 1) & 1, abort);
       ok = __all_sync(0xffffffffu, ok);
-      ++od;
-      if (ok) tc_fence_after();
-      it = peek;
-      if (nhave) load_q(nsb);
-      sh.red[q & 1][half][row] = l_part;  // parity after the last page: free (see red)
+      if (ok) {
+        tc_fence_after();
+        uint32_t v[32];
+        tmem_ld32(lane_base + kColS + 64 * b + 32 * half, v);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(bar(sh.s_free[b]));
+#pragma unroll
+        for (int j = 0; j < 32; ++j) s[j] = __uint_as_float(v[j]);
+        const int key0 = cur.i * kPage + 32 * half;
+        if (limit < key0 + 32) {  // keys this row may not see
+#pragma unroll
+          for (int j = 0; j < 32; ++j) s[j] = (key0 + j < limit) ? s[j] : -INFINITY;
+        }
+        float mx[16];  // tree maximum
+#pragma unroll
+        for (int j = 0; j < 16; ++j) mx[j] = fmaxf(s[j], s[j + 16]);
+#pragma unroll
+        for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+          for (int j = 0; j < w; ++j) mx[j] = fmaxf(mx[j], mx[j + w]);
+        mt = mx[0];
+        sh.red[b][half][row] = mt;
+      }
       ok = bar_red_and_n(ok, pair_bar, 64);
       if (ok) {
-        const float l_sum = l_part + sh.red[q & 1][half ^ 1][row];
-        const float inv = l_sum > 0.f ? 1.0f / l_sum : 0.f;
-        // o_part is chunk-major, [slot][column/4][row][4]: consecutive rows
-        // of a warp write consecutive 16-byte chunks.
-        float4* dst = reinterpret_cast<float4*>(a.o_part) +
-                      ((size_t)seg * (kDc / 4) + r * 64 + half * 32) * a.rows + grow;
-        for (int c = 0; c < 4; ++c) {
-          uint32_t v[32];
-          tmem_ld32(lane_base + kColO + 128 * half + c * 32, v);
-          tmem_wait_ld();
-          if (valid) {
+        mt = fmaxf(mt, sh.red[b][half ^ 1][row]) * a.scale_log2;  // log2 units
+        const bool need = mt > m_used + kRescaleThreshold;
+        if (!cur.seg_first() && __any_sync(0xffffffffu, need)) {  // rescale O once P.V of page q-1 is done
+          ok = mbar_wait(bar(sh.o_done[(q - 1) & 1]), ((q - 1) >> 1) & 1, abort);
+          ok = __all_sync(0xffffffffu, ok);
+          if (ok) {
+            tc_fence_after();
+            const float f = need ? ex2(m_used - mt) : 1.0f;
+            for (int c = 0; c < 8; ++c) {  // 128 columns, 16 at a time
+              uint32_t v[16];
+              const uint32_t col = lane_base + kColO + 128 * half + 16 * c;
+              tmem_ld16(col, v);
+              tmem_wait_ld();
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-              dst[(size_t)(c * 8 + k) * a.rows] =
-                  make_float4(__uint_as_float(v[4 * k]) * inv, __uint_as_float(v[4 * k + 1]) * inv,
-                              __uint_as_float(v[4 * k + 2]) * inv, __uint_as_float(v[4 * k + 3]) * inv);
+              for (int j = 0; j < 16; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * f);
+              tmem_st16(col, v);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            l_part *= f;
           }
         }
-        if (valid && r == 0 && half == 0)
-          a.lse_part[(size_t)seg * a.rows + grow] =
-              l_sum > 0.f ? (m_used + lg2(l_sum)) * 0.69314718055994531f : -INFINITY;
-        tc_fence_before();
+        if (ok) {
+          if (need) m_used = mt;
+          const float base = (m_used == -INFINITY) ? 0.f : m_used;
+          uint32_t pk[16];
+          float psum = 0.f;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float p0 = ex2(fmaf(s[2 * j], a.scale_log2, -base));
+            const float p1 = ex2(fmaf(s[2 * j + 1], a.scale_log2, -base));
+            psum += p0 + p1;  // row sum of the unrounded weights
+            pk[j] = pack_bf16x2(p0, p1);
+          }
+          l_part += psum;
+          // P row into receive slot b (its peer partial was consumed by ID):
+          // K-major, 128-byte swizzle, this thread's four 16-byte chunks
+          const uint32_t dst = xrecv + b * kXSlot + row * 128;
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            st_shared_v4(dst + (((4 * half + c) ^ (row & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
+                         pk[4 * c + 3]);
+          fence_proxy_async();
+          mbar_arrive(bar(sh.p_full[b]));
+        }
       }
-      ok = bar_red_and_n(ok, kBarS, kSoftmaxThreads);
-      sb = nsb; pa = npa; pb = npb;
-      have = nhave;
+      // every QK of this segment is done (S(q) was complete): the next
+      // segment's query may replace it
+      if (nx.valid && nx.seg_first()) {
+        load_q(nx.sb);
+        prefetch_after(nx.it);
+      }
+
+      // ---- end of segment: normalised latent partial and log-sum-exp
+      if (cur.seg_last()) {
+        if (ok) ok = mbar_wait(bar(sh.o_done[b]), (q >> 1) & 1, abort);  // this page's P.V
+        ok = __all_sync(0xffffffffu, ok);
+        if (ok) tc_fence_after();
+        sh.red[b ^ 1][half][row] = l_part;  // parity of the next page: free until its maximum
+        ok = bar_red_and_n(ok, pair_bar, 64);
+        const float l_sum = l_part + sh.red[b ^ 1][half ^ 1][row];
+        ok = bar_red_and_n(ok, pair_bar, 64);  // both sums read before the next page's maxima land there
+        if (ok) {
+          const float inv = l_sum > 0.f ? 1.0f / l_sum : 0.f;
+          // o_part is chunk-major, [slot][column/4][row][4]: consecutive rows
+          // of a warp write consecutive 16-byte chunks.
+          float4* dst = reinterpret_cast<float4*>(a.o_part) +
+                        ((size_t)seg * (kDc / 4) + r * 64 + half * 32) * a.rows + grow;
+          for (int c = 0; c < 8; ++c) {
+            uint32_t v[16];
+            tmem_ld16(lane_base + kColO + 128 * half + 16 * c, v);
+            tmem_wait_ld();
+            if (valid) {
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                dst[(size_t)(c * 4 + k) * a.rows] =
+                    make_float4(__uint_as_float(v[4 * k]) * inv, __uint_as_float(v[4 * k + 1]) * inv,
+                                __uint_as_float(v[4 * k + 2]) * inv, __uint_as_float(v[4 * k + 3]) * inv);
+            }
+          }
+          if (valid && r == 0 && half == 0)
+            a.lse_part[(size_t)seg * a.rows + grow] =
+                l_sum > 0.f ? (m_used + lg2(l_sum)) * 0.69314718055994531f : -INFINITY;
+          tc_fence_before();
+        }
+      }
+      cur = nx;
+      ++q;
     }
     if (!ok) fail();
   }
@@ -1047,13 +1113,13 @@ int decode_max_units(int csize, int* units) {
   return MLA_OK;
 }
 
-cudaError_t launch_decode(const CUtensorMap& tm_cache, const DecodeArgs& a, int units, int csize,
-                          cudaStream_t st) {
+cudaError_t launch_decode(const CUtensorMap& tm_cache, const CUtensorMap& tm_rope, const CUtensorMap& tm_qrope,
+                          const DecodeArgs& a, int units, int csize, cudaStream_t st) {
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];
   cudaError_t e = decode_config(cfg, attr, units, csize, st);
   if (e != cudaSuccess) return e;
-  return cudaLaunchKernelEx(&cfg, decode_kernel, tm_cache, a);
+  return cudaLaunchKernelEx(&cfg, decode_kernel, tm_cache, tm_rope, tm_qrope, a);
 }
 
 cudaError_t launch_combine(const float* o_part, const float* lse_part, const WsHeader* ws, void* o_lat,

@@ -80,7 +80,7 @@ struct DecodeArgs {
   int units;
   const int32_t* seq_lens;
 };
-constexpr int kPlanInKernelMaxB = 448;  // one sequence per decode-kernel thread
+constexpr int kPlanInKernelMaxB = 448;  // one sequence per decode-kernel thread (its block size)
 
 // launchers (return cudaError_t of the launch)
 cudaError_t launch_absorb(const CUtensorMap& tmA, const CUtensorMap& tmB, const void* q_rope,
@@ -89,8 +89,11 @@ cudaError_t launch_project(const CUtensorMap& tmA, const CUtensorMap& tmB, void*
                            int d_g, cudaStream_t st);
 cudaError_t launch_plan(const int32_t* seq_lens, const int32_t* block_table, WsHeader* ws, int B,
                         int Lq, int max_pages, int num_pages, int units, cudaStream_t st);
-cudaError_t launch_decode(const CUtensorMap& tm_cache, const DecodeArgs& a, int units, int csize,
-                          cudaStream_t st);
+// tm_cache: latent boxes (64 x 64, 128-byte swizzle); tm_rope: the cache's
+// RoPE columns (32 x 64 boxes, 64-byte swizzle); tm_qrope: q_cat rows
+// (32 x 128 boxes, 64-byte swizzle)
+cudaError_t launch_decode(const CUtensorMap& tm_cache, const CUtensorMap& tm_rope, const CUtensorMap& tm_qrope,
+                          const DecodeArgs& a, int units, int csize, cudaStream_t st);
 cudaError_t launch_combine(const float* o_part, const float* lse_part, const WsHeader* ws,
                            void* o_lat, float* lse, int B, int Lq, int H, int G, cudaStream_t st);
 int decode_max_units(int csize, int* units);  // clusters of csize CTAs resident at once

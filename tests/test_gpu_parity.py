@@ -78,15 +78,16 @@ def test_decode_step_small(name):
     check_case(c, got, sample_pairs(c, heads))
 
 
-@pytest.mark.parametrize("B,Lq", [(448, 2), (600, 1)])
-def test_decode_large_batch(B, Lq):
-    """Batches at the largest size the decode kernel splits by itself (448)
-    and above it (600, split by the separate plan kernel): ragged lengths,
-    shuffled pages, every sequence checked on a few heads."""
+@pytest.mark.parametrize("B,Lq,launches", [(448, 2, 1), (449, 2, 2), (600, 1, 2)])
+def test_decode_large_batch(B, Lq, launches):
+    """Batches at the largest size the decode kernel splits by itself (448),
+    just above it and well above it (split by the separate plan kernel):
+    ragged lengths, shuffled pages, every sequence checked on a few heads."""
     rng = np.random.default_rng(B)
     lens = [int(x) for x in rng.integers(Lq, 200, size=B)]
     lens[0], lens[-1] = Lq, 64
     c = make_case(B=B, Lq=Lq, H=16, seq_lens=lens, table="perm", seed=47 + B)
+    assert mla.mla_decode_kernel_launches(c.dims) == launches
     got = run_gpu(c)
     assert got["status"] == 0
     pairs = [(b, h) for b in range(B) for h in (0, 7, 15)]
