@@ -59,27 +59,24 @@ constexpr int kRopeBoxBytes = kPage * 32 * 2;   // 64 tokens x 32 bf16 = 4 KiB, 
 constexpr int kStageBytes = 4 * kBoxBytes + kRopeBoxBytes;  // latent half + this CTA's RoPE half
 constexpr int kXSlot = kRowsPerCta * 64 * 2;    // a 128 x 64 tile of 16-bit values, 16 KiB
 constexpr int kQRopeBytes = kRowsPerCta * 32 * 2;  // this CTA's 32 RoPE columns of 128 query rows
-constexpr int kIdentBytes = 64 * 64 * 2;        // 64 x 64 fp16 identity
 // shared memory: stage ring | send slots (2) | receive slots (2) | RoPE
-// query tile | identity | DecodeShared
+// query tile | DecodeShared
 constexpr int kXOff = kStages * kStageBytes;
 constexpr int kRecvOff = kXOff + 2 * kXSlot;
 constexpr int kQRopeOff = kXOff + 4 * kXSlot;
-constexpr int kIdentOff = kQRopeOff + kQRopeBytes;
-constexpr int kSmemShared = kIdentOff + kIdentBytes;
-static_assert(kStageBytes % 1024 == 0 && kQRopeOff % 1024 == 0 && kIdentOff % 1024 == 0,
-              "swizzled tiles need aligned bases");
+constexpr int kSmemShared = kQRopeOff + kQRopeBytes;
+static_assert(kStageBytes % 1024 == 0 && kQRopeOff % 1024 == 0, "swizzled tiles need aligned bases");
 // warps 0-7: softmax warps (TMEM lane quadrant w & 3, key half w >> 2: 32
 // keys of every page, 128 columns of O, 64 columns of Q); warps 8-11:
 // exchange warps (one per quadrant, a whole score row per thread); warp 12:
-// TMA producer; warps 13, 14, 15: QK, ID and P.V issuers
+// TMA producer; warps 13, 14: QK and P.V issuers
 constexpr int kSWarps = 8, kXWarps = 4;
 constexpr int kSoftmaxThreads = 32 * kSWarps, kXThreads = 32 * kXWarps;
-constexpr int kTmaWarp = kSWarps + kXWarps, kMmaWarp = kTmaWarp + 1, kIdWarp = kMmaWarp + 1, kPvWarp = kIdWarp + 1;
+constexpr int kTmaWarp = kSWarps + kXWarps, kMmaWarp = kTmaWarp + 1, kPvWarp = kMmaWarp + 1;
 constexpr int kDecodeThreads = 32 * (kPvWarp + 1);
 static_assert(kPlanInKernelMaxB <= kDecodeThreads, "the in-kernel plan takes one thread per sequence");
-// named barriers: 1..4 = the two softmax warps of a quadrant, 5 = exchange warps
-constexpr uint32_t kBarPair0 = 1, kBarX = 5;
+// named barriers 1..4: the two softmax warps of a quadrant
+constexpr uint32_t kBarPair0 = 1;
 // tensor memory columns: O (256) | Q latent half (128, bf16 pairs) | two
 // score buffers (64 each)
 constexpr uint32_t kColO = 0, kColQ = 256, kColS = 384, kTmemCols = 512;
@@ -100,6 +97,15 @@ __device__ __forceinline__ uint32_t pack_f16x2_sat(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
+}
+__device__ __forceinline__ float2 unpack_f16x2(uint32_t w) {
+  float2 f;
+  asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
+      : "=f"(f.x), "=f"(f.y) : "r"(w));
+  return f;
+}
+__device__ __forceinline__ void ld_shared_v4(uint32_t addr, uint32_t& a, uint32_t& b, uint32_t& c, uint32_t& d) {
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(a), "=r"(b), "=r"(c), "=r"(d) : "r"(addr) : "memory");
 }
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
@@ -129,10 +135,9 @@ __device__ __forceinline__ void set_status(WsHeader* ws, int code) {
 // Shared state of one decode CTA (at the end of dynamic shared memory).
 // Per score buffer / exchange slot b (page parity):
 //   s_full   QK(p) wrote the own partial scores into S_b
-//   x_read   the exchange warps read S_b (it may now receive the peer's part)
 //   xfull    the peer's fp16 partial landed in receive slot b
-//   s_ready  S_b holds the full scores (own + peer)
-//   s_free   the softmax warps read S_b (the next QK may overwrite it)
+//   s_free   the exchange and softmax warps read S_b (the next QK may
+//            overwrite it)
 //   p_full   P(p) is in receive slot b
 //   o_done   P.V of page p is done
 //   can_send the peer's P.V of page p is done: its receive slot b and our
@@ -140,7 +145,7 @@ __device__ __forceinline__ void set_status(WsHeader* ws, int code) {
 struct DecodeShared {
   uint64_t full[kStages], empty[kStages];
   uint64_t q_full, drain;
-  uint64_t s_full[2], x_read[2], xfull[2], s_ready[2], s_free[2], p_full[2], o_done[2], can_send[2];
+  uint64_t s_full[2], xfull[2], s_free[2], p_full[2], o_done[2], can_send[2];
   float red[2][2][kRowsPerCta];  // [parity][key half][row]: partial row maxima (row sums at a segment's end)
   UnitRec rec;                   // this CTA's work unit
   uint32_t tmem;
@@ -352,7 +357,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   uint8_t* stages = smem;
   uint8_t* xbuf = smem + kXOff;  // [send 2][receive 2] x 16 KiB
   const uint32_t qrope = smem_u32(smem + kQRopeOff);
-  const uint32_t ident = smem_u32(smem + kIdentOff);
   DecodeShared& sh = *reinterpret_cast<DecodeShared*>(smem + kSmemShared);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -381,10 +385,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     mbar_init(bar(sh.drain), 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(sh.s_full[s]), 1);
-      mbar_init(bar(sh.x_read[s]), kXThreads);
       mbar_init(bar(sh.xfull[s]), 1);  // armed with the expected bytes, completed by the peer's copy
-      mbar_init(bar(sh.s_ready[s]), 1);
-      mbar_init(bar(sh.s_free[s]), kSoftmaxThreads);
+      mbar_init(bar(sh.s_free[s]), kSoftmaxThreads + kXThreads);
       mbar_init(bar(sh.p_full[s]), kSoftmaxThreads);
       mbar_init(bar(sh.o_done[s]), 1);
       mbar_init(bar(sh.can_send[s]), 1);  // one arrival from the peer's MMA completion
@@ -395,16 +397,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     tma_prefetch_desc(&tm_rope);
     tma_prefetch_desc(&tm_qrope);
   }
-  // 64 x 64 fp16 identity, K-major with 128-byte swizzle (B operand that adds
-  // the peer's partial scores into S)
-  for (int i = threadIdx.x; i < 64 * 8; i += kDecodeThreads) {
-    const int n = i >> 3, c = i & 7;
-    const uint32_t one = (c == (n >> 3)) ? 0x3C00u << (16 * (n & 1)) : 0u;  // element n of row n
-    const int k = (n & 7) >> 1;                                             // its 32-bit word
-    st_shared_v4(ident + n * 128 + ((c ^ (n & 7)) << 4), k == 0 ? one : 0u, k == 1 ? one : 0u,
-                 k == 2 ? one : 0u, k == 3 ? one : 0u);
-  }
-  fence_proxy_async();
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(&sh.tmem), kTmemCols);
     tmem_relinquish();
@@ -483,13 +475,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ QK issuer
     // Per page p in score buffer b = p & 1:
-    //   QK(p):  S_b  = Q . K^T over this CTA's columns           (this warp)
-    //   ID(p):  S_b += peer partial (receive slot b) x identity    (next warp)
-    //   PV(p):  O   += P (receive slot b, written by the softmax) . V
-    // Three issuing threads keep the tensor pipe fed: QKs wait only for
-    // their page and score buffer, IDs for the exchange, P.Vs for the
-    // softmax.  Every dependence between the streams goes through an mbarrier
-    // that a consumer of the earlier stream's results arrives on.
+    //   QK(p):  S_b = Q . K^T over this CTA's columns               (this warp)
+    //   PV(p):  O  += P (receive slot b, written by the softmax) . V (next warp)
+    // Two issuing threads keep the tensor pipe fed: QKs wait only for their
+    // page and score buffer, P.Vs for the softmax.  Every dependence between
+    // the streams goes through an mbarrier.
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16(128, 64, false, false);
       const uint64_t qr0 = sdesc_sw64(qrope, 512);
@@ -527,28 +517,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       if (!ok) fail();
     }
     __syncwarp();  // reconverge before the CTA-wide barrier of the teardown
-  } else if (warp == kIdWarp) {
-    // ------------------------------------------------------------ ID issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_id = idesc_f16(128, 64);
-      const uint64_t id0 = sdesc_sw128(ident, 16, 1024);
-      const int npages = sh.rec.end - sh.rec.start;
-      bool ok = true;
-      for (int p = 0; ok && p < npages; ++p) {
-        const uint32_t b = p & 1;
-        if (!(ok = mbar_wait(bar(sh.x_read[b]), (p >> 1) & 1, abort))) break;
-        if (!(ok = mbar_wait(bar(sh.xfull[b]), (p >> 1) & 1, abort))) break;
-        mbar_arrive_expect_tx(bar(sh.xfull[b]), kXSlot);  // armed for page p+2 (sent after our PV(p))
-        tc_fence_after();
-        const uint64_t rd0 = sdesc_sw128(xrecv + b * kXSlot, 16, 1024);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)  // 64 keys = 4 K steps of 32 bytes
-          mma_ss(tmem + kColS + 64 * b, rd0 + (uint64_t)(kk * 2), id0 + (uint64_t)(kk * 2), idesc_id, 1u);
-        mma_commit(bar(sh.s_ready[b]));
-      }
-      if (!ok) fail();
-    }
-    __syncwarp();  // reconverge before the CTA-wide barrier of the teardown
   } else if (warp == kPvWarp) {
     // ------------------------------------------------------------ P.V issuer
     // P.V of page p frees receive slot p&1 at the peer for its next send.
@@ -579,10 +547,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     __syncwarp();  // reconverge before the CTA-wide barrier of the teardown
   } else if (warp >= kSWarps && warp < kSWarps + kXWarps) {
     // ------------------------------------------------------------ exchange warps
-    // Page p: own partial scores (S_b, fp32) -> fp16 -> send slot b -> one
-    // bulk copy into the peer's receive slot b.  After a failure the loop
-    // keeps running without work, so the named barrier still sees all four
-    // warps.
+    // Page p: own partial scores (S_b, fp32) -> fp16 -> send slot b; each
+    // warp copies its 32 rows (4 KiB) into the peer's receive slot b as soon
+    // as they are written (the peer's barrier counts the bytes of all four).
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
@@ -607,7 +574,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             w[16 * hlf + j] = pack_f16x2_sat(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
         }
         tc_fence_before();
-        mbar_arrive(bar(sh.x_read[b]));
+        mbar_arrive(bar(sh.s_free[b]));
         // the peer's P.V two pages back freed its receive slot and our send slot
         if (p >= 2) ok = mbar_wait<true>(bar(sh.can_send[b]), ((p - 2) >> 1) & 1, abort);
         ok = __all_sync(0xffffffffu, ok);
@@ -619,9 +586,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           fence_proxy_async();
         }
       }
-      ok = bar_red_and_n(ok, kBarX, kXThreads);
-      if (ok && threadIdx.x == 32 * kSWarps)
-        bulk_s2s(peer_recv + b * kXSlot, xsrc + b * kXSlot, kXSlot, b ? peer_xfull1 : peer_xfull0);
+      __syncwarp();
+      if (ok && lane == 0) {
+        const uint32_t off = b * kXSlot + quad * 32 * 128;
+        bulk_s2s(peer_recv + off, xsrc + off, 32 * 128, b ? peer_xfull1 : peer_xfull0);
+      }
       __syncwarp();
     }
     if (!ok) fail();
@@ -714,17 +683,29 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       }
       float s[32];  // raw scores (unscaled) of this thread's 32 keys
       float mt = -INFINITY;
-      if (ok) ok = mbar_wait(bar(sh.s_ready[b]), (q >> 1) & 1, abort);
+      if (ok) ok = mbar_wait(bar(sh.s_full[b]), (q >> 1) & 1, abort);
+      if (ok) ok = mbar_wait(bar(sh.xfull[b]), (q >> 1) & 1, abort);
       ok = __all_sync(0xffffffffu, ok);
       if (ok) {
         tc_fence_after();
         uint32_t v[32];
-        tmem_ld32(lane_base + kColS + 64 * b + 32 * half, v);
+        tmem_ld32(lane_base + kColS + 64 * b + 32 * half, v);  // own partial, fp32
+        const uint32_t src = xrecv + b * kXSlot + row * 128;     // peer partial, fp16
+        uint32_t pw[16];
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          ld_shared_v4(src + (((4 * half + c) ^ (row & 7)) << 4), pw[4 * c], pw[4 * c + 1], pw[4 * c + 2],
+                       pw[4 * c + 3]);
         tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(bar(sh.s_free[b]));
+        if (leader) mbar_arrive_expect_tx(bar(sh.xfull[b]), kXSlot);  // armed for page q+2 (sent after our PV(q))
 #pragma unroll
-        for (int j = 0; j < 32; ++j) s[j] = __uint_as_float(v[j]);
+        for (int k = 0; k < 16; ++k) {
+          const float2 y = unpack_f16x2(pw[k]);
+          s[2 * k] = __uint_as_float(v[2 * k]) + y.x;
+          s[2 * k + 1] = __uint_as_float(v[2 * k + 1]) + y.y;
+        }
         const int key0 = cur.i * kPage + 32 * half;
         if (limit < key0 + 32) {  // keys this row may not see
 #pragma unroll
@@ -777,8 +758,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             pk[j] = pack_bf16x2(p0, p1);
           }
           l_part += psum;
-          // P row into receive slot b (its peer partial was consumed by ID):
-          // K-major, 128-byte swizzle, this thread's four 16-byte chunks
+          // P row into receive slot b, over the peer partial this thread
+          // read there: K-major, 128-byte swizzle, four 16-byte chunks
           const uint32_t dst = xrecv + b * kXSlot + row * 128;
 #pragma unroll
           for (int c = 0; c < 4; ++c)
