@@ -122,7 +122,7 @@ int mla_project_uv(const mla_dims* d, const void* o_lat, const void* W_UV, void*
   {
     cuuint64_t dims[3] = {(cuuint64_t)dg, (cuuint64_t)kDhc, (cuuint64_t)H};
     cuuint64_t strides[2] = {(cuuint64_t)dg * 2, (cuuint64_t)kDhc * dg * 2};
-    cuuint32_t box[3] = {64, kDhc, 1};
+    cuuint32_t box[3] = {64, 64, 1};  // 64 output rows of W_UV per CTA
     if ((rc = make_map(&tB, W_UV, 3, dims, strides, box)) != MLA_OK) return rc;
   }
   return cuda_status(launch_project(tA, tB, out, M, H, dg, static_cast<cudaStream_t>(stream)));

@@ -363,6 +363,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   // 128-byte-swizzled tiles need a 1024-byte aligned base; the whole cluster
   // sees the same layout, so every CTA takes this exit together.
   if (smem_u32(smem) & 1023u) {
+    griddep_wait();
     if (threadIdx.x == 0) set_status(a.ws, MLA_ERR_UNSUPPORTED);
     return;
   }
@@ -407,6 +408,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   tc_fence_after();
   const uint32_t tmem = sh.tmem;
   volatile int* abort = &sh.abort;
+  // set-up above overlaps the kernel before; global memory only from here on
+  griddep_wait();
+  griddep_launch_dependents();
 
   // the work split: computed here (the exchange slots are still unused and
   // serve as scratch), or read from the plan kernel's records
@@ -976,29 +980,45 @@ __global__ void __launch_bounds__(256)
   const int rows = Lq * H;
   const int b = blockIdx.x, r0 = blockIdx.y * kCombineRows, cz = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  griddep_wait();
+  griddep_launch_dependents();
   const WsView v = ws_view(ws, B);
   const int nseg = v.nslot[b];
   const size_t seg0 = (size_t)v.slot0[b];
   const bool table = nseg <= kCombineMaxSeg;
 
-  // log-sum-exp per row (warp w: rows w, w+8, w+16, w+24), then weights
-  for (int rr = warp; rr < kCombineRows; rr += 8) {
-    const int row = r0 + rr;
+  // log-sum-exp per row (warp w: rows w, w+8, w+16, w+24), then weights.
+  // Lane j keeps partial j's value (and j+32's) of the four rows in
+  // registers: one load round for all of them.
+  constexpr int kRowsPerWarp = kCombineRows / 8;
+  float x0[kRowsPerWarp], x1[kRowsPerWarp];
+#pragma unroll
+  for (int k = 0; k < kRowsPerWarp; ++k) {
+    const int row = r0 + warp + 8 * k;
+    x0[k] = (row < rows && lane < nseg) ? lse_part[(seg0 + lane) * rows + row] : -INFINITY;
+    x1[k] = (row < rows && lane + 32 < nseg) ? lse_part[(seg0 + lane + 32) * rows + row] : -INFINITY;
+  }
+#pragma unroll
+  for (int k = 0; k < kRowsPerWarp; ++k) {
+    const int rr = warp + 8 * k, row = r0 + rr;
     float L = -INFINITY;
     if (row < rows) {
-      float mx = -INFINITY;
-      for (int j = lane; j < nseg; j += 32) mx = fmaxf(mx, lse_part[(seg0 + j) * rows + row]);
+      float mx = fmaxf(x0[k], x1[k]);
+      for (int j = lane + 64; j < nseg; j += 32) mx = fmaxf(mx, lse_part[(seg0 + j) * rows + row]);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
       float sum = 0.f;
-      if (mx != -INFINITY)
-        for (int j = lane; j < nseg; j += 32) sum += expf(lse_part[(seg0 + j) * rows + row] - mx);
+      if (mx != -INFINITY) {
+        sum = expf(x0[k] - mx) + expf(x1[k] - mx);
+        for (int j = lane + 64; j < nseg; j += 32) sum += expf(lse_part[(seg0 + j) * rows + row] - mx);
+      }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
       L = (mx == -INFINITY) ? -INFINITY : mx + logf(sum);
-      if (table)
-        for (int j = lane; j < nseg; j += 32)
-          wts[j][rr] = (L == -INFINITY) ? 0.f : expf(lse_part[(seg0 + j) * rows + row] - L);
+      if (table) {
+        if (lane < nseg) wts[lane][rr] = (L == -INFINITY) ? 0.f : expf(x0[k] - L);
+        if (lane + 32 < nseg) wts[lane + 32][rr] = (L == -INFINITY) ? 0.f : expf(x1[k] - L);
+      }
     }
     if (lane == 0) {
       lrow[rr] = L;
@@ -1007,28 +1027,49 @@ __global__ void __launch_bounds__(256)
   }
   __syncthreads();
 
-  // weighted sum: thread = (row lane, chunk group warp)
+  // weighted sum: thread = (row lane, chunk group warp); every load of a
+  // partial for all of the thread's chunks is issued before any is used
   const int row = r0 + lane;
   const bool valid = row < rows;
   const int h = valid ? row % H : 0, g = (h * G) / H;
   const float L = lrow[lane];
-  constexpr int kChunks = kCols / 4;
-  for (int c = warp; c < kChunks; c += 8) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (valid && L != -INFINITY) {
-      const int c4 = g * (DG / 4) + cz * kChunks + c;  // 4-column chunk of the full latent
-      const float4* src = reinterpret_cast<const float4*>(o_part) + (size_t)c4 * rows + row;
-      for (int j = 0; j < nseg; ++j) {
-        const float w = table ? wts[j][lane] : expf(lse_part[(seg0 + j) * rows + row] - L);
-        if (w == 0.f) continue;
-        const float4 v = src[(seg0 + j) * (size_t)(kDc / 4) * rows];
-        acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
+  constexpr int kChunks = kCols / 4, kPer = kChunks / 8;  // chunks of this thread: warp + 8k
+  float4 acc[kPer];
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (valid && L != -INFINITY) {
+    const int c0 = g * (DG / 4) + cz * kChunks + warp;  // first 4-column chunk of the full latent
+    const float4* src = reinterpret_cast<const float4*>(o_part) + (size_t)c0 * rows + row;
+    const size_t slot_stride = (size_t)(kDc / 4) * rows, chunk_stride = (size_t)8 * rows;
+    constexpr int kBatch = 4;  // partials whose loads are all issued before any is used
+#pragma unroll 1
+    for (int j0 = 0; j0 < nseg; j0 += kBatch) {
+      float4 v[kBatch][kPer];
+#pragma unroll
+      for (int jj = 0; jj < kBatch; ++jj) {
+        const float4* sj = src + (seg0 + j0 + jj) * slot_stride;
+#pragma unroll
+        for (int k = 0; k < kPer; ++k)
+          v[jj][k] = (j0 + jj < nseg) ? __ldcs(sj + k * chunk_stride) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int jj = 0; jj < kBatch; ++jj) {
+        const int j = j0 + jj;
+        const float w = j >= nseg ? 0.f : table ? wts[j][lane] : expf(lse_part[(seg0 + j) * rows + row] - L);
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+          acc[k].x += w * v[jj][k].x; acc[k].y += w * v[jj][k].y;
+          acc[k].z += w * v[jj][k].z; acc[k].w += w * v[jj][k].w;
+        }
       }
     }
+  }
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
     uint2 pk;
-    pk.x = pack_bf16x2(acc.x, acc.y);
-    pk.y = pack_bf16x2(acc.z, acc.w);
-    *reinterpret_cast<uint2*>(&tile[lane][c * 4]) = pk;
+    pk.x = pack_bf16x2(acc[k].x, acc[k].y);
+    pk.y = pack_bf16x2(acc[k].z, acc[k].w);
+    *reinterpret_cast<uint2*>(&tile[lane][(warp + 8 * k) * 4]) = pk;
   }
   __syncthreads();
   constexpr int kPieces = kCols * 2 / 16;  // 16-byte pieces per row
@@ -1068,8 +1109,10 @@ static cudaError_t decode_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* a
   attr[0].val.clusterDim.x = csize;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaSuccess;
 }
 
@@ -1083,7 +1126,7 @@ int decode_max_units(int csize, int* units) {
     return MLA_OK;
   }
   cudaLaunchConfig_t cfg;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   if (decode_config(cfg, attr, 1, csize, nullptr) != cudaSuccess) return MLA_ERR_CUDA;
   int n = 0;
   if (cudaOccupancyMaxActiveClusters(&n, decode_kernel, &cfg) != cudaSuccess || n < 1) return MLA_ERR_CUDA;
@@ -1097,7 +1140,7 @@ int decode_max_units(int csize, int* units) {
 cudaError_t launch_decode(const CUtensorMap& tm_cache, const CUtensorMap& tm_rope, const CUtensorMap& tm_qrope,
                           const DecodeArgs& a, int units, int csize, cudaStream_t st) {
   cudaLaunchConfig_t cfg;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cudaError_t e = decode_config(cfg, attr, units, csize, st);
   if (e != cudaSuccess) return e;
   return cudaLaunchKernelEx(&cfg, decode_kernel, tm_cache, tm_rope, tm_qrope, a);
@@ -1107,9 +1150,8 @@ cudaError_t launch_combine(const float* o_part, const float* lse_part, const WsH
                            float* lse, int B, int Lq, int H, int G, cudaStream_t st) {
   dim3 grid(B, (Lq * H + kCombineRows - 1) / kCombineRows, kCombineSplit), block(256);
   auto* ol = static_cast<__nv_bfloat16*>(o_lat);
-  if (G == 1) combine_kernel<512><<<grid, block, 0, st>>>(o_part, lse_part, ws, ol, lse, B, Lq, H, G);
-  else combine_kernel<256><<<grid, block, 0, st>>>(o_part, lse_part, ws, ol, lse, B, Lq, H, G);
-  return cudaGetLastError();
+  if (G == 1) return launch_chained(combine_kernel<512>, grid, block, 0, st, o_part, lse_part, ws, ol, lse, B, Lq, H, G);
+  return launch_chained(combine_kernel<256>, grid, block, 0, st, o_part, lse_part, ws, ol, lse, B, Lq, H, G);
 }
 
 }  // namespace mla

@@ -7,8 +7,10 @@
 //            (matrix absorption, MLA operator write-up §4, einsum qhd,hdc->qhc)
 //   project: out[m,h,:]       = W_UV[h] . o_lat[m,h,:]        (M x d_g x 128 per head)
 //
-// m runs over the B*Lq query rows; one CTA per (head, 128-row block).  Rows
-// past M are zero-filled by the tensor copies and never stored.
+// m runs over the B*Lq query rows.  absorb: one CTA per (head, 128-row
+// block, 256 output columns); project: one CTA per (head, 128-row block,
+// 64 output columns).
+// Rows past M are zero-filled by the tensor copies and never stored.
 #include "mla_internal.h"
 #include "ptx.cuh"
 
@@ -37,10 +39,13 @@ __device__ __forceinline__ void store_row32_bf16(__nv_bfloat16* dst, const uint3
 constexpr int kBox = 16384;  // one 128 x 64 bf16 tile, 128-byte swizzled
 
 // ---------------------------------------------------------------- absorb
-// A = q_nope rows (K-major, 2 tiles of 64 k), B = W_UK[h] (d rows x d_g
-// columns: N-contiguous, i.e. MN-major, d_g/64 tiles of 128 d x 64 c).
+// A = q_nope rows (K-major, 2 tiles of 64 k), B = 256 columns of W_UK[h]
+// (d rows x c columns, N-contiguous, i.e. MN-major: 4 tiles of 128 d x 64
+// c).  Two CTAs per head and per SM, all resident at once: the weight
+// loads of one overlap the MMAs and stores of the other.
+constexpr int kAbsorbCols = 256;
 template <int DG>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(128)
     absorb_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const __nv_bfloat16* __restrict__ q_rope, __nv_bfloat16* __restrict__ q_cat,
                   int M, int H) {
@@ -51,7 +56,7 @@ __global__ void __launch_bounds__(128, 1)
   __shared__ __align__(8) uint64_t bars[2];
   __shared__ uint32_t tmem_holder;
   __shared__ int abort_flag;
-  const int h = blockIdx.x, m0 = blockIdx.y * kRowsPerCta;
+  const int h = blockIdx.x, m0 = blockIdx.y * kRowsPerCta, n0 = blockIdx.z * kAbsorbCols;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t full = smem_u32(&bars[0]), done = smem_u32(&bars[1]);
   if (threadIdx.x == 0) {
@@ -63,29 +68,30 @@ __global__ void __launch_bounds__(128, 1)
     tma_prefetch_desc(&tmB);
   }
   if (warp == 0) {
-    tmem_alloc(smem_u32(&tmem_holder), DG);
+    tmem_alloc(smem_u32(&tmem_holder), kAbsorbCols);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_holder;
+  // set-up above overlaps the kernel before; global memory only from here on
+  griddep_wait();
+  griddep_launch_dependents();
 
   if (threadIdx.x == 0) {
-    mbar_arrive_expect_tx(full, 2 * kBox + (DG / 64) * kBox);
+    mbar_arrive_expect_tx(full, 2 * kBox + (kAbsorbCols / 64) * kBox);
+    for (int nb = 0; nb < kAbsorbCols / 64; ++nb)
+      tma_load_3d(smem_u32(sB + nb * kBox), &tmB, full, n0 + nb * 64, 0, h);
     for (int kb = 0; kb < 2; ++kb) tma_load_3d(smem_u32(sA + kb * kBox), &tmA, full, kb * 64, h, m0);
-    for (int nb = 0; nb < DG / 64; ++nb) tma_load_3d(smem_u32(sB + nb * kBox), &tmB, full, nb * 64, 0, h);
     if (mbar_wait(full, 0, &abort_flag)) {
       tc_fence_after();
-      constexpr uint32_t idesc = idesc_bf16(128, 256, false, true);
+      constexpr uint32_t idesc = idesc_bf16(128, kAbsorbCols, false, true);
 #pragma unroll
       for (int j = 0; j < 8; ++j) {  // K = 128 in steps of 16
         const uint64_t ad = sdesc_sw128(smem_u32(sA) + (j >> 2) * kBox + (j & 3) * 32, 16, 1024);
-#pragma unroll
-        for (int nh = 0; nh < DG / 256; ++nh) {
-          const uint64_t bd = sdesc_sw128(smem_u32(sB) + nh * 4 * kBox + j * 2048, kBox, 1024);
-          mma_ss(tmem + nh * 256, ad, bd, idesc, j > 0 ? 1u : 0u);
-        }
+        const uint64_t bd = sdesc_sw128(smem_u32(sB) + j * 2048, kBox, 1024);  // 64-column atoms kBox apart
+        mma_ss(tmem, ad, bd, idesc, j > 0 ? 1u : 0u);
       }
       mma_commit(done);
     } else {
@@ -99,13 +105,13 @@ __global__ void __launch_bounds__(128, 1)
     const int row = warp * 32 + lane, m = m0 + row;
     __nv_bfloat16* dst = q_cat + ((size_t)m * H + h) * (DG + kDr);
 #pragma unroll 1
-    for (int c = 0; c < DG / 32; ++c) {
+    for (int c = 0; c < kAbsorbCols / 32; ++c) {
       uint32_t r[32];
       tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + c * 32, r);
       tmem_wait_ld();
-      if (m < M) store_row32_bf16(dst + c * 32, r);
+      if (m < M) store_row32_bf16(dst + n0 + c * 32, r);
     }
-    if (m < M) {
+    if (m < M && blockIdx.z == 0) {
       const uint4* src = reinterpret_cast<const uint4*>(q_rope + ((size_t)m * H + h) * kDr);
       uint4* d = reinterpret_cast<uint4*>(dst + DG);
 #pragma unroll
@@ -116,31 +122,33 @@ __global__ void __launch_bounds__(128, 1)
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, DG);
+    tmem_dealloc(tmem, kAbsorbCols);
   }
 }
 
 // ---------------------------------------------------------------- project
-// A = o_lat rows (K-major over d_g), B = W_UV[h] (128 d rows x d_g columns,
-// K-contiguous: K-major).  K is streamed in 64-wide chunks through a 4-slot
-// ring; each slot holds one A tile and one B tile.
+// A = o_lat rows (K-major over d_g), B = 64 rows of W_UV[h] (d rows x d_g
+// columns, K-contiguous: K-major).  K is streamed in 64-wide chunks through
+// a 4-slot ring; each slot holds one A tile (16 KiB) and one B tile (8 KiB).
+// Two CTAs per head (output columns 0-63, 64-127), two CTAs per SM.
+constexpr int kProjectCols = 64;
 template <int DG>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(128)
     project_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    __nv_bfloat16* __restrict__ out, int M, int H) {
-  constexpr int kSlots = 4, kChunks = DG / 64;
+  constexpr int kSlots = 4, kChunks = DG / 64, kBoxB = kProjectCols * 64 * 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   __shared__ __align__(8) uint64_t bars[2 * kSlots + 1];
   __shared__ uint32_t tmem_holder;
   __shared__ int abort_flag;
-  const int h = blockIdx.x, m0 = blockIdx.y * kRowsPerCta;
+  const int h = blockIdx.x, m0 = blockIdx.y * kRowsPerCta, n0 = blockIdx.z * kProjectCols;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t done = smem_u32(&bars[2 * kSlots]);
   auto full = [&](int s) { return smem_u32(&bars[s]); };
   auto empty = [&](int s) { return smem_u32(&bars[kSlots + s]); };
-  auto slotA = [&](int s) { return smem_u32(smem + s * 2 * kBox); };
-  auto slotB = [&](int s) { return smem_u32(smem + s * 2 * kBox + kBox); };
+  auto slotA = [&](int s) { return smem_u32(smem + s * (kBox + kBoxB)); };
+  auto slotB = [&](int s) { return smem_u32(smem + s * (kBox + kBoxB) + kBox); };
   if (threadIdx.x == 0) {
     abort_flag = 0;
     for (int s = 0; s < kSlots; ++s) {
@@ -153,23 +161,26 @@ __global__ void __launch_bounds__(128, 1)
     tma_prefetch_desc(&tmB);
   }
   if (warp == 0) {
-    tmem_alloc(smem_u32(&tmem_holder), 128);
+    tmem_alloc(smem_u32(&tmem_holder), kProjectCols);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_holder;
+  // set-up above overlaps the kernel before; global memory only from here on
+  griddep_wait();
+  griddep_launch_dependents();
 
   if (threadIdx.x == 0) {
     auto load = [&](int c) {
       const int s = c % kSlots;
-      mbar_arrive_expect_tx(full(s), 2 * kBox);
+      mbar_arrive_expect_tx(full(s), kBox + kBoxB);
+      tma_load_3d(slotB(s), &tmB, full(s), c * 64, n0, h);
       tma_load_3d(slotA(s), &tmA, full(s), c * 64, h, m0);
-      tma_load_3d(slotB(s), &tmB, full(s), c * 64, 0, h);
     };
     for (int c = 0; c < kChunks && c < kSlots; ++c) load(c);
-    constexpr uint32_t idesc = idesc_bf16(128, 128, false, false);
+    constexpr uint32_t idesc = idesc_bf16(128, kProjectCols, false, false);
     bool ok = true;
     for (int c = 0; c < kChunks && ok; ++c) {
       const int s = c % kSlots;
@@ -195,9 +206,9 @@ __global__ void __launch_bounds__(128, 1)
   tc_fence_after();
   if (ok) {
     const int row = warp * 32 + lane, m = m0 + row;
-    __nv_bfloat16* dst = out + ((size_t)m * H + h) * kDhc;
+    __nv_bfloat16* dst = out + ((size_t)m * H + h) * kDhc + n0;
 #pragma unroll 1
-    for (int c = 0; c < kDhc / 32; ++c) {
+    for (int c = 0; c < kProjectCols / 32; ++c) {
       uint32_t r[32];
       tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + c * 32, r);
       tmem_wait_ld();
@@ -208,7 +219,7 @@ __global__ void __launch_bounds__(128, 1)
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, 128);
+    tmem_dealloc(tmem, kProjectCols);
   }
 }
 
@@ -221,36 +232,35 @@ cudaError_t set_smem(K kernel, int bytes) {
 
 cudaError_t launch_absorb(const CUtensorMap& tmA, const CUtensorMap& tmB, const void* q_rope,
                           void* q_cat, int M, int H, int d_g, cudaStream_t st) {
-  dim3 grid(H, (M + kRowsPerCta - 1) / kRowsPerCta), block(128);
+  dim3 grid(H, (M + kRowsPerCta - 1) / kRowsPerCta, d_g / kAbsorbCols), block(128);
   const auto* qr = static_cast<const __nv_bfloat16*>(q_rope);
   auto* qc = static_cast<__nv_bfloat16*>(q_cat);
+  const int smem = 2 * kBox + (kAbsorbCols / 64) * kBox + 1024;
   if (d_g == 512) {
-    const int smem = 2 * kBox + 8 * kBox + 1024;
     cudaError_t e = set_smem(absorb_kernel<512>, smem);
     if (e != cudaSuccess) return e;
-    absorb_kernel<512><<<grid, block, smem, st>>>(tmA, tmB, qr, qc, M, H);
+    return launch_chained(absorb_kernel<512>, grid, block, smem, st, tmA, tmB, qr, qc, M, H);
   } else {
-    const int smem = 2 * kBox + 4 * kBox + 1024;
     cudaError_t e = set_smem(absorb_kernel<256>, smem);
     if (e != cudaSuccess) return e;
-    absorb_kernel<256><<<grid, block, smem, st>>>(tmA, tmB, qr, qc, M, H);
+    return launch_chained(absorb_kernel<256>, grid, block, smem, st, tmA, tmB, qr, qc, M, H);
   }
   return cudaGetLastError();
 }
 
 cudaError_t launch_project(const CUtensorMap& tmA, const CUtensorMap& tmB, void* out, int M, int H,
                            int d_g, cudaStream_t st) {
-  dim3 grid(H, (M + kRowsPerCta - 1) / kRowsPerCta), block(128);
-  const int smem = 4 * 2 * kBox + 1024;
+  dim3 grid(H, (M + kRowsPerCta - 1) / kRowsPerCta, kDhc / kProjectCols), block(128);
+  const int smem = 4 * (kBox + kProjectCols * 64 * 2) + 1024;
   auto* o = static_cast<__nv_bfloat16*>(out);
   if (d_g == 512) {
     cudaError_t e = set_smem(project_kernel<512>, smem);
     if (e != cudaSuccess) return e;
-    project_kernel<512><<<grid, block, smem, st>>>(tmA, tmB, o, M, H);
+    return launch_chained(project_kernel<512>, grid, block, smem, st, tmA, tmB, o, M, H);
   } else {
     cudaError_t e = set_smem(project_kernel<256>, smem);
     if (e != cudaSuccess) return e;
-    project_kernel<256><<<grid, block, smem, st>>>(tmA, tmB, o, M, H);
+    return launch_chained(project_kernel<256>, grid, block, smem, st, tmA, tmB, o, M, H);
   }
   return cudaGetLastError();
 }

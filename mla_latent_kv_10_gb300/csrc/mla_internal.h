@@ -2,6 +2,7 @@
 #pragma once
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -94,6 +95,25 @@ cudaError_t launch_plan(const int32_t* seq_lens, const int32_t* block_table, WsH
 // (32 x 128 boxes, 64-byte swizzle)
 cudaError_t launch_decode(const CUtensorMap& tm_cache, const CUtensorMap& tm_rope, const CUtensorMap& tm_qrope,
                           const DecodeArgs& a, int units, int csize, cudaStream_t st);
+// Launch with programmatic stream serialization: the kernel may start its
+// set-up while the kernel before it on the stream finishes (every kernel of
+// this library waits for its predecessor before touching global memory).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_chained(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                           Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 cudaError_t launch_combine(const float* o_part, const float* lse_part, const WsHeader* ws,
                            void* o_lat, float* lse, int B, int Lq, int H, int G, cudaStream_t st);
 int decode_max_units(int csize, int* units);  // clusters of csize CTAs resident at once

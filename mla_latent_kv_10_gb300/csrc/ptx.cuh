@@ -90,6 +90,19 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// ------------------------------------------------------------------ launch chaining
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start while the kernel before it on the stream still
+// runs.  griddep_wait() blocks until that kernel has completed and its
+// memory is visible; every global read or write of this library's kernels
+// comes after it.  griddep_launch_dependents() lets the next kernel start
+// its own set-up; it is called only after griddep_wait(), so when kernel
+// k+1 starts, kernel k-1 has completed.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ registers
 // Move a warpgroup's per-thread register allocation down or up (every warp of
 // the warpgroup executes the same instruction).  An increase waits until
