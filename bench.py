@@ -4,6 +4,9 @@ A step is the whole hot path on one batch of synthetic input:
     mla_absorb_q -> mla_decode_paged -> mla_combine_splits -> mla_project_uv
 (mla_decode_paged is one kernel launch for B <= 448: the decode kernel
 computes its own split; larger batches add a plan kernel before it.)
+Each step is one CUDA-graph replay (the kernels chain by programmatic
+dependent launch); the decode kernel is also timed alone, by events around
+replays of a graph holding only it.
 
 Default workload: DeepSeek-V3 dims, B=16, Lq=1, H=128, all seq_lens 4096,
 64-token pages, contiguous block tables.  Its 75.5 MB cache fits in the
@@ -280,34 +283,28 @@ def main():
     if status != 0:
         raise SystemExit("device status after warm-up: %s" % mla.mla_status_string(status))
 
-    # The timed loop replays CUDA graphs of the same calls (no host launch
-    # overhead); events around the decode graph time mla_decode_paged alone.
+    # The timed loops replay CUDA graphs of the same calls (no host launch
+    # overhead): one graph per step (per cache copy), and, for the decode
+    # kernel's own duration, graphs holding only mla_decode_paged with events
+    # around each replay.
     side = torch.cuda.Stream(dev)
     side.wait_stream(stream)
     with torch.cuda.stream(side):
-        g_pre, g_post = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        g_step = [torch.cuda.CUDAGraph() for _ in range(copies)]
         g_dec = [torch.cuda.CUDAGraph() for _ in range(copies)]
-        with torch.cuda.graph(g_pre, stream=side):
-            pre()
         for c in range(copies):
+            with torch.cuda.graph(g_step[c], stream=side):
+                pre()
+                dec(c)
+                post()
             with torch.cuda.graph(g_dec[c], stream=side):
                 dec(c)
-        with torch.cuda.graph(g_post, stream=side):
-            post()
     stream.wait_stream(side)
     torch.cuda.synchronize(dev)
 
-    def gstep(i, ev=None):
-        g_pre.replay()
-        if ev is not None:
-            ev[0].record(stream)
-        g_dec[i % copies].replay()
-        if ev is not None:
-            ev[1].record(stream)
-        g_post.replay()
-
     for i in range(max(3, args.warmup)):
-        gstep(i)
+        g_step[i % copies].replay()
+        g_dec[i % copies].replay()
     torch.cuda.synchronize(dev)
 
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
@@ -320,8 +317,12 @@ def main():
     time.sleep(0.3)
     t_start.record(stream)
     for i in range(args.steps):
-        gstep(i, evs[i])
+        g_step[i % copies].replay()
     t_end.record(stream)
+    for i in range(args.steps):
+        evs[i][0].record(stream)
+        g_dec[(i + args.steps) % copies].replay()  # continue the rotation of cache copies
+        evs[i][1].record(stream)
     torch.cuda.synchronize(dev)
     clocks = sampler.stop()
     if pg:
@@ -392,8 +393,9 @@ def main():
                      "kernel": "mla_decode_paged"},
         "e2e": {"value": world * step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": mla.launches_per_step(case.dims) * args.steps,
-        "timing": "CUDA graph replays of the API calls; decode timed by events around its graph",
+        "gpu_launches": (mla.launches_per_step(case.dims) + mla.mla_decode_kernel_launches(case.dims)) * args.steps,
+        "timing": "one CUDA-graph replay per step (kernels chained by programmatic dependent launch); "
+                  "decode timed alone by events around replays of a decode-only graph",
         "clocks": clocks,
         "device_status": mla.mla_status_string(status),
     }
