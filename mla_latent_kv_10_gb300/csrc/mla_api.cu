@@ -171,7 +171,7 @@ int mla_decode_paged(const mla_dims* d, const void* q_cat, const void* kv_cache,
   if ((rc = decode_max_units(csize, &units)) != MLA_OK) return rc;
   if (num_splits > 0 && num_splits < units) units = num_splits;
   auto st = static_cast<cudaStream_t>(stream);
-  CUtensorMap tm, tm_rope, tm_qrope;
+  CUtensorMap tm, tm_rope, tm_qrope, tm_qlat;
   {
     cuuint64_t dims[2] = {(cuuint64_t)kRow, (cuuint64_t)d->num_pages * kPage};
     cuuint64_t strides[1] = {(cuuint64_t)kRow * 2};
@@ -187,6 +187,8 @@ int mla_decode_paged(const mla_dims* d, const void* q_cat, const void* kv_cache,
     cuuint64_t strides[1] = {(cuuint64_t)d_q * 2};
     cuuint32_t box[2] = {32, kRowsPerCta};
     if ((rc = make_map(&tm_qrope, q_cat, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B)) != MLA_OK) return rc;
+    cuuint32_t lbox[2] = {64, kRowsPerCta};
+    if ((rc = make_map(&tm_qlat, q_cat, 2, dims, strides, lbox)) != MLA_OK) return rc;
   }
   auto* ws = static_cast<WsHeader*>(workspace);
   // Small batches are split by the decode kernel itself (one launch);
@@ -216,7 +218,7 @@ int mla_decode_paged(const mla_dims* d, const void* q_cat, const void* kv_cache,
   a.plan_in_kernel = in_kernel ? 1 : 0;
   a.units = units;
   a.seq_lens = seq_lens;
-  return cuda_status(launch_decode(tm, tm_rope, tm_qrope, a, units, csize, st));
+  return cuda_status(launch_decode(tm, tm_rope, tm_qrope, tm_qlat, a, units, csize, st));
 }
 
 int mla_combine_splits(const mla_dims* d, const float* o_part, const float* lse_part,

@@ -28,6 +28,13 @@
 //     The page tile in shared memory is used twice: K-major as B for
 //     S = Q.K^T and MN-major as B for O += P.V.  With two P buffers the
 //     softmax of page q+1 never waits for P.V of page q.
+//   * The first segment's query arrives by TMA ahead of the first page: its
+//     latent half into the four (still idle) exchange slots, whence the
+//     softmax warps move it into tensor memory, and its RoPE half into its
+//     shared-memory tile.  Later segments' queries are loaded by the softmax
+//     warps with plain loads.  The exchange slots are handed to the peer
+//     (tensor-memory commit multicast on its "can send" barriers) only once
+//     the query has left them.
 //   * Pages arrive by TMA (four 64 x 64 latent boxes with 128-byte swizzle,
 //     one 32 x 64 RoPE box with 64-byte swizzle) into a 4-stage mbarrier
 //     ring; one thread issues MMAs, one thread issues copies, four exchange
@@ -141,10 +148,13 @@ __device__ __forceinline__ void set_status(WsHeader* ws, int code) {
 //   p_full   P(p) is in receive slot b
 //   o_done   P.V of page p is done
 //   can_send the peer's P.V of page p is done: its receive slot b and our
-//            send slot b are free again (arrives from the peer's MMA)
+//            send slot b are free again (arrives from the peer's MMA);
+//            phase 0 instead says the peer's first query left its slots
+//   q_lat    the first segment's query (latent half in the exchange slots,
+//            RoPE half in its tile) landed
 struct DecodeShared {
   uint64_t full[kStages], empty[kStages];
-  uint64_t q_full, drain;
+  uint64_t q_full, q_lat, drain;
   uint64_t s_full[2], xfull[2], s_free[2], p_full[2], o_done[2], can_send[2];
   float red[2][2][kRowsPerCta];  // [parity][key half][row]: partial row maxima (row sums at a segment's end)
   UnitRec rec;                   // this CTA's work unit
@@ -352,7 +362,8 @@ __device__ void plan_in_block(const DecodeArgs& a, int unit, bool writer, int* s
 
 __global__ void __launch_bounds__(kDecodeThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tm_cache, const __grid_constant__ CUtensorMap tm_rope,
-                  const __grid_constant__ CUtensorMap tm_qrope, const DecodeArgs a) {
+                  const __grid_constant__ CUtensorMap tm_qrope, const __grid_constant__ CUtensorMap tm_qlat,
+                  const DecodeArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* stages = smem;
   uint8_t* xbuf = smem + kXOff;  // [send 2][receive 2] x 16 KiB
@@ -383,6 +394,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       mbar_init(bar(sh.empty[s]), 1);
     }
     mbar_init(bar(sh.q_full), kSoftmaxThreads);
+    mbar_init(bar(sh.q_lat), 1);
     mbar_init(bar(sh.drain), 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(sh.s_full[s]), 1);
@@ -397,6 +409,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     tma_prefetch_desc(&tm_cache);
     tma_prefetch_desc(&tm_rope);
     tma_prefetch_desc(&tm_qrope);
+    tma_prefetch_desc(&tm_qlat);
   }
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(&sh.tmem), kTmemCols);
@@ -420,6 +433,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   } else if (threadIdx.x == 0) {
     sh.rec = ws_view(ws, a.B).rec[unit];
   }
+  fence_proxy_async();  // the plan's scratch writes come before the query copies into the same slots
   __syncthreads();
 
   auto fail = [&]() {
@@ -450,6 +464,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           if (page < 0 || page >= a.num_pages) {  // never dereferenced: clamped and reported
             set_status(ws, MLA_ERR_BAD_TABLE);
             page = 0;
+          }
+          if (pc == 0) {  // the first segment's query, ahead of its first page
+            const int qy = sb * a.Lq * a.H + (int)rg * kRowsPerCta;
+            const int qx = a.G == 1 ? (int)r * 256 : 0;
+            mbar_arrive_expect_tx(bar(sh.q_lat), 4 * kXSlot + kQRopeBytes);
+            for (int j = 0; j < 4; ++j)
+              tma_load_2d(xsrc + j * kXSlot, &tm_qlat, bar(sh.q_lat), qx + 64 * j, qy);
+            tma_load_2d(qrope, &tm_qrope, bar(sh.q_lat), a.d_g + 32 * (int)r, qy);
           }
           const uint32_t dst = smem_u32(stages + st * kStageBytes);
           mbar_arrive_expect_tx(bar(sh.full[st]), bytes);
@@ -487,6 +509,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16(128, 64, false, false);
       const uint64_t qr0 = sdesc_sw64(qrope, 512);
+      const uint16_t peer_mask = (uint16_t)(1u << peer);
       PageCursor c;
       c.init(sh.rec, a);
       uint32_t pc = 0, qc = 0;
@@ -494,6 +517,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       while (ok && c.valid) {
         if (c.seg_first()) {  // the segment's query (loaded after every QK before it finished)
           if (!(ok = mbar_wait(bar(sh.q_full), qc & 1, abort))) break;
+          if (qc == 0) {  // the first query left the exchange slots: the peer may send into them
+            mma_commit_multicast(bar(sh.can_send[0]), peer_mask);
+            mma_commit_multicast(bar(sh.can_send[1]), peer_mask);
+          }
           ++qc;
           tc_fence_after();
         }
@@ -579,8 +606,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         }
         tc_fence_before();
         mbar_arrive(bar(sh.s_free[b]));
-        // the peer's P.V two pages back freed its receive slot and our send slot
-        if (p >= 2) ok = mbar_wait<true>(bar(sh.can_send[b]), ((p - 2) >> 1) & 1, abort);
+        // the peer's P.V two pages back (for the first two pages: its first
+        // query leaving its slots) freed its receive slot and our send slot
+        ok = mbar_wait<true>(bar(sh.can_send[b]), (p >> 1) & 1, abort);
         ok = __all_sync(0xffffffffu, ok);
         if (ok) {
           const uint32_t dst = xsrc + b * kXSlot + row * 128;
@@ -665,10 +693,33 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       if (t.next(a, b2, pa2, pb2)) prefetch_q(b2);
     };
 
+    // the first segment's query: latent half from the exchange slots (box
+    // j = 64 columns, 128-byte swizzle), RoPE half already in its tile
+    auto load_q_first = [&]() {
+      ok = mbar_wait(bar(sh.q_lat), 0, abort);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) return;
+      const bool use = valid && (a.G == 1 || (uint32_t)g == r);
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {
+        uint32_t w[32];
+        const uint32_t src = xsrc + (2 * half + c) * kXSlot + row * 128;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          ld_shared_v4(src + ((k ^ (row & 7)) << 4), w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+          if (!use) w[4 * k] = w[4 * k + 1] = w[4 * k + 2] = w[4 * k + 3] = 0u;
+        }
+        tmem_st32(lane_base + kColQ + 64 * half + 32 * c, w);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(sh.q_full));
+    };
+
     PageCursor cur;
     cur.init(sh.rec, a);
     if (cur.valid) {
-      load_q(cur.sb);
+      load_q_first();
       prefetch_after(cur.it);
     }
     float m_used = -INFINITY, l_part = 0.f;
@@ -1138,12 +1189,12 @@ int decode_max_units(int csize, int* units) {
 }
 
 cudaError_t launch_decode(const CUtensorMap& tm_cache, const CUtensorMap& tm_rope, const CUtensorMap& tm_qrope,
-                          const DecodeArgs& a, int units, int csize, cudaStream_t st) {
+                          const CUtensorMap& tm_qlat, const DecodeArgs& a, int units, int csize, cudaStream_t st) {
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[2];
   cudaError_t e = decode_config(cfg, attr, units, csize, st);
   if (e != cudaSuccess) return e;
-  return cudaLaunchKernelEx(&cfg, decode_kernel, tm_cache, tm_rope, tm_qrope, a);
+  return cudaLaunchKernelEx(&cfg, decode_kernel, tm_cache, tm_rope, tm_qrope, tm_qlat, a);
 }
 
 cudaError_t launch_combine(const float* o_part, const float* lse_part, const WsHeader* ws, void* o_lat,

@@ -92,9 +92,10 @@ cudaError_t launch_plan(const int32_t* seq_lens, const int32_t* block_table, WsH
                         int Lq, int max_pages, int num_pages, int units, cudaStream_t st);
 // tm_cache: latent boxes (64 x 64, 128-byte swizzle); tm_rope: the cache's
 // RoPE columns (32 x 64 boxes, 64-byte swizzle); tm_qrope: q_cat rows
-// (32 x 128 boxes, 64-byte swizzle)
+// (32 x 128 boxes, 64-byte swizzle); tm_qlat: q_cat rows (64 x 128 boxes,
+// 128-byte swizzle)
 cudaError_t launch_decode(const CUtensorMap& tm_cache, const CUtensorMap& tm_rope, const CUtensorMap& tm_qrope,
-                          const DecodeArgs& a, int units, int csize, cudaStream_t st);
+                          const CUtensorMap& tm_qlat, const DecodeArgs& a, int units, int csize, cudaStream_t st);
 // Launch with programmatic stream serialization: the kernel may start its
 // set-up while the kernel before it on the stream finishes (every kernel of
 // this library waits for its predecessor before touching global memory).
