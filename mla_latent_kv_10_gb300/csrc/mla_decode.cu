@@ -84,6 +84,7 @@ constexpr int kDecodeThreads = 32 * (kPvWarp + 1);
 static_assert(kPlanInKernelMaxB <= kDecodeThreads, "the in-kernel plan takes one thread per sequence");
 // named barriers 1..4: the two softmax warps of a quadrant
 constexpr uint32_t kBarPair0 = 1;
+constexpr int kPlanWarpMaxB = 32;  // up to this batch one warp plans (lane = sequence)
 // tensor memory columns: O (256) | Q latent half (128, bf16 pairs) | two
 // score buffers (64 each)
 constexpr uint32_t kColO = 0, kColQ = 256, kColS = 384, kTmemCols = 512;
@@ -360,6 +361,98 @@ __device__ void plan_in_block(const DecodeArgs& a, int unit, bool writer, int* s
   __syncthreads();
 }
 
+__device__ __forceinline__ int warp_scan_incl(int v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int x = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += x;
+  }
+  return v;
+}
+
+// plan_in_block's split for B <= 32, computed by one warp (lane = sequence)
+// with shuffles and votes instead of block-wide barriers.  The balanced
+// split's widest unit is found by counting, per unit, the sequences that
+// start strictly inside it (the unit touches one more sequence than that).
+__device__ void plan_in_warp(const DecodeArgs& a, int unit, bool writer, UnitRec* out) {
+  const unsigned full = 0xffffffffu;
+  const int B = a.B, units = a.units, lane = threadIdx.x & 31;
+  const WsView v = ws_view(a.ws, B);
+  const int lo = a.Lq > 1 ? a.Lq : 1, hi = a.max_pages * kPage;
+  const bool act = lane < B;
+  int np = 0;
+  if (act) {
+    const int n0 = a.seq_lens[lane];
+    const int n = clamp_len(n0, lo, hi);
+    if (writer) {
+      if (n != n0) set_status(a.ws, MLA_ERR_BAD_SEQLEN);
+      v.nlen[lane] = n;
+    }
+    np = (n + kPage - 1) / kPage;
+  }
+  const int incl = warp_scan_incl(np);
+  const int total = __shfl_sync(full, incl, 31);
+  const int off = incl - np;
+  const int chunk = total > 0 ? (total + units - 1) / units : 1;
+
+  const bool inner = act && off % chunk != 0;  // sequence starts inside unit off / chunk
+  const int key = inner ? off / chunk : -1 - lane;
+  const unsigned same = __match_any_sync(full, key);
+  const int segs = 1 + (int)__reduce_max_sync(full, inner ? (unsigned)__popc(same) : 0u);
+  const int cost_bal = chunk + kSwitchPages * (segs - 1);
+
+  const bool feasible = B <= units && total > 0;
+  int u = 0, worst = 0;
+  if (feasible && act) {
+    u = aligned_units(np, units, total);
+    worst = (np + u - 1) / u;
+  }
+  const int uincl = warp_scan_incl(u);
+  const int used = __shfl_sync(full, uincl, 31);
+  const int u0 = uincl - u;
+  worst = (int)__reduce_max_sync(full, (unsigned)worst);
+  const int cost_al = (feasible && used <= units) ? worst : INT_MAX;
+  const int mode = cost_al <= cost_bal ? 1 : 0;
+
+  UnitRec rec{0, 0, 0, 0, 0};
+  if (mode == 1) {
+    const unsigned m = __ballot_sync(full, act && u0 <= unit);  // lane 0 always: u0 = 0
+    const int l0 = 31 - __clz(m);
+    const int nb = __shfl_sync(full, np, l0), ub = __shfl_sync(full, u, l0), j = unit - __shfl_sync(full, u0, l0);
+    if (unit < used)
+      rec = UnitRec{l0, 0, (int)(((long long)j * nb) / ub), (int)(((long long)(j + 1) * nb) / ub), unit - l0};
+  } else {
+    const int st = min(unit * chunk, total), en = min(st + chunk, total);
+    const unsigned m = __ballot_sync(full, act && off <= st);
+    const int l0 = 31 - __clz(m);
+    rec = UnitRec{l0, __shfl_sync(full, off, l0), st, en, unit};
+  }
+  if (lane == 0) *out = rec;
+  if (writer) {
+    if (act) {
+      v.off[lane] = off;
+      if (mode == 1) {
+        v.slot0[lane] = u0;
+        v.nslot[lane] = u;
+      } else {
+        const int kf = off / chunk, kl = (off + np - 1) / chunk;
+        v.slot0[lane] = lane + kf;
+        v.nslot[lane] = kl - kf + 1;
+      }
+    }
+    if (lane == 0) {
+      v.off[B] = total;
+      a.ws->total = total;
+      a.ws->chunk = chunk;
+      a.ws->units = units;
+      a.ws->B = B;
+      a.ws->mode = mode;
+    }
+  }
+  __syncwarp();
+}
+
 __global__ void __launch_bounds__(kDecodeThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tm_cache, const __grid_constant__ CUtensorMap tm_rope,
                   const __grid_constant__ CUtensorMap tm_qrope, const __grid_constant__ CUtensorMap tm_qlat,
@@ -425,9 +518,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   griddep_wait();
   griddep_launch_dependents();
 
-  // the work split: computed here (the exchange slots are still unused and
-  // serve as scratch), or read from the plan kernel's records
-  if (a.plan_in_kernel) {
+  // the work split: computed here (by one warp for small batches, else by
+  // the whole block with the still unused exchange slots as scratch), or
+  // read from the plan kernel's records
+  if (a.plan_in_kernel && a.B <= kPlanWarpMaxB) {
+    if (warp == 0) plan_in_warp(a, unit, unit == 0 && crank == 0, &sh.rec);
+  } else if (a.plan_in_kernel) {
     plan_in_block(a, unit, unit == 0 && crank == 0, reinterpret_cast<int*>(xbuf),
                   reinterpret_cast<int*>(xbuf) + 3 * a.B + 8, &sh.rec);
   } else if (threadIdx.x == 0) {

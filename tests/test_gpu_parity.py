@@ -94,6 +94,63 @@ def test_decode_large_batch(B, Lq, launches):
     check_case(c, got, pairs)
 
 
+def _expected_split(lens, Lq, units):
+    """The work split restated from its rule: pages per sequence; the
+    balanced cut (equal contiguous ranges of the flattened page list, cost =
+    pages per unit + 4 per extra sequence a unit touches) against the
+    sequence-aligned one (units shared out in proportion to pages, cost =
+    most pages a unit gets); the cheaper one, ties to sequence-aligned."""
+    nps = [(max(n, Lq, 1) + 63) // 64 for n in lens]
+    off = np.concatenate([[0], np.cumsum(nps)]).astype(np.int64)
+    B, total = len(lens), int(off[-1])
+    chunk = -(-total // units)
+    segs = 1
+    for k in range(units):
+        st, en = min(k * chunk, total), min(k * chunk + chunk, total)
+        if st < en:
+            segs = max(segs, int(np.sum((off[:-1] < en) & (off[1:] > st))))
+    cost_bal = chunk + 4 * (segs - 1)
+    u = [min(n, max(1, units * n // total)) for n in nps]
+    worst = max(-(-n // x) for n, x in zip(nps, u))
+    cost_al = worst if (B <= units and sum(u) <= units) else math.inf
+    mode = 1 if cost_al <= cost_bal else 0
+    if mode == 1:
+        slot0, nslot = list(np.concatenate([[0], np.cumsum(u)[:-1]])), u
+    else:
+        kf = [int(off[b]) // chunk for b in range(B)]
+        kl = [(int(off[b]) + nps[b] - 1) // chunk for b in range(B)]
+        slot0, nslot = [b + kf[b] for b in range(B)], [kl[b] - kf[b] + 1 for b in range(B)]
+    return dict(total=total, chunk=chunk, mode=mode, off=list(off), slot0=slot0, nslot=nslot)
+
+
+@pytest.mark.parametrize("B", [32, 33])
+@pytest.mark.parametrize("mix", ["skew", "one_long"])
+def test_split_matches_rule(B, mix):
+    """The split the decode kernel writes to the workspace (one planning warp
+    up to 32 sequences, the whole block above) against the rule restated in
+    Python; the outputs against the oracle on a few heads."""
+    rng = np.random.default_rng(B)
+    lens = [int(x) for x in rng.integers(1, 3000, size=B)] if mix == "skew" else [64] * (B - 1) + [20000]
+    c = make_case(B=B, Lq=1, H=16, seq_lens=lens, table="perm", seed=60 + B)
+    t = {k: v.cuda() for k, v in c.tensors().items()}
+    bufs = mla.DecodeBuffers(c.dims)
+    mla.decode_step(c.dims, bufs, t["q_nope"], t["q_rope"], t["W_UK"], t["W_UV"], t["cache"],
+                    t["block_table"], t["seq_lens"])
+    assert mla.mla_get_device_status(bufs.workspace) == 0
+    ws = bufs.workspace.cpu().view(torch.int32).numpy()
+    status, total, chunk, units, wB, mode = ws[:6]
+    assert wB == B
+    want = _expected_split(lens, 1, int(units))
+    assert (total, chunk, mode) == (want["total"], want["chunk"], want["mode"])
+    body = ws[8:]
+    assert list(body[:B + 1]) == want["off"]
+    assert list(body[B + 1:2 * B + 1]) == lens
+    assert list(body[2 * B + 1:3 * B + 1]) == want["slot0"]
+    assert list(body[3 * B + 1:4 * B + 1]) == want["nslot"]
+    got = dict(o_lat=bufs.o_lat.cpu(), lse=bufs.lse.cpu(), out=bufs.out.cpu())
+    check_case(c, got, [(b, h) for b in (0, B // 2, B - 1) for h in (0, 15)])
+
+
 @pytest.mark.parametrize("splits", [1, 3, 7])
 def test_split_count_invariance(splits):
     """Any number of work units gives the same result (fp32 merge order
