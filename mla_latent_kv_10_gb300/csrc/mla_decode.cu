@@ -1,5 +1,5 @@
 // mla_decode.cu — split-KV flash-decoding of MLA over the paged latent cache
-// (plan kernel, decode kernel, log-sum-exp combine kernel).
+// (plan kernel and decode kernel; the partials are merged by mla_combine.cu).
 //
 // Method: MLA operator write-up (nxmr.cn/news/151634) §1 (cache row = 512-d
 // latent + 64-d RoPE key), §3 (64-token pages, a tile of 64 tokens, a
@@ -46,7 +46,7 @@
 //   * Split-KV: the pages of all sequences, in order, are cut into equal
 //     contiguous ranges, one per cluster; a range that covers parts of several
 //     sequences yields one partial (o, lse) per sequence, stored in slot
-//     b + unit.  The combine kernel merges them.
+//     b + unit.  The combine kernel (mla_combine.cu) merges them.
 //   * Every wait is bounded (wall clock); on expiry the kernel records
 //     MLA_ERR_TIMEOUT in the workspace status word, stops, waits for its own
 //     copies and MMAs, frees tensor memory and returns.
@@ -1107,127 +1107,6 @@ __global__ void __launch_bounds__(1024)
   }
 }
 
-// ---------------------------------------------------------------- combine
-// One CTA per (sequence, 32 query rows, quarter of the latent slice).  The
-// log-sum-exp of each row's partials is reduced with warp shuffles over the
-// partial index and turned into per-partial weights in shared memory; the
-// weighted sum then reads the chunk-major partials coalesced (32
-// consecutive rows per warp access).  The bf16 result is staged in shared
-// memory and written out as contiguous row pieces.
-constexpr int kCombineRows = 32, kCombineSplit = 4, kCombineMaxSeg = 64;
-template <int DG>
-__global__ void __launch_bounds__(256)
-    combine_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part,
-                   const WsHeader* __restrict__ ws, __nv_bfloat16* __restrict__ o_lat,
-                   float* __restrict__ lse_out, int B, int Lq, int H, int G) {
-  constexpr int kCols = DG / kCombineSplit;  // columns of this CTA
-  __shared__ __align__(16) __nv_bfloat16 tile[kCombineRows][kCols + 8];
-  __shared__ float wts[kCombineMaxSeg][kCombineRows];
-  __shared__ float lrow[kCombineRows];
-  const int rows = Lq * H;
-  const int b = blockIdx.x, r0 = blockIdx.y * kCombineRows, cz = blockIdx.z;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  griddep_wait();
-  griddep_launch_dependents();
-  const WsView v = ws_view(ws, B);
-  const int nseg = v.nslot[b];
-  const size_t seg0 = (size_t)v.slot0[b];
-  const bool table = nseg <= kCombineMaxSeg;
-
-  // log-sum-exp per row (warp w: rows w, w+8, w+16, w+24), then weights.
-  // Lane j keeps partial j's value (and j+32's) of the four rows in
-  // registers: one load round for all of them.
-  constexpr int kRowsPerWarp = kCombineRows / 8;
-  float x0[kRowsPerWarp], x1[kRowsPerWarp];
-#pragma unroll
-  for (int k = 0; k < kRowsPerWarp; ++k) {
-    const int row = r0 + warp + 8 * k;
-    x0[k] = (row < rows && lane < nseg) ? lse_part[(seg0 + lane) * rows + row] : -INFINITY;
-    x1[k] = (row < rows && lane + 32 < nseg) ? lse_part[(seg0 + lane + 32) * rows + row] : -INFINITY;
-  }
-#pragma unroll
-  for (int k = 0; k < kRowsPerWarp; ++k) {
-    const int rr = warp + 8 * k, row = r0 + rr;
-    float L = -INFINITY;
-    if (row < rows) {
-      float mx = fmaxf(x0[k], x1[k]);
-      for (int j = lane + 64; j < nseg; j += 32) mx = fmaxf(mx, lse_part[(seg0 + j) * rows + row]);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-      float sum = 0.f;
-      if (mx != -INFINITY) {
-        sum = expf(x0[k] - mx) + expf(x1[k] - mx);
-        for (int j = lane + 64; j < nseg; j += 32) sum += expf(lse_part[(seg0 + j) * rows + row] - mx);
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-      L = (mx == -INFINITY) ? -INFINITY : mx + logf(sum);
-      if (table) {
-        if (lane < nseg) wts[lane][rr] = (L == -INFINITY) ? 0.f : expf(x0[k] - L);
-        if (lane + 32 < nseg) wts[lane + 32][rr] = (L == -INFINITY) ? 0.f : expf(x1[k] - L);
-      }
-    }
-    if (lane == 0) {
-      lrow[rr] = L;
-      if (row < rows && lse_out && cz == 0) lse_out[(size_t)b * rows + row] = L;
-    }
-  }
-  __syncthreads();
-
-  // weighted sum: thread = (row lane, chunk group warp); every load of a
-  // partial for all of the thread's chunks is issued before any is used
-  const int row = r0 + lane;
-  const bool valid = row < rows;
-  const int h = valid ? row % H : 0, g = (h * G) / H;
-  const float L = lrow[lane];
-  constexpr int kChunks = kCols / 4, kPer = kChunks / 8;  // chunks of this thread: warp + 8k
-  float4 acc[kPer];
-#pragma unroll
-  for (int k = 0; k < kPer; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (valid && L != -INFINITY) {
-    const int c0 = g * (DG / 4) + cz * kChunks + warp;  // first 4-column chunk of the full latent
-    const float4* src = reinterpret_cast<const float4*>(o_part) + (size_t)c0 * rows + row;
-    const size_t slot_stride = (size_t)(kDc / 4) * rows, chunk_stride = (size_t)8 * rows;
-    constexpr int kBatch = 4;  // partials whose loads are all issued before any is used
-#pragma unroll 1
-    for (int j0 = 0; j0 < nseg; j0 += kBatch) {
-      float4 v[kBatch][kPer];
-#pragma unroll
-      for (int jj = 0; jj < kBatch; ++jj) {
-        const float4* sj = src + (seg0 + j0 + jj) * slot_stride;
-#pragma unroll
-        for (int k = 0; k < kPer; ++k)
-          v[jj][k] = (j0 + jj < nseg) ? __ldcs(sj + k * chunk_stride) : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-#pragma unroll
-      for (int jj = 0; jj < kBatch; ++jj) {
-        const int j = j0 + jj;
-        const float w = j >= nseg ? 0.f : table ? wts[j][lane] : expf(lse_part[(seg0 + j) * rows + row] - L);
-#pragma unroll
-        for (int k = 0; k < kPer; ++k) {
-          acc[k].x += w * v[jj][k].x; acc[k].y += w * v[jj][k].y;
-          acc[k].z += w * v[jj][k].z; acc[k].w += w * v[jj][k].w;
-        }
-      }
-    }
-  }
-#pragma unroll
-  for (int k = 0; k < kPer; ++k) {
-    uint2 pk;
-    pk.x = pack_bf16x2(acc[k].x, acc[k].y);
-    pk.y = pack_bf16x2(acc[k].z, acc[k].w);
-    *reinterpret_cast<uint2*>(&tile[lane][(warp + 8 * k) * 4]) = pk;
-  }
-  __syncthreads();
-  constexpr int kPieces = kCols * 2 / 16;  // 16-byte pieces per row
-  for (int i = threadIdx.x; i < kCombineRows * kPieces; i += 256) {
-    const int rr = i / kPieces, pc = i % kPieces;
-    if (r0 + rr < rows)
-      reinterpret_cast<uint4*>(o_lat + ((size_t)b * rows + r0 + rr) * DG + cz * kCols)[pc] =
-          *reinterpret_cast<const uint4*>(&tile[rr][pc * 8]);
-  }
-}
-
 }  // namespace
 
 cudaError_t launch_plan(const int32_t* seq_lens, const int32_t* block_table, WsHeader* ws, int B,
@@ -1293,12 +1172,5 @@ cudaError_t launch_decode(const CUtensorMap& tm_cache, const CUtensorMap& tm_rop
   return cudaLaunchKernelEx(&cfg, decode_kernel, tm_cache, tm_rope, tm_qrope, tm_qlat, a);
 }
 
-cudaError_t launch_combine(const float* o_part, const float* lse_part, const WsHeader* ws, void* o_lat,
-                           float* lse, int B, int Lq, int H, int G, cudaStream_t st) {
-  dim3 grid(B, (Lq * H + kCombineRows - 1) / kCombineRows, kCombineSplit), block(256);
-  auto* ol = static_cast<__nv_bfloat16*>(o_lat);
-  if (G == 1) return launch_chained(combine_kernel<512>, grid, block, 0, st, o_part, lse_part, ws, ol, lse, B, Lq, H, G);
-  return launch_chained(combine_kernel<256>, grid, block, 0, st, o_part, lse_part, ws, ol, lse, B, Lq, H, G);
-}
 
 }  // namespace mla

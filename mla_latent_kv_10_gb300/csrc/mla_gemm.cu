@@ -66,6 +66,8 @@ __global__ void __launch_bounds__(128)
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    // the weight tiles do not depend on the kernel before: start them now
+    for (int nb = 0; nb < kAbsorbCols / 64; ++nb) tma_prefetch_l2_3d(&tmB, n0 + nb * 64, 0, h);
   }
   if (warp == 0) {
     tmem_alloc(smem_u32(&tmem_holder), kAbsorbCols);
@@ -159,6 +161,8 @@ __global__ void __launch_bounds__(128)
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    // the weight tiles do not depend on the kernel before: start them now
+    for (int c = 0; c < kChunks; ++c) tma_prefetch_l2_3d(&tmB, c * 64, n0, h);
   }
   if (warp == 0) {
     tmem_alloc(smem_u32(&tmem_holder), kProjectCols);
