@@ -394,7 +394,7 @@ def main():
         "e2e": {"value": world * step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": (mla.launches_per_step(case.dims) + mla.mla_decode_kernel_launches(case.dims)) * args.steps,
-        "timing": "one CUDA-graph replay per step (kernels chained by programmatic dependent launch); "
+        "timing": "one CUDA-graph replay per step (absorb, decode and projection chained by programmatic dependent launch; combine launched after the decode); "
                   "decode timed alone by events around replays of a decode-only graph",
         "clocks": clocks,
         "device_status": mla.mla_status_string(status),
