@@ -21,8 +21,10 @@
  *
  * Conventions shared by every entry point
  *   - All tensor arguments are DEVICE pointers owned by the caller. The
- *     library never allocates device memory, keeps no global state and never
- *     synchronises the stream except in mla_get_device_status.
+ *     library never allocates device memory and never synchronises the
+ *     stream except in mla_get_device_status.  Its only state is a
+ *     per-device cache of launch limits (found on first use, guarded by a
+ *     mutex) and the scratch array of mla_decode_attend_noalloc.
  *   - bf16 tensors are passed as raw 16-bit storage (void*); fp32 as float*;
  *     indices as int32.  All tensors are dense, row-major, no padding.
  *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL

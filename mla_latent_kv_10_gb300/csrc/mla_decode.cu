@@ -52,6 +52,7 @@
 //     copies and MMAs, frees tensor memory and returns.
 #include <climits>
 #include <cmath>
+#include <mutex>
 
 #include "mla_internal.h"
 #include "ptx.cuh"
@@ -1115,16 +1116,39 @@ cudaError_t launch_plan(const int32_t* seq_lens, const int32_t* block_table, WsH
   return cudaGetLastError();
 }
 
+// Per-device facts of the decode launch, found once per device and process:
+// whether the kernel's shared-memory limit has been raised there, and how
+// many clusters of 2 and of 4 CTAs fit at once.  Calls may come from several
+// host threads and for several devices, so the table is guarded by a mutex
+// (never held across a CUDA call).  Devices past the table are not cached.
+namespace {
+constexpr int kCachedDevices = 64;
+struct DecodeDeviceInfo {
+  bool smem_set;
+  int units[2];  // clusters of 2 and of 4 CTAs; 0 = not known yet
+};
+std::mutex g_decode_mu;
+DecodeDeviceInfo g_decode_info[kCachedDevices];
+}  // namespace
+
 static cudaError_t decode_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, int units,
                                  int csize, cudaStream_t st) {
-  static int configured_dev = -1;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (configured_dev != dev) {  // attribute is per device; set it again on a new one
+  const bool cached = dev >= 0 && dev < kCachedDevices;
+  bool set = false;
+  if (cached) {
+    std::lock_guard<std::mutex> lock(g_decode_mu);
+    set = g_decode_info[dev].smem_set;
+  }
+  if (!set) {  // the attribute is per device
     e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecodeSmem);
     if (e != cudaSuccess) return e;
-    configured_dev = dev;
+    if (cached) {
+      std::lock_guard<std::mutex> lock(g_decode_mu);
+      g_decode_info[dev].smem_set = true;
+    }
   }
   cfg = cudaLaunchConfig_t{};
   cfg.gridDim = dim3(units * csize);
@@ -1143,13 +1167,16 @@ static cudaError_t decode_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* a
 }
 
 int decode_max_units(int csize, int* units) {
-  static int cache_dev[2] = {-1, -1}, cache_val[2] = {0, 0};
   const int slot = csize == 2 ? 0 : 1;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_CUDA;
-  if (cache_dev[slot] == dev) {
-    *units = cache_val[slot];
-    return MLA_OK;
+  const bool cached = dev >= 0 && dev < kCachedDevices;
+  if (cached) {
+    std::lock_guard<std::mutex> lock(g_decode_mu);
+    if (g_decode_info[dev].units[slot] > 0) {
+      *units = g_decode_info[dev].units[slot];
+      return MLA_OK;
+    }
   }
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[2];
@@ -1157,8 +1184,10 @@ int decode_max_units(int csize, int* units) {
   int n = 0;
   if (cudaOccupancyMaxActiveClusters(&n, decode_kernel, &cfg) != cudaSuccess || n < 1) return MLA_ERR_CUDA;
   if (n > kMaxUnits) n = kMaxUnits;  // the workspace holds per-unit records for at most this many
-  cache_dev[slot] = dev;
-  cache_val[slot] = n;
+  if (cached) {
+    std::lock_guard<std::mutex> lock(g_decode_mu);
+    g_decode_info[dev].units[slot] = n;
+  }
   *units = n;
   return MLA_OK;
 }
