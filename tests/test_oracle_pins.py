@@ -278,3 +278,57 @@ def test_oracle_rejects_bad_tables():
     t.update(seq_lens=torch.tensor([37, 10_000], dtype=torch.int32))
     with pytest.raises(ValueError):
         oracle.decode(c.dims, **t)
+
+
+# ---------------------------------------------------------------- brute force
+
+def _brute_force(c, b, h):
+    """The naive-path definition written out key by key, independently of the
+    oracle: each key's cache row is looked up through the block table by
+    hand, its content key and value are formed by dot products with the
+    head's W_UK / W_UV rows, and the causal window, scaled softmax, latent
+    output and natural-log log-sum-exp follow the formulas directly."""
+    d = c.dims
+    Lq, H, G, P = d["Lq"], d["H"], d["G"], d["page_size"]
+    d_g = d["d_c"] // G
+    g = (h * G) // H
+    lat = slice(g * d_g, (g + 1) * d_g)
+    n = int(c.seq_lens[b])
+    cache, bt = bf(c.cache), c.block_table.numpy()
+    wk, wv = bf(c.W_UK)[h], bf(c.W_UV)[h]  # [d_hc, d_g]
+    outs, lats, lses = [], [], []
+    for l in range(Lq):
+        qn, qr = bf(c.q_nope)[b, l, h], bf(c.q_rope)[b, l, h]
+        last = n - Lq + l  # the newest key this query may see
+        scores, vals, rows = [], [], []
+        for s in range(last + 1):
+            row = cache[int(bt[b, s // P]), s % P]
+            ck, kr = row[lat], row[d["d_c"]:]
+            k = np.array([np.dot(wk[i], ck) for i in range(d["d_hc"])])
+            v = np.array([np.dot(wv[i], ck) for i in range(d["d_hc"])])
+            scores.append((np.dot(qn, k) + np.dot(qr, kr)) * d["scale"])
+            vals.append(v)
+            rows.append(ck)
+        m = max(scores)
+        e = [math.exp(x - m) for x in scores]
+        z = sum(e)
+        outs.append(sum(w / z * v for w, v in zip(e, vals)))
+        lats.append(sum(w / z * r for w, r in zip(e, rows)))
+        lses.append(m + math.log(z))
+    return np.array(outs), np.array(lats), np.array(lses)
+
+
+@pytest.mark.parametrize("B,Lq,H,G,lens", [(2, 1, 16, 1, [1, 70]), (2, 2, 16, 1, [2, 67]),
+                                           (1, 1, 32, 2, [130])])
+def test_oracle_matches_brute_force(B, Lq, H, G, lens):
+    """Tiny inputs spanning one to three pages of a shuffled table: the oracle
+    equals the key-by-key definition to fp64 rounding."""
+    c = make_case(B=B, Lq=Lq, H=H, G=G, seq_lens=lens, table="perm", seed=70 + B + Lq + G)
+    heads = [0, H // 2 - 1, H // 2, H - 1]
+    sel = [(b, h) for b in range(B) for h in heads]
+    out, o_lat, lse = oracle.decode(c.dims, **c.tensors(), sel=sel)
+    for b, h in sel:
+        bo, bl, be = _brute_force(c, b, h)
+        np.testing.assert_allclose(out[b, :, h], bo, rtol=1e-9, atol=1e-12)
+        np.testing.assert_allclose(o_lat[b, :, h], bl, rtol=1e-9, atol=1e-12)
+        np.testing.assert_allclose(lse[b, :, h], be, rtol=1e-12, atol=1e-12)
