@@ -142,6 +142,24 @@ def roofline_entry(dec_bytes, dec_flops, dec_ms, peaks, traffic, peak_src):
             "traffic": traffic, "peak_source": peak_src, "kernel": "mla_decode_paged"}
 
 
+def max_over_ranks(value, dist, device):
+    """The largest of one number over all ranks: a job's time is its slowest
+    rank's.  `dist` is torch.distributed with an initialised group (NCCL on
+    GPUs, gloo on host cores), or None for a single process."""
+    if dist is None:
+        return value
+    import torch
+    x = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(x, op=dist.ReduceOp.MAX)
+    return float(x.item())
+
+
+def job_rate(world, units_per_rank, ms):
+    """Whole-job throughput (units per second): what all ranks processed,
+    over the max-over-ranks time in milliseconds."""
+    return world * units_per_rank / (ms * 1e-3)
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -258,8 +276,8 @@ def main():
         pg = dist
     mla.load_library()
 
-    # each rank decodes its own batch (weak scaling): same shape, own seed
-    case = workload(args.workload) if rank == 0 else workload(args.workload)
+    # every rank decodes a replica of the same batch (weak scaling)
+    case = workload(args.workload)
     d = case.dims
     seq = case.seq_lens.tolist()
     B, Lq, H, G = d["B"], d["Lq"], d["H"], d["G"]
@@ -345,10 +363,7 @@ def main():
         pg.barrier()
     total_ms = t_start.elapsed_time(t_end)
     dec_ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
-    if pg:
-        x = torch.tensor([total_ms], device=dev)
-        pg.all_reduce(x, op=pg.ReduceOp.MAX)
-        total_ms = float(x.item())
+    total_ms = max_over_ranks(total_ms, pg, dev)
     ms = total_ms / args.steps
     status = mla.mla_get_device_status(bufs.workspace, stream)
 
@@ -375,10 +390,7 @@ def main():
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1) / args.steps
-    if pg:
-        x = torch.tensor([e2e_ms], device=dev)
-        pg.all_reduce(x, op=pg.ReduceOp.MAX)
-        e2e_ms = float(x.item())
+    e2e_ms = max_over_ranks(e2e_ms, pg, dev)
 
     peaks, peak_src = load_peaks()
     hbm = peaks["hbm_gbs"]
@@ -388,7 +400,7 @@ def main():
         return
     line = {
         "metric": METRIC,
-        "value": world * step_bytes / (ms * 1e-3) / 1e9,
+        "value": job_rate(world, step_bytes, ms) / 1e9,
         "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
@@ -397,15 +409,15 @@ def main():
                    "seq_len_mean": sum(seq) / len(seq), "page_size": 64,
                    "parallelism": "replicas" if world > 1 else "single",
                    "l2": "inputs larger than L2: %d rotating cache copies (%.0f MB)" % (copies, copies * cache_bytes / 1e6)},
-        "tflops": world * step_flops / (ms * 1e-3) / 1e12,
-        "tokens_per_s": world * B * Lq / (ms * 1e-3),
+        "tflops": job_rate(world, step_flops, ms) / 1e12,
+        "tokens_per_s": job_rate(world, B * Lq, ms),
         "roofline_frac_step": max(step_bytes / (ms * 1e-3) / 1e9 / hbm,
                                   step_flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"]),
         "decode_kernel": {"ms": dec_ms, "gbs": achieved, "tflops": tflops_dec,
                           "tensor_frac": tflops_dec / peaks["bf16_tflops"],
                           "bytes": dec_bytes, "flops": dec_flops},
         "roofline": roofline_entry(dec_bytes, dec_flops, dec_ms, peaks, decode_traffic(args.workload), peak_src),
-        "e2e": {"value": world * step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+        "e2e": {"value": job_rate(world, step_bytes, e2e_ms) / 1e9, "unit": "GB/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": (mla.launches_per_step(case.dims) + mla.mla_decode_kernel_launches(case.dims)) * args.steps,
         "timing": "one CUDA-graph replay per step (absorb, decode and projection chained by programmatic dependent launch; combine launched after the decode); "
