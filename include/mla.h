@@ -35,6 +35,12 @@
  *     workspace; read it with mla_get_device_status.
  *   - Nothing is thrown across the ABI.  Every call is thread-safe as long as
  *     concurrent calls do not share output buffers or workspaces.
+ *   - mla_absorb_q, mla_decode_paged and mla_project_uv launch their kernels
+ *     with programmatic dependent launch: a kernel may start its on-chip
+ *     set-up while the kernel before it on the stream is still running, but
+ *     reads and writes global memory only after that kernel has completed.
+ *     Stream order therefore holds for every caller kernel in between, as
+ *     for ordinary launches.
  *
  * Notation (dims struct):
  *   B batch, Lq new tokens per sequence, H heads, d_hc = 128 content head dim,
