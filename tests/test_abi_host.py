@@ -72,6 +72,21 @@ def test_decode_rejects_bad_arguments(lib):
     assert decode(lib, d, cache=A8) == -3
     assert decode(lib, d, q=A8) == -3
     assert decode(lib, d, op=A8) == -3
+    # int32 and fp32 arrays need 4-byte alignment only
+    assert decode(lib, d, bt=P(0x10002)) == -3
+    assert decode(lib, d, sl=P(0x10001)) == -3
+    assert decode(lib, d, lp=P(0x10002)) == -3
+
+
+def test_decode_rejects_index_overflow(lib):
+    """Token and table indices are 32-bit on the device: dims whose cache rows
+    or table entries would not fit are refused before any launch."""
+    d = dims()
+    d.num_pages = (1 << 31) // 64
+    assert decode(lib, d) == -2
+    d = dims()
+    d.max_pages_per_seq = (1 << 31) // 64
+    assert decode(lib, d) == -2
 
 
 @pytest.mark.parametrize("field,value,code", [
