@@ -29,6 +29,8 @@ def load():
         I, D = ctypes.c_int, ctypes.c_double
         lib.mla_oracle_decode.argtypes = [I] * 10 + [D, I] + [_u16p] * 5 + [_i32p] * 3 + [I] + [_f64p] * 3 + [I]
         lib.mla_oracle_decode.restype = I
+        lib.mla_oracle_decode_latent.argtypes = [I] * 9 + [D, I] + [_u16p] * 2 + [_i32p] * 3 + [I] + [_f64p] * 2 + [I]
+        lib.mla_oracle_decode_latent.restype = I
         lib.mla_oracle_scores_both.argtypes = [I] * 9 + [D] + [_u16p] * 4 + [_i32p] * 2 + [I] * 3 + [_f64p] * 2
         lib.mla_oracle_scores_both.restype = I
         lib.mla_oracle_absorb.argtypes = [I] * 4 + [_u16p] * 2 + [_f64p]
@@ -93,6 +95,34 @@ def decode(dims, q_nope, q_rope, W_UK, W_UV, cache, block_table, seq_lens,
     if rc != 0:
         raise ValueError("oracle rejected the inputs (seq_lens / block_table)")
     return out, o_lat, lse
+
+
+def decode_latent(dims, q_cat, cache, block_table, seq_lens, sel=None, nthreads=0):
+    """Latent-space decode from a given absorbed query q_cat [B,Lq,H,d_g+d_R]
+    (bf16): the absorbed scores q_cat . [c_g | k_R] * scale through the
+    softmax.  Returns (o_lat [B,Lq,H,d_g], lse [B,Lq,H]) as float64; with
+    ``sel`` only those (b, h) pairs are computed (others stay NaN)."""
+    lib = load()
+    B, Lq, H = dims["B"], dims["Lq"], dims["H"]
+    d_c, d_R, G = dims["d_c"], dims["d_R"], dims["G"]
+    d_g = d_c // G
+    o_lat = np.full((B, Lq, H, d_g), np.nan)
+    lse = np.full((B, Lq, H), np.nan)
+    qc, kc = _bits(q_cat), _bits(cache)
+    assert qc.shape == (B, Lq, H, d_g + d_R), qc.shape
+    bt, sl = _i32(block_table), _i32(seq_lens)
+    if sel is None:
+        selp, nsel = None, 0
+    else:
+        s = np.ascontiguousarray(np.asarray(sel, dtype=np.int32).reshape(-1, 2))
+        selp, nsel = _p(s, _i32p), s.shape[0]
+    rc = lib.mla_oracle_decode_latent(
+        B, Lq, H, d_c, d_R, G, dims["page_size"], dims["max_pages"], dims["num_pages"],
+        float(dims["scale"]), int(dims.get("causal", 1)), _p(qc, _u16p), _p(kc, _u16p),
+        _p(bt, _i32p), _p(sl, _i32p), selp, nsel, _p(o_lat, _f64p), _p(lse, _f64p), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle rejected the inputs (seq_lens / block_table)")
+    return o_lat, lse
 
 
 def scores_both(dims, q_nope, q_rope, W_UK, cache, block_table, seq_lens, b, l, h):

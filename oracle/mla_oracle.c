@@ -212,6 +212,88 @@ int mla_oracle_scores_both(int B, int Lq, int H, int d_hc, int d_c, int d_R, int
 }
 
 /*
+ * Decode in the latent space from a given absorbed query: §4 "path B" (the
+ * absorbed scores q_abs . c + q_R . k_R) carried through the softmax.  For
+ * each selected (b, h) (all when sel == NULL) and each l:
+ *   score_s = (q_cat[b,l,h,0:d_g] . c[s] + q_cat[b,l,h,d_g:] . k_R[s]) * scale
+ * over the visible keys s <= n - Lq + l (all n keys if causal == 0), with
+ * c[s] the latent slice of the head's group, then textbook softmax:
+ *   o_lat = sum_s p_s c[s],   lse = max + log(sum_s exp(score_s - max)).
+ * This is what the absorbed path holds before the W_UV projection.  It lets
+ * the decode step be checked on a query given directly, e.g. one whose
+ * scores are far larger than a unit-scale absorption produces.
+ * q_cat bf16 bits [B,Lq,H,d_g+d_R]; outputs double o_lat [B,Lq,H,d_g] and
+ * lse [B,Lq,H] (only selected entries written; either may be NULL).
+ * Returns 0, or -1 on a bad argument (length, table entry out of range).
+ */
+int mla_oracle_decode_latent(int B, int Lq, int H, int d_c, int d_R, int G, int P,
+                             int max_pages, int num_pages, double scale, int causal,
+                             const uint16_t* q_cat, const uint16_t* cache,
+                             const int32_t* block_table, const int32_t* seq_lens,
+                             const int32_t* sel, int n_sel, double* o_lat, double* lse,
+                             int nthreads) {
+  const int d_g = d_c / G;
+  const int row_w = d_c + d_R;
+  const int d_q = d_g + d_R;
+  if (G < 1 || d_c % G != 0 || H % G != 0) return -1;
+  for (int b = 0; b < B; ++b) {
+    int n = seq_lens[b];
+    if (n < Lq || n < 1 || n > max_pages * P) return -1;
+    for (int i = 0; i < (n + P - 1) / P; ++i) {
+      int pg = block_table[(size_t)b * max_pages + i];
+      if (pg < 0 || pg >= num_pages) return -1;
+    }
+  }
+  const int total = sel ? n_sel : B * H;
+  int err = 0;
+#ifdef _OPENMP
+  if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+#endif
+  for (int it = 0; it < total; ++it) {
+    const int b = sel ? sel[2 * it] : it / H;
+    const int h = sel ? sel[2 * it + 1] : it % H;
+    const int lat0 = ((h * G) / H) * d_g;
+    const int n = seq_lens[b];
+    double* score = (double*)malloc(sizeof(double) * (size_t)n);
+    double* q = (double*)malloc(sizeof(double) * (size_t)d_q);
+    double* acc = (double*)malloc(sizeof(double) * (size_t)d_g);
+    if (!score || !q || !acc) {
+      err = 1;
+    } else {
+      for (int l = 0; l < Lq; ++l) {
+        const size_t qi = ((size_t)b * Lq + l) * H + h;
+        for (int j = 0; j < d_q; ++j) q[j] = bf16_to_double(q_cat[qi * d_q + j]);
+        const int last = causal ? n - Lq + l : n - 1;
+        double mx = -INFINITY;
+        for (int s = 0; s <= last; ++s) {
+          const uint16_t* row = cache_row(cache, block_table, max_pages, P, row_w, b, s);
+          double sc = 0.0;
+          for (int c = 0; c < d_g; ++c) sc += q[c] * bf16_to_double(row[lat0 + c]);
+          for (int j = 0; j < d_R; ++j) sc += q[d_g + j] * bf16_to_double(row[d_c + j]);
+          sc *= scale;
+          score[s] = sc;
+          if (sc > mx) mx = sc;
+        }
+        double z = 0.0;
+        for (int s = 0; s <= last; ++s) z += exp(score[s] - mx);
+        for (int c = 0; c < d_g; ++c) acc[c] = 0.0;
+        for (int s = 0; s <= last; ++s) {
+          const double p = exp(score[s] - mx) / z;
+          const uint16_t* row = cache_row(cache, block_table, max_pages, P, row_w, b, s);
+          for (int c = 0; c < d_g; ++c) acc[c] += p * bf16_to_double(row[lat0 + c]);
+        }
+        if (o_lat)
+          for (int c = 0; c < d_g; ++c) o_lat[qi * d_g + c] = acc[c];
+        if (lse) lse[qi] = mx + log(z);
+      }
+    }
+    free(score); free(q); free(acc);
+  }
+  return err ? -1 : 0;
+}
+
+/*
  * Absorbed content query (§4 "path B"): q_abs[r,h,:] = q_nope[r,h,:] . W_UK[h]
  * for rows r = 0..R-1 (R = B*Lq).  Output double [R,H,d_g].
  */

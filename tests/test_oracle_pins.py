@@ -332,3 +332,143 @@ def test_oracle_matches_brute_force(B, Lq, H, G, lens):
         np.testing.assert_allclose(out[b, :, h], bo, rtol=1e-9, atol=1e-12)
         np.testing.assert_allclose(o_lat[b, :, h], bl, rtol=1e-9, atol=1e-12)
         np.testing.assert_allclose(lse[b, :, h], be, rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------- path B through the softmax
+
+def test_naive_scores_logsumexp_equals_decode_lse():
+    """The §4 script's path-A scores, computed by the self-check function,
+    are the scores the (separately pinned) decode normalises: their
+    log-sum-exp is the decode's lse on the same row (Lq = 1, all keys
+    visible).  Ties the scale, the RoPE term and the k_R offset of the
+    self-check to the decode's."""
+    for G in (1, 2):
+        c = make_case(B=2, Lq=1, H=16, G=G, seq_lens=[37, 200], table="perm", seed=17 + G)
+        _, _, lse = oracle.decode(c.dims, **c.tensors())
+        for b, h in [(0, 0), (1, 5), (1, 15), (0, 9)]:
+            sa, sb = oracle.scores_both(c.dims, c.q_nope, c.q_rope, c.W_UK, c.cache,
+                                        c.block_table, c.seq_lens, b, 0, h)
+            m = sa.max()
+            assert m + math.log(np.exp(sa - m).sum()) == pytest.approx(lse[b, 0, h], abs=1e-11)
+            m = sb.max()
+            assert m + math.log(np.exp(sb - m).sum()) == pytest.approx(lse[b, 0, h], abs=1e-11)
+
+
+def _exact_absorption(c, shift_of):
+    """W_UK[h] = a shifted identity (W_UK[h, d, d + shift(h)] = 1), so the
+    absorbed query q_nope . W_UK[h] is q_nope itself placed at columns
+    shift(h)..shift(h)+127: exactly representable in bf16.  Returns q_cat."""
+    d = c.dims
+    d_g = d["d_c"] // d["G"]
+    c.W_UK.zero_()
+    B, Lq, H = d["B"], d["Lq"], d["H"]
+    q_cat = torch.zeros(B, Lq, H, d_g + d["d_R"], dtype=torch.bfloat16)
+    for h in range(H):
+        sft = shift_of(h)
+        for i in range(d["d_hc"]):
+            c.W_UK[h, i, i + sft] = 1.0
+        q_cat[:, :, h, sft:sft + d["d_hc"]] = c.q_nope[:, :, h]
+    q_cat[..., d_g:] = c.q_rope
+    return q_cat
+
+
+@pytest.mark.parametrize("Lq,G,lens", [(1, 1, [37, 200]), (2, 1, [2, 130]), (1, 2, [65, 9])])
+def test_latent_decode_equals_decode_under_exact_absorption(Lq, G, lens):
+    """§4: absorbing W_UK into the query leaves the scores unchanged, so when
+    the absorbed query is exact the latent-space decode from q_cat equals
+    the pinned non-absorbed decode: same o_lat and lse."""
+    c = make_case(B=2, Lq=Lq, H=16, G=G, seq_lens=lens, table="perm", seed=23 + Lq + G)
+    d_g = 512 // G
+    q_cat = _exact_absorption(c, lambda h: (5 * h) % (d_g - 128))
+    _, lat_a, lse_a = oracle.decode(c.dims, **c.tensors())
+    lat_b, lse_b = oracle.decode_latent(c.dims, q_cat, c.cache, c.block_table, c.seq_lens)
+    np.testing.assert_allclose(lat_b, lat_a, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(lse_b, lse_a, rtol=1e-12, atol=1e-12)
+
+
+def test_latent_decode_closed_forms():
+    """One visible key: o_lat = c_0 and lse = its score (q_cat . row * scale).
+    Zero query: o_lat = mean of exactly n rows, lse = log n."""
+    c = make_case(B=3, Lq=1, H=16, seq_lens=[1, 1, 1], table="perm", seed=29)
+    q_cat = (torch.randn(3, 1, 16, 576, generator=torch.Generator().manual_seed(3)) * 4).to(torch.bfloat16)
+    lat, lse = oracle.decode_latent(c.dims, q_cat, c.cache, c.block_table, c.seq_lens)
+    for b in range(3):
+        row = bf(c.cache[int(c.block_table[b, 0]), 0])
+        for h in (0, 15):
+            np.testing.assert_allclose(lat[b, 0, h], row[:D_C], rtol=0, atol=1e-12)
+            assert lse[b, 0, h] == pytest.approx(float(bf(q_cat[b, 0, h]) @ row) * c.dims["scale"], rel=1e-12)
+    lens = [70, 3]
+    c = make_case(B=2, Lq=1, H=16, seq_lens=lens, table="perm", seed=31)
+    lat, lse = oracle.decode_latent(c.dims, torch.zeros(2, 1, 16, 576, dtype=torch.bfloat16), c.cache,
+                                    c.block_table, c.seq_lens)
+    for b, n in enumerate(lens):
+        rows = np.stack([bf(c.cache[int(c.block_table[b, s // PAGE]), s % PAGE, :D_C]) for s in range(n)])
+        np.testing.assert_allclose(lat[b, 0, 4], rows.mean(axis=0), atol=1e-12)
+        assert lse[b, 0, 4] == pytest.approx(math.log(n), abs=1e-12)
+
+
+def _brute_force_latent(c, q_cat, b, h):
+    """The absorbed path written out key by key: the key's row looked up by
+    hand, score = q_cat . [latent slice of the head's group | k_R] * scale,
+    the causal window, softmax, latent output, natural-log lse."""
+    d = c.dims
+    Lq, H, G, P = d["Lq"], d["H"], d["G"], d["page_size"]
+    d_g = d["d_c"] // G
+    lat = slice(((h * G) // H) * d_g, ((h * G) // H + 1) * d_g)
+    n = int(c.seq_lens[b])
+    cache, bt, q = bf(c.cache), c.block_table.numpy(), bf(q_cat)
+    lats, lses = [], []
+    for l in range(Lq):
+        scores, rows = [], []
+        for s in range(n - Lq + l + 1):
+            row = cache[int(bt[b, s // P]), s % P]
+            scores.append((np.dot(q[b, l, h, :d_g], row[lat]) + np.dot(q[b, l, h, d_g:], row[d["d_c"]:])) * d["scale"])
+            rows.append(row[lat])
+        m = max(scores)
+        e = [math.exp(x - m) for x in scores]
+        lats.append(sum(w / sum(e) * r for w, r in zip(e, rows)))
+        lses.append(m + math.log(sum(e)))
+    return np.array(lats), np.array(lses)
+
+
+@pytest.mark.parametrize("B,Lq,H,G,lens,mag", [(2, 1, 16, 1, [1, 70], 1.0), (2, 2, 16, 1, [2, 67], 32.0),
+                                               (1, 1, 32, 2, [130], 16.0)])
+def test_latent_decode_matches_brute_force(B, Lq, H, G, lens, mag):
+    """Tiny inputs over one to three shuffled pages, including queries whose
+    scores reach the hundreds: the latent decode equals the key-by-key
+    definition to fp64 rounding."""
+    c = make_case(B=B, Lq=Lq, H=H, G=G, seq_lens=lens, table="perm", seed=80 + B + Lq + G)
+    d_g = 512 // G
+    q_cat = (torch.randn(B, Lq, H, d_g + 64, generator=torch.Generator().manual_seed(9)) * mag).to(torch.bfloat16)
+    heads = [0, H // 2 - 1, H // 2, H - 1]
+    sel = [(b, h) for b in range(B) for h in heads]
+    lat, lse = oracle.decode_latent(c.dims, q_cat, c.cache, c.block_table, c.seq_lens, sel=sel)
+    for b, h in sel:
+        bl, be = _brute_force_latent(c, q_cat, b, h)
+        np.testing.assert_allclose(lat[b, :, h], bl, rtol=1e-9, atol=1e-12)
+        np.testing.assert_allclose(lse[b, :, h], be, rtol=1e-12, atol=1e-12)
+
+
+def test_bf16_absorbed_query_limits_accuracy_at_large_logits():
+    """What the bf16 absorbed query (the step's own intermediate) costs, by
+    the oracle alone: rounding q_abs = q_nope . W_UK to bf16 and decoding in
+    the latent space stays far inside max|err| <= 2e-2 max|ref|, cos >=
+    0.9999 at unit-scale logits, but with queries scaled x32 (scores in the
+    hundreds) the rounding alone moves o_lat beyond both bounds.  So the
+    end-to-end GPU check at large logits uses x8, and larger scores are
+    checked on the decode step from a given bf16 q_cat."""
+    def cos_after_rounding(mag):
+        c = make_case(B=2, Lq=1, H=128, seq_lens=[4096, 4096], table="contig", seed=33)
+        c.q_nope.copy_((c.q_nope.double() * mag).to(torch.bfloat16))
+        c.q_rope.copy_((c.q_rope.double() * mag).to(torch.bfloat16))
+        sel = [(b, h) for b in range(2) for h in range(0, 128, 9)]
+        _, lat_ref, _ = oracle.decode(c.dims, **c.tensors(), sel=sel)
+        q_cat = torch.cat([torch.from_numpy(oracle.absorb(c.q_nope, c.W_UK)).to(torch.bfloat16), c.q_rope], -1)
+        lat, _ = oracle.decode_latent(c.dims, q_cat, c.cache, c.block_table, c.seq_lens, sel=sel)
+        g = np.concatenate([lat[b, 0, h] for b, h in sel])
+        r = np.concatenate([lat_ref[b, 0, h] for b, h in sel])
+        return float(g @ r / np.linalg.norm(g) / np.linalg.norm(r)), np.abs(g - r).max() / np.abs(r).max()
+    cos1, err1 = cos_after_rounding(1.0)
+    assert cos1 > 0.99999 and err1 < 5e-3
+    cos32, err32 = cos_after_rounding(32.0)
+    assert cos32 < 0.9999 and err32 > 2e-2
