@@ -13,10 +13,12 @@ Default workload: DeepSeek-V3 dims, B=16, Lq=1, H=128, all seq_lens 4096,
 129 MB L2, so the timed loop rotates through 4 copies of the cache (302 MB),
 which keeps every step's cache reads coming from HBM.
 
-Prints ONE JSON line (rank 0).  `value` is latent-KV GB/s of the whole step
-(algorithmic bytes / step time); TFLOP/s, tokens/s and the roofline fraction
-ride along.  `--impl reference` times the fp64 CPU oracle on a bounded sample
-of the same workload instead.
+Prints ONE JSON line (rank 0).  `value` is latent-KV GB/s of the whole step:
+the latent cache bytes one step reads (every cached row once, 1152 B per
+token) over the step time.  The step's other algorithmic bytes (weights,
+queries, outputs), TFLOP/s, tokens/s and the decode kernel's roofline ride
+along.  `--impl reference` times the fp64 CPU oracle on a bounded sample of
+the same workload instead.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 For N > 1 launch with torchrun; each rank runs its own batch (weak scaling, no
@@ -180,7 +182,7 @@ def run_reference(args, world, rank):
     d = case.dims
     seq = case.seq_lens.tolist()
     B, H = d["B"], d["H"]
-    step_bytes = acc.step_bytes(seq, d["Lq"], H, d["G"])
+    kv_bytes = acc.latent_kv_bytes(seq)
     step_flops = acc.step_flops(seq, d["Lq"], H, d["G"])
     nt = oracle.num_threads()
     rng = np.random.default_rng(0)
@@ -200,7 +202,7 @@ def run_reference(args, world, rank):
             times.append(dt)
             work += frac
     total = sum(times)
-    value = step_bytes * work / total / 1e9
+    value = kv_bytes * work / total / 1e9
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
@@ -228,7 +230,7 @@ def cpu_baseline(case, budget_s=12.0):
     nt = oracle.num_threads()
     B, H = d["B"], d["H"]
     rng = np.random.default_rng(1)
-    step_bytes = acc.step_bytes(seq, d["Lq"], H, d["G"])
+    kv_bytes = acc.latent_kv_bytes(seq)
     n_pairs = nt
     sel = list(zip(rng.integers(0, B, n_pairs).tolist(), rng.integers(0, H, n_pairs).tolist()))
     t0 = time.perf_counter()
@@ -243,7 +245,7 @@ def cpu_baseline(case, budget_s=12.0):
         total_t += time.perf_counter() - t0
         frac += sum(seq[b] for b, _ in sel2) / (sum(seq) * H)
         n_pairs += len(sel2)
-    return {"value": step_bytes * frac / total_t / 1e9, "unit": "GB/s", "cores": nt, "kind": "oracle",
+    return {"value": kv_bytes * frac / total_t / 1e9, "unit": "GB/s", "cores": nt, "kind": "oracle",
             "sample": "%d random (sequence, head) pairs of the same workload, %.1f s; scaled by the "
                       "fraction of the step's work they cover" % (n_pairs, total_t)}
 
@@ -288,6 +290,7 @@ def main():
     bufs = mla.DecodeBuffers(d, dev)
     stream = torch.cuda.current_stream(dev)
 
+    kv_bytes = acc.latent_kv_bytes(seq)
     step_bytes = acc.step_bytes(seq, Lq, H, G)
     step_flops = acc.step_flops(seq, Lq, H, G)
     dec_bytes = acc.decode_bytes(seq, Lq, H, G)
@@ -318,31 +321,47 @@ def main():
         raise SystemExit("device status after warm-up: %s" % mla.mla_status_string(status))
 
     # The timed loops replay CUDA graphs of the same calls (no host launch
-    # overhead): one graph per step (per cache copy), and, for the decode
-    # kernel's own duration, graphs holding only mla_decode_paged with events
-    # around each replay.
+    # overhead): one graph per step (per cache copy).  The decode kernel's
+    # own duration: a graph of DEC_CHAIN decode launches back to back over
+    # the rotating cache copies, events around each replay, divided by the
+    # launches (each launch waits for the one before it to complete before
+    # touching memory; only its on-chip set-up overlaps the tail of the one
+    # before, as between the kernels of a step); and, for reference, events
+    # around replays of a graph holding a single decode launch (which adds
+    # the graph's launch latency).
+    DEC_CHAIN = 8
     side = torch.cuda.Stream(dev)
     side.wait_stream(stream)
     with torch.cuda.stream(side):
         g_step = [torch.cuda.CUDAGraph() for _ in range(copies)]
-        g_dec = [torch.cuda.CUDAGraph() for _ in range(copies)]
+        g_one = [torch.cuda.CUDAGraph() for _ in range(copies)]
+        g_chain = torch.cuda.CUDAGraph()
         for c in range(copies):
             with torch.cuda.graph(g_step[c], stream=side):
                 pre()
                 dec(c)
                 post()
-            with torch.cuda.graph(g_dec[c], stream=side):
+            with torch.cuda.graph(g_one[c], stream=side):
                 dec(c)
+        with torch.cuda.graph(g_chain, stream=side):
+            for j in range(DEC_CHAIN):
+                dec(j % copies)
     stream.wait_stream(side)
     torch.cuda.synchronize(dev)
 
     for i in range(max(3, args.warmup)):
         g_step[i % copies].replay()
-        g_dec[i % copies].replay()
+        g_one[i % copies].replay()
+        g_chain.replay()
     torch.cuda.synchronize(dev)
 
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    def event_pair():
+        return torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    ev_one = [event_pair() for _ in range(args.steps)]
+    ev_chain = [event_pair() for _ in range(args.steps)]
+    t_start, t_end = event_pair()
+    s_start, s_end = event_pair()
     sampler = ClockSampler(local)
     if pg:
         pg.barrier()
@@ -354,15 +373,30 @@ def main():
         g_step[i % copies].replay()
     t_end.record(stream)
     for i in range(args.steps):
-        evs[i][0].record(stream)
-        g_dec[(i + args.steps) % copies].replay()  # continue the rotation of cache copies
-        evs[i][1].record(stream)
+        ev_chain[i][0].record(stream)
+        g_chain.replay()
+        ev_chain[i][1].record(stream)
+    for i in range(args.steps):
+        ev_one[i][0].record(stream)
+        g_one[(i + args.steps) % copies].replay()  # continue the rotation of cache copies
+        ev_one[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    # a sustained run of about a second of steps, so that the clock record
+    # spans many samples under load
+    step_ms_est = t_start.elapsed_time(t_end) / args.steps
+    n_sus = max(args.steps, int(1000.0 / max(step_ms_est, 1e-3)))
+    s_start.record(stream)
+    for i in range(n_sus):
+        g_step[i % copies].replay()
+    s_end.record(stream)
     torch.cuda.synchronize(dev)
     clocks = sampler.stop()
     if pg:
         pg.barrier()
     total_ms = t_start.elapsed_time(t_end)
-    dec_ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
+    dec_ms = sum(a.elapsed_time(b) for a, b in ev_chain) / (args.steps * DEC_CHAIN)
+    dec_ms_one = sum(a.elapsed_time(b) for a, b in ev_one) / args.steps
+    sus_ms = s_start.elapsed_time(s_end) / n_sus
     total_ms = max_over_ranks(total_ms, pg, dev)
     ms = total_ms / args.steps
     status = mla.mla_get_device_status(bufs.workspace, stream)
@@ -400,7 +434,7 @@ def main():
         return
     line = {
         "metric": METRIC,
-        "value": job_rate(world, step_bytes, ms) / 1e9,
+        "value": job_rate(world, kv_bytes, ms) / 1e9,
         "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
@@ -409,19 +443,28 @@ def main():
                    "seq_len_mean": sum(seq) / len(seq), "page_size": 64,
                    "parallelism": "replicas" if world > 1 else "single",
                    "l2": "inputs larger than L2: %d rotating cache copies (%.0f MB)" % (copies, copies * cache_bytes / 1e6)},
+        "value_counts": "latent KV cache bytes read per step (%d B) over the step time" % kv_bytes,
+        "step_gbs": job_rate(world, step_bytes, ms) / 1e9,
+        "step_bytes": step_bytes,
         "tflops": job_rate(world, step_flops, ms) / 1e12,
         "tokens_per_s": job_rate(world, B * Lq, ms),
         "roofline_frac_step": max(step_bytes / (ms * 1e-3) / 1e9 / hbm,
                                   step_flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"]),
         "decode_kernel": {"ms": dec_ms, "gbs": achieved, "tflops": tflops_dec,
                           "tensor_frac": tflops_dec / peaks["bf16_tflops"],
-                          "bytes": dec_bytes, "flops": dec_flops},
+                          "bytes": dec_bytes, "flops": dec_flops,
+                          "ms_single_launch_graph": dec_ms_one,
+                          "timing": "mean per launch over %d-launch graphs (events around each replay); "
+                                    "ms_single_launch_graph: events around one-launch graphs" % DEC_CHAIN},
         "roofline": roofline_entry(dec_bytes, dec_flops, dec_ms, peaks, decode_traffic(args.workload), peak_src),
-        "e2e": {"value": job_rate(world, step_bytes, e2e_ms) / 1e9, "unit": "GB/s",
+        "e2e": {"value": job_rate(world, kv_bytes, e2e_ms) / 1e9, "unit": "GB/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": (mla.launches_per_step(case.dims) + mla.mla_decode_kernel_launches(case.dims)) * args.steps,
+        "gpu_launches": mla.launches_per_step(case.dims) * args.steps,
         "timing": "one CUDA-graph replay per step (absorb, decode and projection chained by programmatic dependent launch; combine launched after the decode); "
-                  "decode timed alone by events around replays of a decode-only graph",
+                  "gpu_launches counts the kernels of the timed steps",
+        "sustained": {"steps": n_sus, "ms_per_step": sus_ms, "seconds": sus_ms * n_sus / 1e3,
+                      "note": "step graphs replayed back to back for about a second after the timed "
+                              "region, inside the clock record"},
         "clocks": clocks,
         "device_status": mla.mla_status_string(status),
     }

@@ -186,6 +186,24 @@ int mla_project_uv(const mla_dims* dims, const void* o_lat, const void* W_UV,
                    void* out, void* stream);
 
 /*
+ * Testing hook for the decode kernel's timeout path (no counterpart in the
+ * source pages), process-wide, for the mla_decode_paged launches that
+ * follow:
+ *   wait_limit_ns  wall-clock limit of every wait between the kernel's warps
+ *                  (0 restores the default, 2 s);
+ *   stall_page     >= 0: before the QK of that page of its work unit, each
+ *                  CTA's MMA-issuing thread also waits on a barrier that
+ *                  nothing completes, so that wait gives up after the limit
+ *                  (-1 restores the default: no such wait).
+ * A wait that gives up records MLA_ERR_TIMEOUT in the workspace status word;
+ * the kernel then waits for the copies and MMAs it started and returns.
+ * Nothing is skipped and no memory is touched out of bounds, so the context
+ * stays usable.  Errors: MLA_ERR_INVALID_ARG (wait_limit_ns < 0 or
+ * stall_page < -1).
+ */
+int mla_set_timeout_test(long long wait_limit_ns, int stall_page);
+
+/*
  * Synchronise `stream`, then return the sticky device status of `workspace`
  * (MLA_OK or the first device error recorded since the workspace was zeroed).
  */

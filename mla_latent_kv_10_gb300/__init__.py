@@ -15,7 +15,7 @@ __all__ = [
     "MLAError", "Dims", "load_library", "library_path",
     "mla_absorb_q", "mla_decode_paged", "mla_combine_splits", "mla_project_uv",
     "mla_decode_workspace_size", "mla_decode_num_slots", "mla_decode_kernel_launches",
-    "launches_per_step", "mla_get_device_status",
+    "launches_per_step", "mla_get_device_status", "mla_set_timeout_test",
     "mla_status_string", "make_dims", "DecodeBuffers", "decode_step",
 ]
 
@@ -62,6 +62,7 @@ def load_library():
         "mla_combine_splits": [DP, P, P, P, S, P, P, P],
         "mla_project_uv": [DP, P, P, P, P],
         "mla_get_device_status": [P, P],
+        "mla_set_timeout_test": [ctypes.c_longlong, I],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -158,6 +159,12 @@ def mla_combine_splits(dims, o_part, lse_part, workspace, o_lat, lse=None, strea
 def mla_project_uv(dims, o_lat, W_UV, out, stream=None):
     _check(load_library().mla_project_uv(_dims(dims), _ptr(o_lat), _ptr(W_UV), _ptr(out), _stream(stream)),
            "mla_project_uv")
+
+
+def mla_set_timeout_test(wait_limit_ns: int, stall_page: int):
+    """Testing hook of the decode kernel's timeout path (process-wide; 0, -1
+    restores the defaults)."""
+    _check(load_library().mla_set_timeout_test(int(wait_limit_ns), int(stall_page)), "mla_set_timeout_test")
 
 
 def mla_get_device_status(workspace, stream=None) -> int:

@@ -38,6 +38,12 @@ def compression_ratio(d_c: int = 512, d_R: int = 64, heads: int = 128, head_dim:
     return 1.0 - bytes_per_token(d_c, d_R) / mha_bytes_per_token(heads, head_dim)
 
 
+def latent_kv_bytes(seq_lens, d_c: int = 512, d_R: int = 64) -> int:
+    """Latent KV cache bytes one decode step of one layer reads: every cached
+    row of every sequence once (the new tokens' rows included)."""
+    return sum(int(n) for n in seq_lens) * bytes_per_token(d_c, d_R)
+
+
 def decode_bytes(seq_lens, Lq: int, H: int, G: int = 1, d_c: int = 512, d_R: int = 64) -> int:
     """Algorithmic HBM bytes of mla_decode_paged + mla_combine_splits: every
     visible cache row once, q_cat in, o_lat (bf16) and lse (fp32) out."""

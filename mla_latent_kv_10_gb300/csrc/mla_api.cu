@@ -3,6 +3,7 @@
 // beyond per-device launch-configuration caches.
 #include <cmath>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include <cudaTypedefs.h>
@@ -59,13 +60,30 @@ int check_dims(const mla_dims* d) {
   return MLA_OK;
 }
 
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;  // 2 s
+std::atomic<unsigned long long> g_wait_ns{kDefaultWaitNs};
+std::atomic<int> g_stall_page{-1};
+
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA; }
 
 int row_blocks(const mla_dims* d) { return (d->Lq * d->H + kRowsPerCta - 1) / kRowsPerCta; }
 
 }  // namespace
 
+namespace mla {
+unsigned long long decode_wait_limit_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
+int decode_stall_page() { return g_stall_page.load(std::memory_order_relaxed); }
+}  // namespace mla
+
 extern "C" {
+
+int mla_set_timeout_test(long long wait_limit_ns, int stall_page) {
+  if (wait_limit_ns < 0 || stall_page < -1) return MLA_ERR_INVALID_ARG;
+  g_wait_ns.store(wait_limit_ns == 0 ? kDefaultWaitNs : (unsigned long long)wait_limit_ns,
+                  std::memory_order_relaxed);
+  g_stall_page.store(stall_page, std::memory_order_relaxed);
+  return MLA_OK;
+}
 
 const char* mla_status_string(int s) {
   switch (s) {
@@ -218,6 +236,8 @@ int mla_decode_paged(const mla_dims* d, const void* q_cat, const void* kv_cache,
   a.plan_in_kernel = in_kernel ? 1 : 0;
   a.units = units;
   a.seq_lens = seq_lens;
+  a.wait_ns = decode_wait_limit_ns();
+  a.stall_page = decode_stall_page();
   return cuda_status(launch_decode(tm, tm_rope, tm_qrope, tm_qlat, a, units, csize, st));
 }
 

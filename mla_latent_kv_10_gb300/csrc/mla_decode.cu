@@ -14,42 +14,50 @@
 //     tensor-memory columns of an SM, so each 128-row block runs on a CTA
 //     PAIR (cluster rank bit 0 = r): CTA r owns latent half r (256 columns of
 //     O) and loads only its half of each page plus half of the 64 RoPE
-//     columns.  Each CTA computes a partial score tile over its columns, in
-//     log2 units, rounds it to fp16 and sends it to the peer with one bulk
-//     shared-to-shared copy (16 KiB per page); both CTAs add the same two
-//     fp16 partials, so they hold bit-identical scores and run the same
-//     online softmax.  The exchange is double-buffered and the softmax warps
-//     run one page behind the exchange, so the copy of page q overlaps the
+//     columns.  Each CTA computes a partial score tile over its columns
+//     (fp32 in tensor memory), converts it to 16-bit fixed point with a
+//     power-of-two scale per query row and sends it to the peer with one
+//     bulk shared-to-shared copy per TMEM lane quadrant (16 KiB + 512 B of
+//     scales per page).  Each CTA adds its own fp32 partial to the peer's
+//     dequantised one; the two CTAs' scores differ by at most 2^-14 of the
+//     row's largest partial, and each CTA normalises its half of O by its
+//     own row sums, so each half is an exact softmax average of slightly
+//     different weights.  The exchange is double-buffered and the softmax
+//     warps run one page behind it, so the copy of page q overlaps the
 //     softmax of page q-1.
 //   * Tensor memory per CTA (all 512 columns): O (256) | Q latent half (128,
-//     bf16 pairs, the MMA A operand) | S (64) | two P buffers (32 each, bf16
-//     pairs, A operand of the P.V MMA).  The RoPE half of Q is a 64-byte
-//     swizzled tile in shared memory (A operand of the last two K steps).
-//     The page tile in shared memory is used twice: K-major as B for
-//     S = Q.K^T and MN-major as B for O += P.V.  With two P buffers the
-//     softmax of page q+1 never waits for P.V of page q.
+//     bf16 pairs, the MMA A operand) | two score tiles S (64 each).  The
+//     RoPE half of Q is a 64-byte swizzled tile in shared memory (A operand
+//     of the last two K steps).  The page tile in shared memory is used
+//     twice: K-major as B for S = Q.K^T and MN-major as B for O += P.V.
+//   * P (bf16) is written by the softmax warps into the receive slot whose
+//     peer partial they have just read, row for row, as the K-major
+//     128-byte-swizzled A operand of P.V.
 //   * The first segment's query arrives by TMA ahead of the first page: its
 //     latent half into the four (still idle) exchange slots, whence the
 //     softmax warps move it into tensor memory, and its RoPE half into its
 //     shared-memory tile.  Later segments' queries are loaded by the softmax
-//     warps with plain loads.  The exchange slots are handed to the peer
-//     (tensor-memory commit multicast on its "can send" barriers) only once
-//     the query has left them.
+//     warps with plain loads (RoPE tile by TMA).  The exchange slots are
+//     handed to the peer (a relaxed remote arrive on its "can send"
+//     barriers) only once the query has left them.
 //   * Pages arrive by TMA (four 64 x 64 latent boxes with 128-byte swizzle,
 //     one 32 x 64 RoPE box with 64-byte swizzle) into a 4-stage mbarrier
-//     ring; one thread issues MMAs, one thread issues copies, four exchange
-//     warps move partial scores, eight softmax warps (two per TMEM lane
-//     quadrant, one query row and half the page's keys per thread) do the
-//     masking, online softmax and epilogue.  Rescaling of O after a new row
-//     maximum is deferred until the maximum has grown by 2^8 (log2 units),
-//     so it is rare.
+//     ring; one thread issues QK MMAs, one issues P.V MMAs, one issues
+//     copies, four exchange warps move partial scores, eight softmax warps
+//     (two per TMEM lane quadrant, one query row and half the page's keys
+//     per thread) do the masking, online softmax and epilogue.  Rescaling of
+//     O after a new row maximum is deferred until the maximum has grown by
+//     2^8 (log2 units), so it is rare.
 //   * Split-KV: the pages of all sequences, in order, are cut into equal
 //     contiguous ranges, one per cluster; a range that covers parts of several
 //     sequences yields one partial (o, lse) per sequence, stored in slot
 //     b + unit.  The combine kernel (mla_combine.cu) merges them.
-//   * Every wait is bounded (wall clock); on expiry the kernel records
-//     MLA_ERR_TIMEOUT in the workspace status word, stops, waits for its own
-//     copies and MMAs, frees tensor memory and returns.
+//   * Every wait is bounded (wall clock).  A wait that gives up records
+//     MLA_ERR_TIMEOUT in the workspace status word and raises the abort flag
+//     of both CTAs of the pair; every role then leaves its loop, and the
+//     teardown waits (ignoring the flag) for every copy and MMA this CTA
+//     started and every exchange copy the peer sent it, frees tensor memory
+//     and returns.
 #include <climits>
 #include <cmath>
 #include <mutex>
@@ -60,12 +68,16 @@
 namespace mla {
 
 namespace {
-
 constexpr int kStages = 4;
 constexpr int kBoxBytes = kPage * 64 * 2;       // 64 tokens x 64 bf16 = 8 KiB, 128-byte swizzle
 constexpr int kRopeBoxBytes = kPage * 32 * 2;   // 64 tokens x 32 bf16 = 4 KiB, 64-byte swizzle
 constexpr int kStageBytes = 4 * kBoxBytes + kRopeBoxBytes;  // latent half + this CTA's RoPE half
-constexpr int kXSlot = kRowsPerCta * 64 * 2;    // a 128 x 64 tile of 16-bit values, 16 KiB
+constexpr int kXRowBytes = kPage * 2;           // one query row's 64 partial scores, int16
+constexpr int kXQuadBytes = 32 * kXRowBytes;    // the 32 rows of one TMEM lane quadrant, 4 KiB
+constexpr int kXSlot = 4 * kXQuadBytes;         // exchange slot: 128 rows x 64 int16 = 16 KiB
+constexpr int kXScaleBytes = 32 * 4;            // a quadrant's 32 row scales (fp32), 128 B
+constexpr int kXQuadTx = kXQuadBytes + kXScaleBytes;  // bytes one quadrant's copy lands per page
+constexpr int kQBoxBytes = kRowsPerCta * 64 * 2;   // 128 query rows x 64 latent bf16, 16 KiB
 constexpr int kQRopeBytes = kRowsPerCta * 32 * 2;  // this CTA's 32 RoPE columns of 128 query rows
 // shared memory: stage ring | send slots (2) | receive slots (2) | RoPE
 // query tile | DecodeShared
@@ -73,7 +85,9 @@ constexpr int kXOff = kStages * kStageBytes;
 constexpr int kRecvOff = kXOff + 2 * kXSlot;
 constexpr int kQRopeOff = kXOff + 4 * kXSlot;
 constexpr int kSmemShared = kQRopeOff + kQRopeBytes;
-static_assert(kStageBytes % 1024 == 0 && kQRopeOff % 1024 == 0, "swizzled tiles need aligned bases");
+static_assert(kStageBytes % 1024 == 0 && kXSlot % 1024 == 0 && kQRopeOff % 1024 == 0,
+              "swizzled tiles need aligned bases");
+static_assert(4 * kQBoxBytes == 4 * kXSlot, "the first query's latent half fills the four exchange slots");
 // warps 0-7: softmax warps (TMEM lane quadrant w & 3, key half w >> 2: 32
 // keys of every page, 128 columns of O, 64 columns of Q); warps 8-11:
 // exchange warps (one per quadrant, a whole score row per thread); warp 12:
@@ -102,17 +116,6 @@ __device__ __forceinline__ float lg2(float x) {
   return y;
 }
 
-__device__ __forceinline__ uint32_t pack_f16x2_sat(float lo, float hi) {
-  uint32_t r;
-  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-__device__ __forceinline__ float2 unpack_f16x2(uint32_t w) {
-  float2 f;
-  asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
-      : "=f"(f.x), "=f"(f.y) : "r"(w));
-  return f;
-}
 __device__ __forceinline__ void ld_shared_v4(uint32_t addr, uint32_t& a, uint32_t& b, uint32_t& c, uint32_t& d) {
   asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(a), "=r"(b), "=r"(c), "=r"(d) : "r"(addr) : "memory");
 }
@@ -123,11 +126,60 @@ __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 // Copy `bytes` of this CTA's shared memory into another CTA of the cluster;
-// completion is counted in bytes on the destination CTA's mbarrier.
+// completion is counted in bytes on the destination CTA's mbarrier.  The
+// copies of one thread form bulk groups, so it can wait until their source
+// has been read (bulk_wait_read_all).
 __device__ __forceinline__ void bulk_s2s(uint32_t dst_cluster, uint32_t src, uint32_t bytes, uint32_t bar_cluster) {
   asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                ::"r"(dst_cluster), "r"(src), "r"(bytes), "r"(bar_cluster) : "memory");
 }
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Partial scores cross the pair as 16-bit fixed point with a power-of-two
+// scale per row: q = round(x * 2^k), k chosen so that the row's largest |x|
+// maps below 2^14.  The absolute error of every key is then at most 2^-14 of
+// the row's largest |partial|, about 8 times below that of fp16 at the same
+// size, and independent of where the key sits in the row.  The rounding
+// uses the float adder: x * 2^k + (1.5 * 2^23 + 2^15) holds q + 2^15 in its
+// low 16 mantissa bits, and a byte permute puts those bits back under the
+// same exponent on the receiving side, so both directions stay on full-rate
+// FMA and integer pipes instead of the conversion unit.
+constexpr float kRoundMagic = 12615680.0f;      // 1.5 * 2^23 + 2^15
+constexpr uint32_t kRoundMagicHigh = 0x4B400000u;  // the top 16 bits of its encoding (low bits vary)
+__device__ __forceinline__ int row_scale_exp(float maxabs) {
+  const int e = (int)((__float_as_uint(maxabs) >> 23) & 0xffu) - 127;  // floor(log2 maxabs) (normal numbers)
+  const int k = 13 - e;
+  return k < -100 ? -100 : (k > 100 ? 100 : k);  // zero or tiny rows: any scale will do
+}
+__device__ __forceinline__ float exp2_int(int k) { return __uint_as_float((uint32_t)(k + 127) << 23); }
+// two values already multiplied by 2^k -> two rounded 16-bit codes (q + 2^15)
+__device__ __forceinline__ uint32_t pack_fixed16x2(float lo, float hi) {
+  return __byte_perm(__float_as_uint(lo + kRoundMagic), __float_as_uint(hi + kRoundMagic), 0x5410);
+}
+__device__ __forceinline__ float2 unpack_fixed16x2(uint32_t w) {
+  return make_float2(__uint_as_float(__byte_perm(w, kRoundMagicHigh, 0x7610)) - kRoundMagic,
+                     __uint_as_float(__byte_perm(w, kRoundMagicHigh, 0x7632)) - kRoundMagic);
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+// largest of 32 values (three-input maxima)
+__device__ __forceinline__ float max32(const float (&x)[32]) {
+  float m[11];
+#pragma unroll
+  for (int j = 0; j < 10; ++j) m[j] = fmax3(x[3 * j], x[3 * j + 1], x[3 * j + 2]);
+  m[10] = fmaxf(x[30], x[31]);
+  const float a = fmax3(m[0], m[1], m[2]), b = fmax3(m[3], m[4], m[5]), c = fmax3(m[6], m[7], m[8]);
+  return fmaxf(fmax3(a, b, c), fmaxf(m[9], m[10]));
+}
+__device__ __forceinline__ void bulk_wait_read_1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+
 // Named barrier `id` over `n` threads with an AND vote: every thread learns
 // whether all of them are still ok (so none is left waiting alone).
 __device__ __forceinline__ bool bar_red_and_n(bool ok, uint32_t id, uint32_t n) {
@@ -142,26 +194,37 @@ __device__ __forceinline__ void set_status(WsHeader* ws, int code) {
 }
 
 // Shared state of one decode CTA (at the end of dynamic shared memory).
-// Per score buffer / exchange slot b (page parity):
+// Per score buffer / receive slot b (page parity):
 //   s_full   QK(p) wrote the own partial scores into S_b
-//   xfull    the peer's fp16 partial landed in receive slot b
+//   xfull    [b][quadrant]: the peer's 16-bit partial of that quadrant's
+//            32 rows and their scales landed (receive slot b, xscale_recv)
 //   s_free   the exchange and softmax warps read S_b (the next QK may
 //            overwrite it)
 //   p_full   P(p) is in receive slot b
 //   o_done   P.V of page p is done
-//   can_send the peer's P.V of page p is done: its receive slot b and our
-//            send slot b are free again (arrives from the peer's MMA);
-//            phase 0 instead says the peer's first query left its slots
-//   q_lat    the first segment's query (latent half in the exchange slots,
+//   can_send the peer's P.V of page p is done: its receive slot b is free
+//            again (a remote arrive from the peer's P.V thread); phase 0
+//            instead says the peer's first query left its slots
+// Per segment:
+//   q_lat    the first segment's query (latent half in the receive slots,
 //            RoPE half in its tile) landed
+//   q_full   a segment's latent query is in tensor memory
+//   q_tma    a later segment's RoPE query tile landed
+//   drain    [QK, P.V]: every MMA the issuing thread started is done
+//            (teardown after an abort)
 struct DecodeShared {
+  float xscale_send[2][kRowsPerCta];  // 2^-k of each row's 16-bit partial: ours (copied to the peer)
+  float xscale_recv[2][kRowsPerCta];  // and the peer's
   uint64_t full[kStages], empty[kStages];
-  uint64_t q_full, q_lat, drain;
-  uint64_t s_full[2], xfull[2], s_free[2], p_full[2], o_done[2], can_send[2];
+  uint64_t q_full, q_tma, q_lat, drain[2];
+  uint64_t never;                // testing: a barrier nothing completes (see DecodeArgs::stall_page)
+  uint64_t s_full[2], s_free[2], p_full[2], o_done[2], can_send[2];
+  uint64_t xfull[2][4];
   float red[2][2][kRowsPerCta];  // [parity][key half][row]: partial row maxima (row sums at a segment's end)
   UnitRec rec;                   // this CTA's work unit
   uint32_t tmem;
   int abort;
+  int peer_sent[4];              // pages the peer's exchange warp of each quadrant sent here (teardown)
 };
 
 // All shared memory is dynamic: stage ring, exchange slots, then the small state.
@@ -460,7 +523,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                   const DecodeArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* stages = smem;
-  uint8_t* xbuf = smem + kXOff;  // [send 2][receive 2] x 16 KiB
+  const uint32_t xsend = smem_u32(smem + kXOff);     // send slots 0 and 1
+  const uint32_t xrecv = smem_u32(smem + kRecvOff);  // receive slots 0 and 1
   const uint32_t qrope = smem_u32(smem + kQRopeOff);
   DecodeShared& sh = *reinterpret_cast<DecodeShared*>(smem + kSmemShared);
 
@@ -478,28 +542,34 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   const uint32_t peer = crank ^ 1u;
   const int unit = (int)cluster_id_x();
   WsHeader* ws = a.ws;
+  const uint64_t lim = a.wait_ns;        // limit of every pipeline wait
 
   auto bar = [](uint64_t& x) { return smem_u32(&x); };
 
   if (threadIdx.x == 0) {
     sh.abort = 0;
+    for (int q = 0; q < 4; ++q) sh.peer_sent[q] = 0;
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(sh.full[s]), 1);
       mbar_init(bar(sh.empty[s]), 1);
     }
     mbar_init(bar(sh.q_full), kSoftmaxThreads);
+    mbar_init(bar(sh.q_tma), 1);
     mbar_init(bar(sh.q_lat), 1);
-    mbar_init(bar(sh.drain), 1);
+    mbar_init(bar(sh.drain[0]), 1);
+    mbar_init(bar(sh.drain[1]), 1);
+    mbar_init(bar(sh.never), 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(sh.s_full[s]), 1);
-      mbar_init(bar(sh.xfull[s]), 1);  // armed with the expected bytes, completed by the peer's copy
       mbar_init(bar(sh.s_free[s]), kSoftmaxThreads + kXThreads);
       mbar_init(bar(sh.p_full[s]), kSoftmaxThreads);
       mbar_init(bar(sh.o_done[s]), 1);
       mbar_init(bar(sh.can_send[s]), 1);  // one arrival from the peer's MMA completion
+      for (int q = 0; q < 4; ++q) mbar_init(bar(sh.xfull[s][q]), 1);  // armed, completed by the peer's stores
     }
     fence_mbar_init();
-    for (int s = 0; s < 2; ++s) mbar_arrive_expect_tx(bar(sh.xfull[s]), kXSlot);
+    for (int s = 0; s < 2; ++s)
+      for (int q = 0; q < 4; ++q) mbar_arrive_expect_tx(bar(sh.xfull[s][q]), kXQuadTx);
     tma_prefetch_desc(&tm_cache);
     tma_prefetch_desc(&tm_rope);
     tma_prefetch_desc(&tm_qrope);
@@ -511,7 +581,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync();  // peer barriers initialised before any remote arrive
+  cluster_sync();  // peer barriers initialised before any remote arrive or store
   tc_fence_after();
   const uint32_t tmem = sh.tmem;
   volatile int* abort = &sh.abort;
@@ -525,19 +595,25 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   if (a.plan_in_kernel && a.B <= kPlanWarpMaxB) {
     if (warp == 0) plan_in_warp(a, unit, unit == 0 && crank == 0, &sh.rec);
   } else if (a.plan_in_kernel) {
-    plan_in_block(a, unit, unit == 0 && crank == 0, reinterpret_cast<int*>(xbuf),
-                  reinterpret_cast<int*>(xbuf) + 3 * a.B + 8, &sh.rec);
+    int* scratch = reinterpret_cast<int*>(smem + kXOff);
+    plan_in_block(a, unit, unit == 0 && crank == 0, scratch, scratch + 3 * a.B + 8, &sh.rec);
   } else if (threadIdx.x == 0) {
     sh.rec = ws_view(ws, a.B).rec[unit];
   }
   fence_proxy_async();  // the plan's scratch writes come before the query copies into the same slots
   __syncthreads();
 
+  // A wait that gives up stops both CTAs of the pair.
+  const uint32_t peer_abort = mapa(smem_u32(&sh.abort), peer);
   auto fail = [&]() {
     *abort = 1;
+    st_cluster_u32(peer_abort, 1u);
     set_status(ws, MLA_ERR_TIMEOUT);
   };
-  const uint32_t xsrc = smem_u32(xbuf), xrecv = smem_u32(smem + kRecvOff);
+  // What this thread started and the teardown must see finished.
+  uint32_t issued = 0;  // TMA producer: pages whose copies were issued
+  uint32_t nq_tma = 0;  // thread 0: RoPE query tiles loaded by TMA for later segments
+  int sent = 0;         // exchange warps: pages copied to the peer
 
   if (warp == kTmaWarp) {
     // ------------------------------------------------------------ TMA producer
@@ -547,13 +623,13 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       SegIter it;
       it.init(sh.rec);
       int sb, pa, pb;
-      uint32_t pc = 0;
       bool ok = true;
       while (ok && it.next(a, sb, pa, pb)) {
         const int32_t* bt = a.block_table + (size_t)sb * a.max_pages;
-        for (int i = pa; i < pb; ++i, ++pc) {
+        for (int i = pa; i < pb; ++i) {
+          const uint32_t pc = issued;
           const int st = pc % kStages;
-          if (pc >= (uint32_t)kStages && !(ok = mbar_wait(bar(sh.empty[st]), ((pc / kStages) - 1) & 1, abort))) {
+          if (pc >= (uint32_t)kStages && !(ok = mbar_wait(bar(sh.empty[st]), ((pc / kStages) - 1) & 1, abort, lim))) {
             fail();
             break;
           }
@@ -565,9 +641,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           if (pc == 0) {  // the first segment's query, ahead of its first page
             const int qy = sb * a.Lq * a.H + (int)rg * kRowsPerCta;
             const int qx = a.G == 1 ? (int)r * 256 : 0;
-            mbar_arrive_expect_tx(bar(sh.q_lat), 4 * kXSlot + kQRopeBytes);
-            for (int j = 0; j < 4; ++j)
-              tma_load_2d(xsrc + j * kXSlot, &tm_qlat, bar(sh.q_lat), qx + 64 * j, qy);
+            mbar_arrive_expect_tx(bar(sh.q_lat), 4 * kQBoxBytes + kQRopeBytes);
+            for (int j = 0; j < 4; ++j) tma_load_2d(xsend + j * kQBoxBytes, &tm_qlat, bar(sh.q_lat), qx + 64 * j, qy);
             tma_load_2d(qrope, &tm_qrope, bar(sh.q_lat), a.d_g + 32 * (int)r, qy);
           }
           const uint32_t dst = smem_u32(stages + st * kStageBytes);
@@ -578,20 +653,15 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           // this CTA's 32 RoPE columns
           tma_load_2d_hint(dst + 4 * kBoxBytes, &tm_rope, bar(sh.full[st]), kDc + 32 * (int)r, page * kPage,
                            policy);
+          ++issued;
           // At start-up every CTA of the grid asks for its pages at once; let
           // the first page land before queueing the rest so compute starts
           // as early as possible instead of after the whole initial burst.
-          if (pc == 0 && !(ok = mbar_wait(bar(sh.full[0]), 0, abort))) {
+          if (pc == 0 && !(ok = mbar_wait(bar(sh.full[0]), 0, abort, lim))) {
             fail();
-            ++pc;
             break;
           }
         }
-      }
-      // Copies still in flight must land before this CTA may exit.
-      if (!ok) {
-        for (uint32_t k = (pc > (uint32_t)kStages ? pc - kStages : 0); k < pc; ++k)
-          mbar_wait(bar(sh.full[k % kStages]), (k / kStages) & 1, abort, 100000000ull);
       }
     }
     __syncwarp();  // reconverge before the CTA-wide barrier of the teardown
@@ -606,25 +676,26 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16(128, 64, false, false);
       const uint64_t qr0 = sdesc_sw64(qrope, 512);
-      const uint16_t peer_mask = (uint16_t)(1u << peer);
       PageCursor c;
       c.init(sh.rec, a);
       uint32_t pc = 0, qc = 0;
       bool ok = true;
       while (ok && c.valid) {
         if (c.seg_first()) {  // the segment's query (loaded after every QK before it finished)
-          if (!(ok = mbar_wait(bar(sh.q_full), qc & 1, abort))) break;
+          if (!(ok = mbar_wait(bar(sh.q_full), qc & 1, abort, lim))) break;
+          if (qc > 0 && !(ok = mbar_wait(bar(sh.q_tma), (qc - 1) & 1, abort, lim))) break;
           if (qc == 0) {  // the first query left the exchange slots: the peer may send into them
-            mma_commit_multicast(bar(sh.can_send[0]), peer_mask);
-            mma_commit_multicast(bar(sh.can_send[1]), peer_mask);
+            mbar_arrive_remote_relaxed(mapa(bar(sh.can_send[0]), peer));
+            mbar_arrive_remote_relaxed(mapa(bar(sh.can_send[1]), peer));
           }
           ++qc;
           tc_fence_after();
         }
         const uint32_t b = pc & 1;
         const int st = pc % kStages;
-        if (!(ok = mbar_wait(bar(sh.full[st]), (pc / kStages) & 1, abort))) break;
-        if (pc >= 2 && !(ok = mbar_wait(bar(sh.s_free[b]), ((pc - 2) >> 1) & 1, abort))) break;
+        if (pc == (uint32_t)a.stall_page && !(ok = mbar_wait(bar(sh.never), 0, abort, lim))) break;
+        if (!(ok = mbar_wait(bar(sh.full[st]), (pc / kStages) & 1, abort, lim))) break;
+        if (pc >= 2 && !(ok = mbar_wait(bar(sh.s_free[b]), ((pc - 2) >> 1) & 1, abort, lim))) break;
         tc_fence_after();
         const uint32_t sbase = smem_u32(stages + st * kStageBytes);
         const uint64_t kd0 = sdesc_sw128(sbase, 16, 1024);
@@ -647,17 +718,23 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     __syncwarp();  // reconverge before the CTA-wide barrier of the teardown
   } else if (warp == kPvWarp) {
     // ------------------------------------------------------------ P.V issuer
-    // P.V of page p frees receive slot p&1 at the peer for its next send.
+    // Once P.V of page p is done, receive slot p&1 (and the peer's send
+    // slot) are free for the peer's next copy: this thread waits for the
+    // MMA locally and tells the peer with a relaxed remote arrive (the
+    // slot's reads are complete, so no release ordering is needed; a
+    // tensor-core commit straight to the peer costs a cluster-scope
+    // release, over a thousand cycles on the critical loop).
     if (lane == 0) {
       constexpr uint32_t idesc_pv = idesc_bf16(128, 256, false, true);
-      const uint16_t peer_mask = (uint16_t)(1u << peer);
+      const uint32_t peer_can_send0 = mapa(bar(sh.can_send[0]), peer);
+      const uint32_t peer_can_send1 = mapa(bar(sh.can_send[1]), peer);
       PageCursor c;
       c.init(sh.rec, a);
       bool ok = true;
       for (uint32_t p = 0; ok && c.valid; ++p) {
         const uint32_t b = p & 1;
         const bool acc = !c.seg_first();  // a segment's first P.V starts O afresh
-        if (!(ok = mbar_wait(bar(sh.p_full[b]), (p >> 1) & 1, abort))) break;
+        if (!(ok = mbar_wait(bar(sh.p_full[b]), (p >> 1) & 1, abort, lim))) break;
         tc_fence_after();
         const uint64_t pd0 = sdesc_sw128(xrecv + b * kXSlot, 16, 1024);
         const uint64_t vd0 = sdesc_sw128(smem_u32(stages + (p % kStages) * kStageBytes), kBoxBytes, 1024);
@@ -667,7 +744,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                  (acc || kk > 0) ? 1u : 0u);
         mma_commit(bar(sh.empty[p % kStages]));
         mma_commit(bar(sh.o_done[b]));
-        mma_commit_multicast(bar(sh.can_send[b]), peer_mask);
+        if (!(ok = mbar_wait(bar(sh.o_done[b]), (p >> 1) & 1, abort, lim))) break;
+        mbar_arrive_remote_relaxed(b ? peer_can_send1 : peer_can_send0);
         c.advance(a);
       }
       if (!ok) fail();
@@ -675,61 +753,75 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     __syncwarp();  // reconverge before the CTA-wide barrier of the teardown
   } else if (warp >= kSWarps && warp < kSWarps + kXWarps) {
     // ------------------------------------------------------------ exchange warps
-    // Page p: own partial scores (S_b, fp32) -> fp16 -> send slot b; each
-    // warp copies its 32 rows (4 KiB) into the peer's receive slot b as soon
-    // as they are written (the peer's barrier counts the bytes of all four).
+    // Page p: own partial scores (S_b, fp32) -> 16-bit fixed point with a
+    // per-row scale -> send slot b (one row per thread, 128-byte swizzled
+    // rows) -> one bulk copy per warp of its 32 rows (4 KiB) and their
+    // scales (128 B) into the peer's receive slot b, counted on the peer's
+    // barrier of this quadrant.
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
     const uint32_t peer_recv = mapa(xrecv, peer);
-    const uint32_t peer_xfull0 = mapa(bar(sh.xfull[0]), peer), peer_xfull1 = mapa(bar(sh.xfull[1]), peer);
+    const uint32_t peer_scale = mapa(smem_u32(&sh.xscale_recv[0][0]), peer);
+    const uint32_t peer_xfull0 = mapa(bar(sh.xfull[0][quad]), peer);
+    const uint32_t peer_xfull1 = mapa(bar(sh.xfull[1][quad]), peer);
     const int npages = sh.rec.end - sh.rec.start;
     bool ok = true;
-    for (int p = 0; p < npages; ++p) {
+    for (int p = 0; ok && p < npages; ++p) {
       const uint32_t b = p & 1;
-      if (ok) ok = mbar_wait(bar(sh.s_full[b]), (p >> 1) & 1, abort);
+      ok = mbar_wait(bar(sh.s_full[b]), (p >> 1) & 1, abort, lim);
       ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t v[64];
+      tmem_ld32(lane_base + kColS + 64 * b, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+      tmem_ld32(lane_base + kColS + 64 * b + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(bar(sh.s_free[b]));
+      float mx = 0.f;
+#pragma unroll
+      for (int k = 0; k < 64; k += 2) mx = fmax3(mx, fabsf(__uint_as_float(v[k])), fabsf(__uint_as_float(v[k + 1])));
+      const int ke = row_scale_exp(mx);
+      const float up = exp2_int(ke);
       uint32_t w[32];
-      if (ok) {
-        tc_fence_after();
 #pragma unroll
-        for (int hlf = 0; hlf < 2; ++hlf) {
-          uint32_t v[32];
-          tmem_ld32(lane_base + kColS + 64 * b + 32 * hlf, v);
-          tmem_wait_ld();
+      for (int k = 0; k < 32; ++k)
+        w[k] = pack_fixed16x2(__uint_as_float(v[2 * k]) * up, __uint_as_float(v[2 * k + 1]) * up);
+      // send slot b is free once our copy of page p-2 has read it
+      if (lane == 0 && p >= 2) bulk_wait_read_1();
+      __syncwarp();
+      const uint32_t dst = xsend + b * kXSlot + row * kXRowBytes;
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            w[16 * hlf + j] = pack_f16x2_sat(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
-        }
-        tc_fence_before();
-        mbar_arrive(bar(sh.s_free[b]));
-        // the peer's P.V two pages back (for the first two pages: its first
-        // query leaving its slots) freed its receive slot and our send slot
-        ok = mbar_wait<true>(bar(sh.can_send[b]), (p >> 1) & 1, abort);
-        ok = __all_sync(0xffffffffu, ok);
-        if (ok) {
-          const uint32_t dst = xsrc + b * kXSlot + row * 128;
-#pragma unroll
-          for (int c = 0; c < 8; ++c)
-            st_shared_v4(dst + ((c ^ (row & 7)) << 4), w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
-          fence_proxy_async();
-        }
+      for (int c = 0; c < 8; ++c)
+        st_shared_v4(dst + ((c ^ (row & 7)) << 4), w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+      sh.xscale_send[b][row] = exp2_int(-ke);
+      fence_proxy_async();
+      // the peer's P.V two pages back (for the first two pages: its first
+      // query leaving its slots) freed its receive slot b
+      ok = mbar_wait<true>(bar(sh.can_send[b]), (p >> 1) & 1, abort, lim);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      if (lane == 0) {
+        const uint32_t off = b * kXSlot + quad * kXQuadBytes, xb = b ? peer_xfull1 : peer_xfull0;
+        const uint32_t soff = (b * kRowsPerCta + quad * 32) * 4;
+        bulk_s2s(peer_recv + off, xsend + off, kXQuadBytes, xb);
+        bulk_s2s(peer_scale + soff, smem_u32(&sh.xscale_send[0][0]) + soff, kXScaleBytes, xb);
+        bulk_commit_group();
       }
       __syncwarp();
-      if (ok && lane == 0) {
-        const uint32_t off = b * kXSlot + quad * 32 * 128;
-        bulk_s2s(peer_recv + off, xsrc + off, 32 * 128, b ? peer_xfull1 : peer_xfull0);
-      }
-      __syncwarp();
+      sent = p + 1;
     }
     if (!ok) fail();
   } else {
     // ------------------------------------------------------------ softmax warps
     // Thread = one query row (TMEM lane) and 32 of each page's 64 keys (key
-    // half).  Page q: full scores (S_b) -> mask -> row maximum shared with
-    // the partner warp -> online softmax -> P (bf16) into receive slot b, in
-    // the layout of an MMA operand.  After a failure the loops keep running
-    // without work, so every named barrier still sees both warps.
+    // half).  Page q: full scores (own S_b in fp32 + the peer's 16-bit
+    // partial in receive slot b) -> mask -> row maximum shared with the
+    // partner warp -> online softmax -> P (bf16) into receive slot b, over
+    // the partial this thread read there, in the layout of an MMA operand.
+    // After a failure the loops keep running without work, so every named
+    // barrier still sees both warps.
     const int quad = warp & 3, half = warp >> 2;
     const int row = quad * 32 + lane;              // TMEM lane = query row in this block
     const int grow = (int)rg * kRowsPerCta + row;  // row of the (l, h) list
@@ -749,9 +841,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     auto qrow_of = [&](int b) { return a.q_cat + ((size_t)(b * a.Lq + l) * a.H + h) * d_q; };
     auto load_q = [&](int b) {
       if (!ok) return;
-      if (leader)
-        tma_load_2d(qrope, &tm_qrope, bar(sh.q_full), a.d_g + 32 * (int)r,
-                    b * a.Lq * a.H + (int)rg * kRowsPerCta);
+      if (leader) {
+        mbar_arrive_expect_tx(bar(sh.q_tma), kQRopeBytes);
+        tma_load_2d(qrope, &tm_qrope, bar(sh.q_tma), a.d_g + 32 * (int)r, b * a.Lq * a.H + (int)rg * kRowsPerCta);
+        ++nq_tma;
+      }
       const uint4* lat = nullptr;
       if (valid) {
         const __nv_bfloat16* qrow = qrow_of(b);
@@ -770,8 +864,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       }
       tmem_wait_st();
       tc_fence_before();
-      if (leader) mbar_arrive_expect_tx(bar(sh.q_full), kQRopeBytes);
-      else mbar_arrive(bar(sh.q_full));
+      mbar_arrive(bar(sh.q_full));
     };
     // pull what this thread will load for sequence b into L2 ahead of use
     auto prefetch_q = [&](int b) {
@@ -793,14 +886,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     // the first segment's query: latent half from the exchange slots (box
     // j = 64 columns, 128-byte swizzle), RoPE half already in its tile
     auto load_q_first = [&]() {
-      ok = mbar_wait(bar(sh.q_lat), 0, abort);
+      ok = mbar_wait(bar(sh.q_lat), 0, abort, lim);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) return;
       const bool use = valid && (a.G == 1 || (uint32_t)g == r);
 #pragma unroll 1
       for (int c = 0; c < 2; ++c) {
         uint32_t w[32];
-        const uint32_t src = xsrc + (2 * half + c) * kXSlot + row * 128;
+        const uint32_t src = xsend + (2 * half + c) * kQBoxBytes + row * 128;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           ld_shared_v4(src + ((k ^ (row & 7)) << 4), w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
@@ -835,42 +928,39 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       }
       float s[32];  // raw scores (unscaled) of this thread's 32 keys
       float mt = -INFINITY;
-      if (ok) ok = mbar_wait(bar(sh.s_full[b]), (q >> 1) & 1, abort);
-      if (ok) ok = mbar_wait(bar(sh.xfull[b]), (q >> 1) & 1, abort);
+      // own partial (fp32, tensor memory) requested as soon as QK is done,
+      // while the peer's partial may still be on its way
+      uint32_t v[32];
+      if (ok) ok = mbar_wait(bar(sh.s_full[b]), (q >> 1) & 1, abort, lim);
+      if (ok) ok = mbar_wait(bar(sh.xfull[b][quad]), (q >> 1) & 1, abort, lim);
       ok = __all_sync(0xffffffffu, ok);
       if (ok) {
         tc_fence_after();
-        uint32_t v[32];
-        tmem_ld32(lane_base + kColS + 64 * b + 32 * half, v);  // own partial, fp32
-        const uint32_t src = xrecv + b * kXSlot + row * 128;     // peer partial, fp16
+        tmem_ld32(lane_base + kColS + 64 * b + 32 * half, v);
+        const uint32_t src = xrecv + b * kXSlot + row * kXRowBytes;  // the peer's, 16-bit
         uint32_t pw[16];
 #pragma unroll
         for (int c = 0; c < 4; ++c)
           ld_shared_v4(src + (((4 * half + c) ^ (row & 7)) << 4), pw[4 * c], pw[4 * c + 1], pw[4 * c + 2],
                        pw[4 * c + 3]);
+        const float down = sh.xscale_recv[b][row];
         tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(bar(sh.s_free[b]));
-        if (leader) mbar_arrive_expect_tx(bar(sh.xfull[b]), kXSlot);  // armed for page q+2 (sent after our PV(q))
+        // armed for page q+2 (sent by the peer only after our P.V of page q)
+        if (half == 0 && lane == 0) mbar_arrive_expect_tx(bar(sh.xfull[b][quad]), kXQuadTx);
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
-          const float2 y = unpack_f16x2(pw[k]);
-          s[2 * k] = __uint_as_float(v[2 * k]) + y.x;
-          s[2 * k + 1] = __uint_as_float(v[2 * k + 1]) + y.y;
+          const float2 y = unpack_fixed16x2(pw[k]);
+          s[2 * k] = fmaf(y.x, down, __uint_as_float(v[2 * k]));
+          s[2 * k + 1] = fmaf(y.y, down, __uint_as_float(v[2 * k + 1]));
         }
         const int key0 = cur.i * kPage + 32 * half;
         if (limit < key0 + 32) {  // keys this row may not see
 #pragma unroll
           for (int j = 0; j < 32; ++j) s[j] = (key0 + j < limit) ? s[j] : -INFINITY;
         }
-        float mx[16];  // tree maximum
-#pragma unroll
-        for (int j = 0; j < 16; ++j) mx[j] = fmaxf(s[j], s[j + 16]);
-#pragma unroll
-        for (int w = 8; w >= 1; w >>= 1)
-#pragma unroll
-          for (int j = 0; j < w; ++j) mx[j] = fmaxf(mx[j], mx[j + w]);
-        mt = mx[0];
+        mt = max32(s);
         sh.red[b][half][row] = mt;
       }
       ok = bar_red_and_n(ok, pair_bar, 64);
@@ -878,7 +968,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         mt = fmaxf(mt, sh.red[b][half ^ 1][row]) * a.scale_log2;  // log2 units
         const bool need = mt > m_used + kRescaleThreshold;
         if (!cur.seg_first() && __any_sync(0xffffffffu, need)) {  // rescale O once P.V of page q-1 is done
-          ok = mbar_wait(bar(sh.o_done[(q - 1) & 1]), ((q - 1) >> 1) & 1, abort);
+          ok = mbar_wait(bar(sh.o_done[(q - 1) & 1]), ((q - 1) >> 1) & 1, abort, lim);
           ok = __all_sync(0xffffffffu, ok);
           if (ok) {
             tc_fence_after();
@@ -912,7 +1002,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           l_part += psum;
           // P row into receive slot b, over the peer partial this thread
           // read there: K-major, 128-byte swizzle, four 16-byte chunks
-          const uint32_t dst = xrecv + b * kXSlot + row * 128;
+          const uint32_t dst = xrecv + b * kXSlot + row * kXRowBytes;
 #pragma unroll
           for (int c = 0; c < 4; ++c)
             st_shared_v4(dst + (((4 * half + c) ^ (row & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
@@ -930,7 +1020,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 
       // ---- end of segment: normalised latent partial and log-sum-exp
       if (cur.seg_last()) {
-        if (ok) ok = mbar_wait(bar(sh.o_done[b]), (q >> 1) & 1, abort);  // this page's P.V
+        if (ok) ok = mbar_wait(bar(sh.o_done[b]), (q >> 1) & 1, abort, lim);  // this page's P.V
         ok = __all_sync(0xffffffffu, ok);
         if (ok) tc_fence_after();
         sh.red[b ^ 1][half][row] = l_part;  // parity of the next page: free until its maximum
@@ -968,21 +1058,40 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   }
 
   // ------------------------------------------------------------ teardown
+  // Every role has left its loop.  Each thread that started asynchronous
+  // work waits (ignoring the abort flag) until it is done: after a normal
+  // run these waits return at once; after an abort they keep copies and
+  // MMAs from landing in memory that is about to be released.
   __syncthreads();
+  if (warp == kTmaWarp && lane == 0) {
+    for (uint32_t k = issued > (uint32_t)kStages ? issued - kStages : 0; k < issued; ++k)
+      mbar_wait_quiet(bar(sh.full[k % kStages]), (k / kStages) & 1);
+    if (issued > 0) mbar_wait_quiet(bar(sh.q_lat), 0);
+  } else if ((warp == kMmaWarp || warp == kPvWarp) && lane == 0) {
+    const int d = warp == kMmaWarp ? 0 : 1;
+    mma_commit(bar(sh.drain[d]));
+    mbar_wait_quiet(bar(sh.drain[d]), 0);
+  } else if (threadIdx.x == 0 && nq_tma > 0) {
+    mbar_wait_quiet(bar(sh.q_tma), (nq_tma - 1) & 1);
+  } else if (warp >= kSWarps && warp < kSWarps + kXWarps && lane == 0) {
+    bulk_wait_read_all();  // this thread's copies have read their send slot
+    st_cluster_u32(mapa(smem_u32(&sh.peer_sent[warp - kSWarps]), peer), (uint32_t)sent);
+  }
+  __syncwarp();
+  cluster_sync();  // every copy of the pair issued, the counts of pages sent visible
+  // partial scores the peer sent here but this CTA never read (after an
+  // abort): its last two pages of each quadrant may still be in flight
+  if (warp >= kSWarps && warp < kSWarps + kXWarps && lane == 0) {
+    const int qd = warp - kSWarps, n = sh.peer_sent[qd];
+    for (int p = n > 2 ? n - 2 : 0; p < n; ++p) mbar_wait_quiet(bar(sh.xfull[p & 1][qd]), (p >> 1) & 1);
+  }
+  __syncwarp();
   if (warp == kMmaWarp) {
-    if (*abort) {  // let MMAs already issued finish before freeing their memory
-      if (lane == 0) {
-        mma_commit(bar(sh.drain));
-        mbar_wait(bar(sh.drain), 0, abort, 100000000ull);
-      }
-      __syncwarp();
-    }
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
-  cluster_sync();  // the peer may still write into this CTA's exchange buffer until here
+  cluster_sync();  // neither CTA leaves while the other may still signal it
 }
-
 // ---------------------------------------------------------------- plan
 // One CTA; used when B is too large for the decode kernel to plan for
 // itself.  Validates lengths and table entries, prefix-sums pages per

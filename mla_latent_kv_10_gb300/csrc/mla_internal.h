@@ -80,7 +80,14 @@ struct DecodeArgs {
   int plan_in_kernel; // 1: every CTA computes the split itself (B <= kPlanInKernelMaxB)
   int units;
   const int32_t* seq_lens;
+  unsigned long long wait_ns;  // wall-clock limit of each pipeline wait inside the kernel
+  int stall_page;              // testing: the QK issuer waits on a barrier nothing completes before this page (-1: off)
 };
+// Testing settings of the decode launches (mla_set_timeout_test): the limit
+// of the pipeline waits (normally 2 s) and the page before which the QK
+// issuer stalls (normally -1, never).
+unsigned long long decode_wait_limit_ns();
+int decode_stall_page();
 constexpr int kPlanInKernelMaxB = 448;  // one sequence per decode-kernel thread (its block size)
 
 // launchers (return cudaError_t of the launch)

@@ -90,6 +90,20 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// Bounded wait that ignores the abort flag: for draining work this thread
+// (or its CTA) started before it gave up, which must land before the memory
+// it targets is released.  Gives up only after `limit_ns`.
+__device__ __forceinline__ bool mbar_wait_quiet(uint32_t bar, uint32_t parity,
+                                                uint64_t limit_ns = 100000000ull) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+#pragma unroll 1
+  for (uint32_t i = 0;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63) == 63 && globaltimer_ns() - t0 > limit_ns) return false;
+  }
+}
+
 // ------------------------------------------------------------------ launch chaining
 // Programmatic dependent launch: a kernel launched with programmatic stream
 // serialization may start while the kernel before it on the stream still
@@ -143,6 +157,20 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, float4 v) {
   asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y),
                "f"(v.z), "f"(v.w)
                : "memory");
+}
+__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+// Asynchronous 16-byte store into another CTA of the cluster; its bytes are
+// counted (complete_tx) on the mbarrier `cluster_bar`, which must live in the
+// destination CTA.
+__device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, uint32_t a, uint32_t b, uint32_t c,
+                                            uint32_t d, uint32_t cluster_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+          cluster_addr),
+      "r"(a), "r"(b), "r"(c), "r"(d), "r"(cluster_bar)
+      : "memory");
 }
 __device__ __forceinline__ void cluster_arrive() {
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");

@@ -67,3 +67,26 @@ def check_case(case, got, pairs, nthreads=0):
     errs["lse"] = assert_close(got["lse"].to(torch.float64).numpy()[bi, :, hi], ref_lse[bi, :, hi], "lse")
     errs["out"] = assert_close(got["out"].to(torch.float64).numpy()[bi, :, hi], ref_out[bi, :, hi], "out")
     return errs
+
+
+def run_decode_only(case, q_cat, num_splits=0, device="cuda"):
+    """mla_decode_paged + mla_combine_splits on a given q_cat (bf16
+    [B,Lq,H,d_g+64]); returns host copies of o_lat, lse and the status."""
+    t = {k: v.to(device) for k, v in case.tensors().items()}
+    bufs = mla.DecodeBuffers(case.dims, device)
+    bufs.q_cat.copy_(q_cat.to(device))
+    mla.mla_decode_paged(case.dims, bufs.q_cat, t["cache"], t["block_table"], t["seq_lens"], num_splits,
+                         bufs.o_part, bufs.lse_part, bufs.workspace)
+    mla.mla_combine_splits(case.dims, bufs.o_part, bufs.lse_part, bufs.workspace, bufs.o_lat, bufs.lse)
+    status = mla.mla_get_device_status(bufs.workspace)
+    torch.cuda.synchronize()
+    return dict(o_lat=bufs.o_lat.cpu(), lse=bufs.lse.cpu(), status=status,
+                ws=bufs.workspace.cpu().view(torch.int32).numpy())
+
+
+def scaled_queries(case, mag):
+    """Scale q_nope and q_rope by `mag` (in fp64) and round to bf16 once:
+    logits grow by mag (scores in the tens to hundreds)."""
+    case.q_nope = (case.q_nope.double() * mag).to(torch.bfloat16)
+    case.q_rope = (case.q_rope.double() * mag).to(torch.bfloat16)
+    return case

@@ -126,3 +126,12 @@ def test_python_binding_raises_mla_error(lib):
     with pytest.raises(mla.MLAError) as e:
         mla.mla_decode_workspace_size(dims(G=3))
     assert e.value.code == -2
+
+
+def test_timeout_test_hook_arguments(lib):
+    """The testing hook of the decode kernel's timeout path validates its
+    arguments on the host (no GPU needed) and restores the defaults."""
+    assert lib.mla_set_timeout_test(-1, -1) == -1
+    assert lib.mla_set_timeout_test(0, -2) == -1
+    assert lib.mla_set_timeout_test(1000, 3) == 0
+    assert lib.mla_set_timeout_test(0, -1) == 0
