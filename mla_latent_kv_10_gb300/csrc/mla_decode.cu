@@ -225,6 +225,7 @@ struct DecodeShared {
   uint32_t tmem;
   int abort;
   int peer_sent[4];              // pages the peer's exchange warp of each quadrant sent here (teardown)
+  int lens[kPlanInKernelMaxB];   // validated sequence lengths (in-kernel plan)
 };
 
 // All shared memory is dynamic: stage ring, exchange slots, then the small state.
@@ -239,14 +240,19 @@ __device__ __forceinline__ int aligned_units(int np, int units, int total) {
 
 // Walks the (sequence, page range) segments of one work unit from its
 // UnitRec, reading page counts from seq_lens (validated lengths).
+// Lengths come from shared memory (validated by the in-kernel plan) or,
+// when the plan kernel split the work, from seq_lens (clamped here).
 struct SegIter {
   int b, o, start, end, bias;
-  __device__ void init(const UnitRec& r) {
+  const int* lens;
+  bool raw;
+  __device__ void init(const UnitRec& r, const int* l, bool clamp) {
     b = r.b; o = r.o; start = r.start; end = r.end; bias = r.bias;
+    lens = l; raw = clamp;
   }
   __device__ int slot(int sb) const { return sb + bias; }
-  __device__ static int len(const DecodeArgs& a, int sb) {
-    return clamp_len(a.seq_lens[sb], a.Lq > 1 ? a.Lq : 1, a.max_pages * kPage);
+  __device__ int len(const DecodeArgs& a, int sb) const {
+    return raw ? clamp_len(lens[sb], a.Lq > 1 ? a.Lq : 1, a.max_pages * kPage) : lens[sb];
   }
   // Next non-empty segment: sequence sb, pages [pa, pb) of that sequence.
   __device__ bool next(const DecodeArgs& a, int& sb, int& pa, int& pb) {
@@ -273,8 +279,8 @@ struct PageCursor {
   SegIter it;
   int sb, pa, pb, i;
   bool valid;
-  __device__ void init(const UnitRec& r, const DecodeArgs& a) {
-    it.init(r);
+  __device__ void init(const UnitRec& r, const DecodeArgs& a, const int* l, bool clamp) {
+    it.init(r, l, clamp);
     valid = it.next(a, sb, pa, pb);
     i = pa;
   }
@@ -336,7 +342,8 @@ constexpr int kSwitchPages = 4;  // cost of a sequence switch inside a unit, in 
 // and this unit's UnitRec.  `writer` also stores the per-sequence slot
 // ranges and the header for the combine kernel.  scr: >= 3*B + 3 ints of
 // shared scratch; red: 33 ints.
-__device__ void plan_in_block(const DecodeArgs& a, int unit, bool writer, int* scr, int* red, UnitRec* out) {
+__device__ void plan_in_block(const DecodeArgs& a, int unit, bool writer, int* scr, int* red, int* lens_s,
+                              UnitRec* out) {
   const int B = a.B, units = a.units, tid = threadIdx.x;
   const WsView v = ws_view(a.ws, B);
   int* off_s = scr;            // [B+1]
@@ -350,6 +357,7 @@ __device__ void plan_in_block(const DecodeArgs& a, int unit, bool writer, int* s
       if (n != n0) set_status(a.ws, MLA_ERR_BAD_SEQLEN);
       v.nlen[tid] = n;
     }
+    lens_s[tid] = n;
     np = (n + kPage - 1) / kPage;
   }
   int total = 0;
@@ -439,7 +447,8 @@ __device__ __forceinline__ int warp_scan_incl(int v) {
 // with shuffles and votes instead of block-wide barriers.  The balanced
 // split's widest unit is found by counting, per unit, the sequences that
 // start strictly inside it (the unit touches one more sequence than that).
-__device__ void plan_in_warp(const DecodeArgs& a, int unit, bool writer, UnitRec* out) {
+// n0: seq_lens[lane] (lanes < B), loaded by the caller ahead of time.
+__device__ void plan_in_warp(const DecodeArgs& a, int unit, bool writer, int n0, int* lens_s, UnitRec* out) {
   const unsigned full = 0xffffffffu;
   const int B = a.B, units = a.units, lane = threadIdx.x & 31;
   const WsView v = ws_view(a.ws, B);
@@ -447,12 +456,12 @@ __device__ void plan_in_warp(const DecodeArgs& a, int unit, bool writer, UnitRec
   const bool act = lane < B;
   int np = 0;
   if (act) {
-    const int n0 = a.seq_lens[lane];
     const int n = clamp_len(n0, lo, hi);
     if (writer) {
       if (n != n0) set_status(a.ws, MLA_ERR_BAD_SEQLEN);
       v.nlen[lane] = n;
     }
+    lens_s[lane] = n;
     np = (n + kPage - 1) / kPage;
   }
   const int incl = warp_scan_incl(np);
@@ -545,8 +554,27 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   const uint64_t lim = a.wait_ns;        // limit of every pipeline wait
 
   auto bar = [](uint64_t& x) { return smem_u32(&x); };
+  const bool warp_plan = a.plan_in_kernel && a.B <= kPlanWarpMaxB;
 
-  if (threadIdx.x == 0) {
+  // Warp 0 (the planning warp for small batches) waits for the kernel
+  // before and requests the sequence lengths at once, so their load
+  // overlaps the set-up below.  The TMA warp pulls this CTA's share of the
+  // block table into L2 (a prefetch cannot return stale data, so it may
+  // precede the wait).
+  int n_pre = 0;
+  if (warp == 0 && warp_plan) {
+    griddep_wait();
+    if (lane < a.B) n_pre = a.seq_lens[lane];
+  } else if (warp == kTmaWarp) {
+    const size_t lines = ((size_t)a.B * a.max_pages * 4 + 127) / 128;
+    const size_t ctas = (size_t)gridDim.x, per = (lines + ctas - 1) / ctas;
+    const char* tb = reinterpret_cast<const char*>(a.block_table);
+    for (size_t k = lane; k < per && k < 256; k += 32) {
+      const size_t line = (size_t)blockIdx.x * per + k;
+      if (line < lines) asm volatile("prefetch.global.L2 [%0];" ::"l"(tb + line * 128));
+    }
+  }
+  if (threadIdx.x == kTmaWarp * 32) {
     sh.abort = 0;
     for (int q = 0; q < 4; ++q) sh.peer_sent[q] = 0;
     for (int s = 0; s < kStages; ++s) {
@@ -564,7 +592,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       mbar_init(bar(sh.s_free[s]), kSoftmaxThreads + kXThreads);
       mbar_init(bar(sh.p_full[s]), kSoftmaxThreads);
       mbar_init(bar(sh.o_done[s]), 1);
-      mbar_init(bar(sh.can_send[s]), 1);  // one arrival from the peer's MMA completion
+      mbar_init(bar(sh.can_send[s]), 1);  // one remote arrival from the peer
       for (int q = 0; q < 4; ++q) mbar_init(bar(sh.xfull[s][q]), 1);  // armed, completed by the peer's stores
     }
     fence_mbar_init();
@@ -581,7 +609,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync();  // peer barriers initialised before any remote arrive or store
+  // The peer's barriers must be initialised before any remote arrive or
+  // copy: arrive on the cluster barrier now (relaxed: the initialisation
+  // fence above already orders the barrier set-up), wait after the plan.
+  cluster_arrive_relaxed();
   tc_fence_after();
   const uint32_t tmem = sh.tmem;
   volatile int* abort = &sh.abort;
@@ -593,15 +624,18 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   // the whole block with the still unused exchange slots as scratch), or
   // read from the plan kernel's records
   if (a.plan_in_kernel && a.B <= kPlanWarpMaxB) {
-    if (warp == 0) plan_in_warp(a, unit, unit == 0 && crank == 0, &sh.rec);
+    if (warp == 0) plan_in_warp(a, unit, unit == 0 && crank == 0, n_pre, sh.lens, &sh.rec);
   } else if (a.plan_in_kernel) {
     int* scratch = reinterpret_cast<int*>(smem + kXOff);
-    plan_in_block(a, unit, unit == 0 && crank == 0, scratch, scratch + 3 * a.B + 8, &sh.rec);
+    plan_in_block(a, unit, unit == 0 && crank == 0, scratch, scratch + 3 * a.B + 8, sh.lens, &sh.rec);
   } else if (threadIdx.x == 0) {
     sh.rec = ws_view(ws, a.B).rec[unit];
   }
   fence_proxy_async();  // the plan's scratch writes come before the query copies into the same slots
   __syncthreads();
+  cluster_wait();
+  const int* lens = a.plan_in_kernel ? sh.lens : a.seq_lens;  // where the page walkers read lengths
+  const bool lens_raw = !a.plan_in_kernel;
 
   // A wait that gives up stops both CTAs of the pair.
   const uint32_t peer_abort = mapa(smem_u32(&sh.abort), peer);
@@ -617,52 +651,56 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 
   if (warp == kTmaWarp) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
+    // The whole warp walks the unit's pages (lane 0 issues the copies); the
+    // block-table entries of up to 32 pages come in with one coalesced load.
+    {
       const uint32_t bytes = kStageBytes;
       const uint64_t policy = l2_policy_evict_first();
       SegIter it;
-      it.init(sh.rec);
+      it.init(sh.rec, lens, lens_raw);
       int sb, pa, pb;
       bool ok = true;
       while (ok && it.next(a, sb, pa, pb)) {
         const int32_t* bt = a.block_table + (size_t)sb * a.max_pages;
-        for (int i = pa; i < pb; ++i) {
-          const uint32_t pc = issued;
-          const int st = pc % kStages;
-          if (pc >= (uint32_t)kStages && !(ok = mbar_wait(bar(sh.empty[st]), ((pc / kStages) - 1) & 1, abort, lim))) {
-            fail();
-            break;
-          }
-          int page = bt[i];
-          if (page < 0 || page >= a.num_pages) {  // never dereferenced: clamped and reported
-            set_status(ws, MLA_ERR_BAD_TABLE);
-            page = 0;
-          }
-          if (pc == 0) {  // the first segment's query, ahead of its first page
-            const int qy = sb * a.Lq * a.H + (int)rg * kRowsPerCta;
-            const int qx = a.G == 1 ? (int)r * 256 : 0;
-            mbar_arrive_expect_tx(bar(sh.q_lat), 4 * kQBoxBytes + kQRopeBytes);
-            for (int j = 0; j < 4; ++j) tma_load_2d(xsend + j * kQBoxBytes, &tm_qlat, bar(sh.q_lat), qx + 64 * j, qy);
-            tma_load_2d(qrope, &tm_qrope, bar(sh.q_lat), a.d_g + 32 * (int)r, qy);
-          }
-          const uint32_t dst = smem_u32(stages + st * kStageBytes);
-          mbar_arrive_expect_tx(bar(sh.full[st]), bytes);
-          for (int j = 0; j < 4; ++j)  // this CTA's latent half
-            tma_load_2d_hint(dst + j * kBoxBytes, &tm_cache, bar(sh.full[st]), (int)(r * 256 + j * 64),
-                             page * kPage, policy);
-          // this CTA's 32 RoPE columns
-          tma_load_2d_hint(dst + 4 * kBoxBytes, &tm_rope, bar(sh.full[st]), kDc + 32 * (int)r, page * kPage,
-                           policy);
-          ++issued;
-          // At start-up every CTA of the grid asks for its pages at once; let
-          // the first page land before queueing the rest so compute starts
-          // as early as possible instead of after the whole initial burst.
-          if (pc == 0 && !(ok = mbar_wait(bar(sh.full[0]), 0, abort, lim))) {
-            fail();
-            break;
+        for (int c0 = pa; ok && c0 < pb; c0 += 32) {
+          const int nc = min(32, pb - c0);
+          const int mine = lane < nc ? bt[c0 + lane] : 0;
+          for (int j = 0; j < nc; ++j) {
+            const uint32_t pc = issued;
+            const int st = pc % kStages;
+            if (pc >= (uint32_t)kStages) {
+              ok = mbar_wait(bar(sh.empty[st]), ((pc / kStages) - 1) & 1, abort, lim);
+              ok = __all_sync(0xffffffffu, ok);
+              if (!ok) break;
+            }
+            int page = __shfl_sync(0xffffffffu, mine, j);
+            if (page < 0 || page >= a.num_pages) {  // never dereferenced: clamped and reported
+              if (lane == 0) set_status(ws, MLA_ERR_BAD_TABLE);
+              page = 0;
+            }
+            if (lane == 0) {
+              if (pc == 0) {  // the first segment's query, ahead of its first page
+                const int qy = sb * a.Lq * a.H + (int)rg * kRowsPerCta;
+                const int qx = a.G == 1 ? (int)r * 256 : 0;
+                mbar_arrive_expect_tx(bar(sh.q_lat), 4 * kQBoxBytes + kQRopeBytes);
+                for (int q = 0; q < 4; ++q)
+                  tma_load_2d(xsend + q * kQBoxBytes, &tm_qlat, bar(sh.q_lat), qx + 64 * q, qy);
+                tma_load_2d(qrope, &tm_qrope, bar(sh.q_lat), a.d_g + 32 * (int)r, qy);
+              }
+              const uint32_t dst = smem_u32(stages + st * kStageBytes);
+              mbar_arrive_expect_tx(bar(sh.full[st]), bytes);
+              for (int q = 0; q < 4; ++q)  // this CTA's latent half
+                tma_load_2d_hint(dst + q * kBoxBytes, &tm_cache, bar(sh.full[st]), (int)(r * 256 + q * 64),
+                                 page * kPage, policy);
+              // this CTA's 32 RoPE columns
+              tma_load_2d_hint(dst + 4 * kBoxBytes, &tm_rope, bar(sh.full[st]), kDc + 32 * (int)r, page * kPage,
+                               policy);
+            }
+            ++issued;
           }
         }
       }
+      if (!ok && lane == 0) fail();
     }
     __syncwarp();  // reconverge before the CTA-wide barrier of the teardown
   } else if (warp == kMmaWarp) {
@@ -677,7 +715,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       constexpr uint32_t idesc_qk = idesc_bf16(128, 64, false, false);
       const uint64_t qr0 = sdesc_sw64(qrope, 512);
       PageCursor c;
-      c.init(sh.rec, a);
+      c.init(sh.rec, a, lens, lens_raw);
       uint32_t pc = 0, qc = 0;
       bool ok = true;
       while (ok && c.valid) {
@@ -729,7 +767,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       const uint32_t peer_can_send0 = mapa(bar(sh.can_send[0]), peer);
       const uint32_t peer_can_send1 = mapa(bar(sh.can_send[1]), peer);
       PageCursor c;
-      c.init(sh.rec, a);
+      c.init(sh.rec, a, lens, lens_raw);
       bool ok = true;
       for (uint32_t p = 0; ok && c.valid; ++p) {
         const uint32_t b = p & 1;
@@ -907,7 +945,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     };
 
     PageCursor cur;
-    cur.init(sh.rec, a);
+    cur.init(sh.rec, a, lens, lens_raw);
     if (cur.valid) {
       load_q_first();
       prefetch_after(cur.it);
@@ -923,7 +961,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         m_used = -INFINITY;
         l_part = 0.f;
         seg = cur.it.slot(cur.sb);
-        const int n = SegIter::len(a, cur.sb);
+        const int n = cur.it.len(a, cur.sb);
         limit = a.causal ? n - a.Lq + l + 1 : n;  // keys [0, limit) visible
       }
       float s[32];  // raw scores (unscaled) of this thread's 32 keys

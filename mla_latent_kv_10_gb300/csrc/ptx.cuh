@@ -175,6 +175,11 @@ __device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, uint32_t a, u
 __device__ __forceinline__ void cluster_arrive() {
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
+// Arrive without release ordering (after fence.mbarrier_init, which orders
+// the barrier initialisations the peers rely on).
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
 __device__ __forceinline__ void cluster_wait() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
