@@ -2,6 +2,8 @@
 
 A step is the whole hot path on one batch of synthetic input:
     mla_absorb_q -> mla_decode_paged -> mla_combine_splits -> mla_project_uv
+(--fused runs mla_combine_project, the merge inside the W_UV projection,
+instead of the last two; it measured slightly slower in the step.)
 (mla_decode_paged is one kernel launch for B <= 448: the decode kernel
 computes its own split; larger batches add a plan kernel before it.)
 Each step is one CUDA-graph replay (the kernels chain by programmatic
@@ -209,7 +211,7 @@ def run_reference(args, world, rank):
         "ms_per_step": 1e3 * total / work,  # time the oracle would take for one whole step
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "tflops": step_flops * work / total / 1e12,
-        "config": {"workload": WORKLOAD_TEXT[args.workload], "B": B, "Lq": d["Lq"], "H": H, "G": d["G"],
+        "config": {"workload": WORKLOAD_TEXT[args.workload], "step": "fused" if args.fused else "four calls", "B": B, "Lq": d["Lq"], "H": H, "G": d["G"],
                    "parallelism": "replicas" if world > 1 else "single"},
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": nt, "kind": "oracle",
                          "sample": "%d random (sequence, head) pairs per step; metric scaled by the "
@@ -259,6 +261,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--splits", type=int, default=0)
+    ap.add_argument("--fused", action="store_true", help="one fused combine + projection launch")
     args = ap.parse_args()
     world, rank, local = dist_env()
     if args.impl == "reference":
@@ -304,8 +307,12 @@ def main():
                              bufs.o_part, bufs.lse_part, bufs.workspace)
 
     def post():
-        mla.mla_combine_splits(d, bufs.o_part, bufs.lse_part, bufs.workspace, bufs.o_lat, bufs.lse)
-        mla.mla_project_uv(d, bufs.o_lat, t["W_UV"], bufs.out)
+        if not args.fused:
+            mla.mla_combine_splits(d, bufs.o_part, bufs.lse_part, bufs.workspace, bufs.o_lat, bufs.lse)
+            mla.mla_project_uv(d, bufs.o_lat, t["W_UV"], bufs.out)
+        else:
+            mla.mla_combine_project(d, bufs.o_part, bufs.lse_part, bufs.workspace, t["W_UV"], bufs.out,
+                                    bufs.o_lat, bufs.lse)
 
     def step(i):
         pre()
@@ -439,7 +446,7 @@ def main():
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) cache and queries, N(0,1/d_g) weights)",
-        "config": {"workload": WORKLOAD_TEXT[args.workload], "B": B, "Lq": Lq, "H": H, "G": G,
+        "config": {"workload": WORKLOAD_TEXT[args.workload], "step": "fused" if args.fused else "four calls", "B": B, "Lq": Lq, "H": H, "G": G,
                    "seq_len_mean": sum(seq) / len(seq), "page_size": 64,
                    "parallelism": "replicas" if world > 1 else "single",
                    "l2": "inputs larger than L2: %d rotating cache copies (%.0f MB)" % (copies, copies * cache_bytes / 1e6)},
@@ -459,9 +466,10 @@ def main():
         "roofline": roofline_entry(dec_bytes, dec_flops, dec_ms, peaks, decode_traffic(args.workload), peak_src),
         "e2e": {"value": job_rate(world, kv_bytes, e2e_ms) / 1e9, "unit": "GB/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": mla.launches_per_step(case.dims) * args.steps,
-        "timing": "one CUDA-graph replay per step (absorb, decode and projection chained by programmatic dependent launch; combine launched after the decode); "
-                  "gpu_launches counts the kernels of the timed steps",
+        "gpu_launches": mla.launches_per_step(case.dims, fused=args.fused) * args.steps,
+        "timing": "one CUDA-graph replay per step: absorb, decode, combine, projection (absorb, decode and "
+                  "projection chained by programmatic dependent launch; --fused: one combine + projection "
+                  "kernel); gpu_launches counts the kernels of the timed steps",
         "sustained": {"steps": n_sus, "ms_per_step": sus_ms, "seconds": sus_ms * n_sus / 1e3,
                       "note": "step graphs replayed back to back for about a second after the timed "
                               "region, inside the clock record"},

@@ -18,6 +18,8 @@
  *
  * One decode step of one layer is four calls on one stream:
  *   mla_absorb_q  →  mla_decode_paged  →  mla_combine_splits  →  mla_project_uv
+ * or three, with the last two fused:
+ *   mla_absorb_q  →  mla_decode_paged  →  mla_combine_project
  *
  * Conventions shared by every entry point
  *   - All tensor arguments are DEVICE pointers owned by the caller. The
@@ -131,6 +133,15 @@ int mla_decode_workspace_size(const mla_dims* dims, size_t* bytes);
 /*
  * mla_decode_paged — split-KV flash-decoding over the paged latent cache.
  *
+ * Source: the attention of the MLA operator write-up §4 ("path B": scores
+ * from the absorbed query against the cached latent and RoPE key, scale
+ * (d_hc + d_R)^-1/2) over the paged cache of §1/§3 (row = 512-d latent +
+ * 64-d RoPE key, 64-token pages).  The split into key ranges with a
+ * per-range (o, lse) and the causal window of multi-token decode are not on
+ * the pages (they are silent on both); the split is flash-decoding's, and
+ * the window is the plainest reading: query l of Lq new tokens sees every
+ * key up to and including its own position.
+ *
  * For each sequence b (n = seq_lens[b] cached tokens, the last Lq of them
  * being the new tokens) and query row (l, h) with visible keys
  * s = 0 .. n-Lq+l:
@@ -164,7 +175,8 @@ int mla_decode_paged(const mla_dims* dims, const void* q_cat,
 
 /*
  * mla_combine_splits — merge the split partials of mla_decode_paged by
- * log-sum-exp (flash-decoding reduction):
+ * log-sum-exp (flash-decoding reduction; the pages are silent on the merge,
+ * this is the exact identity of a softmax taken over disjoint key ranges):
  *     L = log sum_k exp(lse_k),   o_lat = sum_k exp(lse_k - L) * o_k
  * Ranges with lse = -inf contribute nothing.
  * o_part / lse_part / workspace: exactly as passed to mla_decode_paged (the
@@ -177,7 +189,9 @@ int mla_combine_splits(const mla_dims* dims, const float* o_part,
 
 /*
  * mla_project_uv — map the latent output back to the head dimension with
- * W_UV (the up-projection of the values, applied after attention):
+ * W_UV (the up-projection of the values, applied after attention; the MLA
+ * operator write-up §1 says only that the latent is mapped back to the high
+ * dimension when needed, the absorbed form of V = c . W_UV^T per head):
  *     out[b,l,h,:] = W_UV[h] (d_hc x d_g) . o_lat[b,l,h,:]
  * o_lat bf16 [B,Lq,H,d_g]; W_UV bf16 [H,d_hc,d_g]; out bf16 [B,Lq,H,d_hc].
  * fp32 accumulation on the tensor cores.
@@ -202,6 +216,24 @@ int mla_project_uv(const mla_dims* dims, const void* o_lat, const void* W_UV,
  * stall_page < -1).
  */
 int mla_set_timeout_test(long long wait_limit_ns, int stall_page);
+
+/*
+ * mla_combine_project — mla_combine_splits and mla_project_uv in one kernel:
+ * the merged latent rows of each head go straight into on-chip memory as
+ * the operand of the W_UV product, so o_lat never makes a round trip
+ * through device memory (the MLA operator write-up §1 points out that
+ * intermediate reads and writes eat the absorbed path's gains).
+ *     out[b,l,h,:] = W_UV[h] . sum_k exp(lse_k - L) o_k,   L = log sum_k exp(lse_k)
+ * o_part / lse_part / workspace: as passed to mla_decode_paged.  W_UV and
+ * out: as for mla_project_uv.  o_lat (bf16 [B,Lq,H,d_g]) and lse (fp32
+ * [B,Lq,H]) are also written when not NULL.  Same rounding as the two calls
+ * (o_lat rounded to bf16 before the product).
+ * Errors: MLA_ERR_INVALID_ARG / UNSUPPORTED / MISALIGNED / WORKSPACE / CUDA.
+ */
+int mla_combine_project(const mla_dims* dims, const float* o_part,
+                        const float* lse_part, const void* workspace,
+                        size_t ws_bytes, const void* W_UV, void* out,
+                        void* o_lat, float* lse, void* stream);
 
 /*
  * Synchronise `stream`, then return the sticky device status of `workspace`

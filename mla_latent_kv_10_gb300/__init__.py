@@ -13,7 +13,7 @@ import os
 
 __all__ = [
     "MLAError", "Dims", "load_library", "library_path",
-    "mla_absorb_q", "mla_decode_paged", "mla_combine_splits", "mla_project_uv",
+    "mla_absorb_q", "mla_decode_paged", "mla_combine_splits", "mla_project_uv", "mla_combine_project",
     "mla_decode_workspace_size", "mla_decode_num_slots", "mla_decode_kernel_launches",
     "launches_per_step", "mla_get_device_status", "mla_set_timeout_test",
     "mla_status_string", "make_dims", "DecodeBuffers", "decode_step",
@@ -61,6 +61,7 @@ def load_library():
         "mla_decode_paged": [DP, P, P, P, P, I, P, P, P, S, P],
         "mla_combine_splits": [DP, P, P, P, S, P, P, P],
         "mla_project_uv": [DP, P, P, P, P],
+        "mla_combine_project": [DP, P, P, P, S, P, P, P, P, P],
         "mla_get_device_status": [P, P],
         "mla_set_timeout_test": [ctypes.c_longlong, I],
     }
@@ -135,10 +136,10 @@ def mla_decode_kernel_launches(dims) -> int:
     return n.value
 
 
-def launches_per_step(dims) -> int:
-    """Kernel launches of one decode_step: absorb, decode (+ plan), combine,
-    project."""
-    return 3 + mla_decode_kernel_launches(dims)
+def launches_per_step(dims, fused=False) -> int:
+    """Kernel launches of one decode_step: absorb, decode (+ plan), then
+    combine and project (two) or the fused combine + project (one)."""
+    return (2 if fused else 3) + mla_decode_kernel_launches(dims)
 
 
 def mla_decode_paged(dims, q_cat, kv_cache, block_table, seq_lens, num_splits, o_part, lse_part,
@@ -167,6 +168,13 @@ def mla_set_timeout_test(wait_limit_ns: int, stall_page: int):
     _check(load_library().mla_set_timeout_test(int(wait_limit_ns), int(stall_page)), "mla_set_timeout_test")
 
 
+def mla_combine_project(dims, o_part, lse_part, workspace, W_UV, out, o_lat=None, lse=None, stream=None):
+    _check(load_library().mla_combine_project(
+        _dims(dims), _ptr(o_part), _ptr(lse_part), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(W_UV), _ptr(out), _ptr(o_lat), _ptr(lse),
+        _stream(stream)), "mla_combine_project")
+
+
 def mla_get_device_status(workspace, stream=None) -> int:
     return load_library().mla_get_device_status(_ptr(workspace), _stream(stream))
 
@@ -192,12 +200,18 @@ class DecodeBuffers:
 
 
 def decode_step(dims, bufs: DecodeBuffers, q_nope, q_rope, W_UK, W_UV, cache, block_table, seq_lens,
-                num_splits=0, stream=None):
+                num_splits=0, stream=None, fused=False):
     """The whole hot path of one layer's decode step: absorb, paged decode,
-    combine, project.  All tensors on the device; results land in ``bufs``."""
+    then combine and project (or, with ``fused``, the fused combine +
+    project, which also writes o_lat and lse).  All tensors on the device;
+    results land in ``bufs``."""
     mla_absorb_q(dims, q_nope, q_rope, W_UK, bufs.q_cat, stream)
     mla_decode_paged(dims, bufs.q_cat, cache, block_table, seq_lens, num_splits, bufs.o_part,
                      bufs.lse_part, bufs.workspace, stream)
-    mla_combine_splits(dims, bufs.o_part, bufs.lse_part, bufs.workspace, bufs.o_lat, bufs.lse, stream)
-    mla_project_uv(dims, bufs.o_lat, W_UV, bufs.out, stream)
+    if fused:
+        mla_combine_project(dims, bufs.o_part, bufs.lse_part, bufs.workspace, W_UV, bufs.out, bufs.o_lat,
+                            bufs.lse, stream)
+    else:
+        mla_combine_splits(dims, bufs.o_part, bufs.lse_part, bufs.workspace, bufs.o_lat, bufs.lse, stream)
+        mla_project_uv(dims, bufs.o_lat, W_UV, bufs.out, stream)
     return bufs.out

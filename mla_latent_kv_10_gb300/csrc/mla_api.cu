@@ -249,8 +249,35 @@ int mla_combine_splits(const mla_dims* d, const float* o_part, const float* lse_
   if (!o_part || !lse_part || !o_lat) return MLA_ERR_INVALID_ARG;
   if (!workspace || ws_bytes < ws_bytes_for(d->B)) return MLA_ERR_WORKSPACE;
   if (!aligned16(o_part) || !aligned16(o_lat) || !aligned16(workspace)) return MLA_ERR_MISALIGNED;
+  int slots = 0;
+  if ((rc = mla_decode_num_slots(d, &slots)) != MLA_OK) return rc;
   return cuda_status(launch_combine(o_part, lse_part, static_cast<const WsHeader*>(workspace), o_lat,
-                                    lse, d->B, d->Lq, d->H, d->G, static_cast<cudaStream_t>(stream)));
+                                    lse, d->B, d->Lq, d->H, d->G, slots, static_cast<cudaStream_t>(stream)));
+}
+
+int mla_combine_project(const mla_dims* d, const float* o_part, const float* lse_part, const void* workspace,
+                        size_t ws_bytes, const void* W_UV, void* out, void* o_lat, float* lse, void* stream) {
+  int rc = check_dims(d);
+  if (rc != MLA_OK) return rc;
+  if (!o_part || !lse_part || !W_UV || !out) return MLA_ERR_INVALID_ARG;
+  if (!workspace || ws_bytes < ws_bytes_for(d->B)) return MLA_ERR_WORKSPACE;
+  if (!aligned16(o_part) || !aligned16(W_UV) || !aligned16(out) || !aligned16(workspace) ||
+      (o_lat && !aligned16(o_lat)) || (reinterpret_cast<uintptr_t>(lse_part) & 3u) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return MLA_ERR_MISALIGNED;
+  const int H = d->H, dg = kDc / d->G;
+  CUtensorMap tA;
+  {
+    cuuint64_t dims[3] = {(cuuint64_t)dg, (cuuint64_t)kDhc, (cuuint64_t)H};
+    cuuint64_t strides[2] = {(cuuint64_t)dg * 2, (cuuint64_t)kDhc * dg * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)kDhc, 1};  // all 128 output rows of W_UV[h], 64 latent columns
+    if ((rc = make_map(&tA, W_UV, 3, dims, strides, box)) != MLA_OK) return rc;
+  }
+  int slots = 0;
+  if ((rc = mla_decode_num_slots(d, &slots)) != MLA_OK) return rc;
+  return cuda_status(launch_combine_project(tA, o_part, lse_part, static_cast<const WsHeader*>(workspace), out,
+                                            o_lat, lse, d->B, d->Lq, d->H, d->G, slots,
+                                            static_cast<cudaStream_t>(stream)));
 }
 
 int mla_get_device_status(const void* workspace, void* stream) {

@@ -51,7 +51,8 @@
 //   * Split-KV: the pages of all sequences, in order, are cut into equal
 //     contiguous ranges, one per cluster; a range that covers parts of several
 //     sequences yields one partial (o, lse) per sequence, stored in slot
-//     b + unit.  The combine kernel (mla_combine.cu) merges them.
+//     b + unit (o chunk-major, [slot][column/4][row][4] fp32).  mla_combine.cu
+//     merges them, alone or inside the W_UV projection.
 //   * Every wait is bounded (wall clock).  A wait that gives up records
 //     MLA_ERR_TIMEOUT in the workspace status word and raises the abort flag
 //     of both CTAs of the pair; every role then leaves its loop, and the
@@ -1067,8 +1068,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         ok = bar_red_and_n(ok, pair_bar, 64);  // both sums read before the next page's maxima land there
         if (ok) {
           const float inv = l_sum > 0.f ? 1.0f / l_sum : 0.f;
-          // o_part is chunk-major, [slot][column/4][row][4]: consecutive rows
-          // of a warp write consecutive 16-byte chunks.
+          // o_part is chunk-major, [slot][column/4][row][4]: each 16-byte
+          // store of a warp covers 512 contiguous bytes (32 consecutive rows).
           float4* dst = reinterpret_cast<float4*>(a.o_part) +
                         ((size_t)seg * (kDc / 4) + r * 64 + half * 32) * a.rows + grow;
           for (int c = 0; c < 8; ++c) {

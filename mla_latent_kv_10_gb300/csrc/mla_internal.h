@@ -122,8 +122,13 @@ cudaError_t launch_chained(void (*kernel)(KArgs...), dim3 grid, dim3 block, size
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// slots: partial slots the caller allocated (bounds every slot range read)
 cudaError_t launch_combine(const float* o_part, const float* lse_part, const WsHeader* ws,
-                           void* o_lat, float* lse, int B, int Lq, int H, int G, cudaStream_t st);
+                           void* o_lat, float* lse, int B, int Lq, int H, int G, int slots, cudaStream_t st);
+// tmA: W_UV in 64-column boxes of one head's 128 rows
+cudaError_t launch_combine_project(const CUtensorMap& tmA, const float* o_part, const float* lse_part,
+                                   const WsHeader* ws, void* out, void* o_lat, float* lse, int B, int Lq, int H,
+                                   int G, int slots, cudaStream_t st);
 int decode_max_units(int csize, int* units);  // clusters of csize CTAs resident at once
 
 }  // namespace mla

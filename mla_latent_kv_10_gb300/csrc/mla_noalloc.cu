@@ -40,9 +40,17 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 // Device address of the scratch array for the current device.  Looked up once
 // per device (host code cannot use the symbol itself: on the host it names a
 // stand-in object, not device memory).
+// Devices past the cache are looked up on every call (as the decode's
+// launch cache does).
 int scratch_address(void** out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MLA_ERR_CUDA;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return MLA_ERR_CUDA;
+  if (dev >= kMaxDevices) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return MLA_ERR_CUDA;
+    *out = p;
+    return MLA_OK;
+  }
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
   if (!g_scratch_ptr[dev]) {
     void* p = nullptr;

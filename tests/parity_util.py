@@ -32,12 +32,13 @@ def assert_close(got, ref, what, rel=REL_MAX, cos=COS_MIN):
     return err / max(scale, 1e-300)
 
 
-def run_gpu(case, num_splits=0, device="cuda"):
-    """Upload a case, run the four entry points, return host copies."""
+def run_gpu(case, num_splits=0, device="cuda", fused=False):
+    """Upload a case, run the four entry points (or three, with the fused
+    combine + project), return host copies."""
     t = {k: v.to(device) for k, v in case.tensors().items()}
     bufs = mla.DecodeBuffers(case.dims, device)
     mla.decode_step(case.dims, bufs, t["q_nope"], t["q_rope"], t["W_UK"], t["W_UV"], t["cache"],
-                    t["block_table"], t["seq_lens"], num_splits=num_splits)
+                    t["block_table"], t["seq_lens"], num_splits=num_splits, fused=fused)
     status = mla.mla_get_device_status(bufs.workspace)
     torch.cuda.synchronize()
     return dict(q_cat=bufs.q_cat.cpu(), o_lat=bufs.o_lat.cpu(), lse=bufs.lse.cpu(), out=bufs.out.cpu(),

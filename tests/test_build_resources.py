@@ -20,7 +20,7 @@ pytestmark = pytest.mark.skipif(shutil.which(NVCC) is None and not os.path.exist
 ENTRY = re.compile(r"Compiling entry function '([^']+)'")
 SPILL = re.compile(r"(\d+) bytes spill stores, (\d+) bytes spill loads")
 REGS = re.compile(r"Used (\d+) registers")
-HOT = ("decode_kernel", "combine_kernel", "absorb_kernel", "project_kernel")
+HOT = ("decode_kernel", "combine_kernel", "combine_project_kernel", "absorb_kernel", "project_kernel")
 
 
 def resource_report(source, tmp_path):

@@ -17,11 +17,12 @@ FULL = {
 }
 
 
+@pytest.mark.parametrize("fused", [False, True])
 @pytest.mark.parametrize("name", list(FULL))
-def test_full_size_workload(name):
+def test_full_size_workload(name, fused):
     case = workload(name)
-    got = run_gpu(case)
+    got = run_gpu(case, fused=fused)
     assert got["status"] == 0
     seqs, heads = FULL[name]
     errs = check_case(case, got, sample_pairs(case, heads, seqs))
-    print(name, {k: "%.2e" % v for k, v in errs.items()})
+    print(name, "fused" if fused else "", {k: "%.2e" % v for k, v in errs.items()})

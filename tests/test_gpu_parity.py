@@ -288,3 +288,36 @@ def test_combine_with_more_than_64_partials(B, Lq, H, lens):
     assert nslot[0] > 64, nslot
     got = dict(o_lat=bufs.o_lat.cpu(), lse=bufs.lse.cpu(), out=bufs.out.cpu())
     check_case(c, got, sample_pairs(c, 6))
+
+
+
+# ---------------------------------------------------------------- fused combine + project
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_fused_combine_project_matches_two_calls_and_oracle(name):
+    """mla_combine_project gives exactly what mla_combine_splits followed by
+    mla_project_uv gives (same merge order, same bf16 rounding of o_lat, same
+    MMA), and so matches the oracle."""
+    c = SMALL[name]()
+    two = run_gpu(c)
+    one = run_gpu(c, fused=True)
+    assert one["status"] == 0
+    assert torch.equal(one["o_lat"], two["o_lat"])
+    assert torch.equal(one["lse"], two["lse"])
+    assert torch.equal(one["out"], two["out"])
+    heads = None if c.dims["H"] <= 32 else 10
+    check_case(c, one, sample_pairs(c, heads))
+
+
+def test_fused_combine_project_without_optional_outputs():
+    """o_lat and lse are optional outputs of the fused call."""
+    c = make_case(B=3, Lq=2, H=128, seq_lens=[300, 2, 1000], table="perm", seed=48)
+    ref = run_gpu(c, fused=True)
+    t = {k: v.cuda() for k, v in c.tensors().items()}
+    bufs = mla.DecodeBuffers(c.dims)
+    mla.mla_absorb_q(c.dims, t["q_nope"], t["q_rope"], t["W_UK"], bufs.q_cat)
+    mla.mla_decode_paged(c.dims, bufs.q_cat, t["cache"], t["block_table"], t["seq_lens"], 0,
+                         bufs.o_part, bufs.lse_part, bufs.workspace)
+    mla.mla_combine_project(c.dims, bufs.o_part, bufs.lse_part, bufs.workspace, t["W_UV"], bufs.out)
+    assert mla.mla_get_device_status(bufs.workspace) == 0
+    assert torch.equal(bufs.out.cpu(), ref["out"])
