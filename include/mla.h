@@ -47,7 +47,8 @@
  * Notation (dims struct):
  *   B batch, Lq new tokens per sequence, H heads, d_hc = 128 content head dim,
  *   d_c = 512 latent width, d_R = 64 RoPE width, G latent groups (1 = MLA,
- *   2 = GLA), d_g = d_c / G latent width per group, P = page_size = 64.
+ *   2, 4 or 8 = GLA), d_g = d_c / G latent width per group, P = page_size =
+ *   64.
  *   Head h belongs to group g(h) = floor(h * G / H) (contiguous head blocks).
  *   Cache row of one token = [c_0 | ... | c_{G-1} | k_R], d_c + d_R = 576 bf16.
  */
@@ -63,12 +64,12 @@ extern "C" {
 
 typedef struct mla_dims {
   int B;                 /* batch (sequences), >= 1                          */
-  int Lq;                /* new query tokens per sequence, 1..2              */
+  int Lq;                /* new query tokens per sequence, 1..4              */
   int H;                 /* heads, multiple of 16, 16..128                   */
   int d_hc;              /* content head dim, must be 128                    */
   int d_c;               /* total latent width, must be 512                  */
   int d_R;               /* decoupled RoPE width, must be 64                 */
-  int G;                 /* latent groups: 1 (MLA) or 2 (GLA)                */
+  int G;                 /* latent groups: 1 (MLA), 2, 4 or 8 (GLA)          */
   int page_size;         /* tokens per cache page, must be 64                */
   int max_pages_per_seq; /* row length of block_table                        */
   int num_pages;         /* physical pages in the cache                      */

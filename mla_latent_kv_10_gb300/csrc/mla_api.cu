@@ -51,8 +51,8 @@ int check_dims(const mla_dims* d) {
   if (!(d->scale > 0.f) || !std::isfinite(d->scale)) return MLA_ERR_INVALID_ARG;
   if (d->d_hc != kDhc || d->d_c != kDc || d->d_R != kDr || d->page_size != kPage)
     return MLA_ERR_UNSUPPORTED;
-  if (d->G != 1 && d->G != 2) return MLA_ERR_UNSUPPORTED;
-  if (d->Lq > 2 || d->H % 16 != 0 || d->H > 128 || d->H % d->G != 0) return MLA_ERR_UNSUPPORTED;
+  if (d->G != 1 && d->G != 2 && d->G != 4 && d->G != 8) return MLA_ERR_UNSUPPORTED;
+  if (d->Lq > 4 || d->H % 16 != 0 || d->H > 128 || d->H % d->G != 0) return MLA_ERR_UNSUPPORTED;
   // TMA row coordinate page*64 and table indices stay in int32
   if ((long long)d->num_pages * kPage >= (1LL << 31)) return MLA_ERR_UNSUPPORTED;
   if ((long long)d->B * d->max_pages_per_seq >= (1LL << 31)) return MLA_ERR_UNSUPPORTED;

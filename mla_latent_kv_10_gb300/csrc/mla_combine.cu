@@ -113,9 +113,9 @@ __global__ void __launch_bounds__(kCombineThreads, 1)
     combine_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part,
                    const WsHeader* __restrict__ ws, __nv_bfloat16* __restrict__ o_lat,
                    float* __restrict__ lse_out, int B, int Lq, int H, int G, int slots) {
-  constexpr int kCols = kCombineCols;  // columns of this CTA
+  constexpr int kCols = DG < kCombineCols ? DG : kCombineCols;  // columns of this CTA
   constexpr int kWarps = kCombineThreads / 32;
-  static_assert(DG % kCols == 0, "latent slice in whole CTA column ranges");
+  static_assert(DG % kCols == 0 && (kCols / 4) % (kCombineThreads / 32) == 0, "latent slice in whole CTA column ranges");
   __shared__ __align__(16) __nv_bfloat16 tile[kCombineRows][kCols + 8];
   __shared__ float wts[kCombineMaxSeg][kCombineRows];
   __shared__ float lrow[kCombineRows];
@@ -307,20 +307,23 @@ __global__ void __launch_bounds__(kCpThreads, 1)
 
   // ---- merge the CTA's rows into the B tile
   if (plan_ok) {
-    constexpr int kLaneChunks = DG / 8 / 32;  // 8-column chunks per lane and row (2 or 1)
+    // 8-column chunks per lane and row: 2 or 1 (a 128- or 64-wide group latent
+    // has fewer chunks than lanes; the spare lanes repeat chunks, which
+    // writes the same values twice)
+    constexpr int kLaneChunks = DG >= 256 ? DG / 8 / 32 : 1;
 #pragma unroll 1
     for (int rr = warp; rr < mt; rr += kWarps) {
       const int m = m0 + rr, row = (m % Lq) * H + h;
       const int bi = m / Lq - b0;
       int chs[kLaneChunks];
 #pragma unroll
-      for (int i = 0; i < kLaneChunks; ++i) chs[i] = g * (DG / 8) + lane + 32 * i;
+      for (int i = 0; i < kLaneChunks; ++i) chs[i] = g * (DG / 8) + (lane + 32 * i) % (DG / 8);
       float4 acc[kLaneChunks][2];
       float L;
       merge_row(plan_s0[bi], plan_n[bi], o_part, lse_part, row, rows, chs, acc, L);
 #pragma unroll
       for (int i = 0; i < kLaneChunks; ++i) {
-        const int ch = lane + 32 * i, box = ch >> 3, c8 = ch & 7;
+        const int ch = (lane + 32 * i) % (DG / 8), box = ch >> 3, c8 = ch & 7;
         const uint32_t w0 = pack_bf16x2(acc[i][0].x, acc[i][0].y), w1 = pack_bf16x2(acc[i][0].z, acc[i][0].w);
         const uint32_t w2 = pack_bf16x2(acc[i][1].x, acc[i][1].y), w3 = pack_bf16x2(acc[i][1].z, acc[i][1].w);
         const uint32_t dst = sB + box * boxB + rr * 128 + ((c8 ^ (rr & 7)) << 4);
@@ -379,6 +382,33 @@ __global__ void __launch_bounds__(kCpThreads, 1)
   }
 }
 
+template <int DG>
+cudaError_t launch_combine_dg(const float* o_part, const float* lse_part, const WsHeader* ws, __nv_bfloat16* ol,
+                              float* lse, int B, int Lq, int H, int G, int slots, cudaStream_t st) {
+  constexpr int kCols = DG < kCombineCols ? DG : kCombineCols;
+  dim3 grid(B, (Lq * H + kCombineRows - 1) / kCombineRows, DG / kCols), block(kCombineThreads);
+  combine_kernel<DG><<<grid, block, 0, st>>>(o_part, lse_part, ws, ol, lse, B, Lq, H, G, slots);
+  return cudaGetLastError();
+}
+template <int DG>
+cudaError_t launch_combine_project_dg(const CUtensorMap& tmA, const float* o_part, const float* lse_part,
+                                      const WsHeader* ws, __nv_bfloat16* o, __nv_bfloat16* ol, float* lse, int B,
+                                      int Lq, int H, int G, int slots, cudaStream_t st) {
+  const int M = B * Lq;
+  const int mt = M < kCpRows ? M : kCpRows;
+  const int N = (mt + 15) / 16 * 16;
+  dim3 grid(H, (M + kCpRows - 1) / kCpRows);
+  const int smem = (DG / 64) * kDhc * 64 * 2 + N * DG * 2 + 1024;
+  const int smem_max = (DG / 64) * kDhc * 64 * 2 + kCpRows * DG * 2 + 1024;
+  cudaError_t e = cudaFuncSetAttribute(combine_project_kernel<DG>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
+  if (e != cudaSuccess) return e;
+  // launched plainly (like the combine): chained, its CTAs wait on the SMs
+  // of work units that finished early, and the step measured slower
+  combine_project_kernel<DG><<<grid, kCpThreads, smem, st>>>(tmA, o_part, lse_part, ws, o, ol, lse, B, Lq, H, G,
+                                                             slots, N);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 // The combine is launched plainly, not chained to the decode: chained, its
@@ -388,37 +418,28 @@ __global__ void __launch_bounds__(kCpThreads, 1)
 // chained.)
 cudaError_t launch_combine(const float* o_part, const float* lse_part, const WsHeader* ws, void* o_lat,
                            float* lse, int B, int Lq, int H, int G, int slots, cudaStream_t st) {
-  const int d_g = kDc / G;
-  dim3 grid(B, (Lq * H + kCombineRows - 1) / kCombineRows, d_g / kCombineCols), block(kCombineThreads);
   auto* ol = static_cast<__nv_bfloat16*>(o_lat);
-  if (G == 1) combine_kernel<512><<<grid, block, 0, st>>>(o_part, lse_part, ws, ol, lse, B, Lq, H, G, slots);
-  else combine_kernel<256><<<grid, block, 0, st>>>(o_part, lse_part, ws, ol, lse, B, Lq, H, G, slots);
-  return cudaGetLastError();
+  switch (kDc / G) {
+    case 512: return launch_combine_dg<512>(o_part, lse_part, ws, ol, lse, B, Lq, H, G, slots, st);
+    case 256: return launch_combine_dg<256>(o_part, lse_part, ws, ol, lse, B, Lq, H, G, slots, st);
+    case 128: return launch_combine_dg<128>(o_part, lse_part, ws, ol, lse, B, Lq, H, G, slots, st);
+    case 64: return launch_combine_dg<64>(o_part, lse_part, ws, ol, lse, B, Lq, H, G, slots, st);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t launch_combine_project(const CUtensorMap& tmA, const float* o_part, const float* lse_part,
                                    const WsHeader* ws, void* out, void* o_lat, float* lse, int B, int Lq, int H,
                                    int G, int slots, cudaStream_t st) {
-  const int d_g = kDc / G, M = B * Lq;
-  const int mt = M < kCpRows ? M : kCpRows;
-  const int N = (mt + 15) / 16 * 16;
-  dim3 grid(H, (M + kCpRows - 1) / kCpRows), block(kCpThreads);
-  const int smem = (d_g / 64) * kDhc * 64 * 2 + N * d_g * 2 + 1024;
-  const int smem_max = (d_g / 64) * kDhc * 64 * 2 + kCpRows * d_g * 2 + 1024;
   auto* o = static_cast<__nv_bfloat16*>(out);
   auto* ol = static_cast<__nv_bfloat16*>(o_lat);
-  // launched plainly (like the combine): chained, its CTAs wait on the SMs
-  // of work units that finished early, and the step measured slower
-  if (d_g == 512) {
-    cudaError_t e = cudaFuncSetAttribute(combine_project_kernel<512>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
-    if (e != cudaSuccess) return e;
-    combine_project_kernel<512><<<grid, kCpThreads, smem, st>>>(tmA, o_part, lse_part, ws, o, ol, lse, B, Lq, H, G, slots, N);
-  } else {
-    cudaError_t e = cudaFuncSetAttribute(combine_project_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
-    if (e != cudaSuccess) return e;
-    combine_project_kernel<256><<<grid, kCpThreads, smem, st>>>(tmA, o_part, lse_part, ws, o, ol, lse, B, Lq, H, G, slots, N);
+  switch (kDc / G) {
+    case 512: return launch_combine_project_dg<512>(tmA, o_part, lse_part, ws, o, ol, lse, B, Lq, H, G, slots, st);
+    case 256: return launch_combine_project_dg<256>(tmA, o_part, lse_part, ws, o, ol, lse, B, Lq, H, G, slots, st);
+    case 128: return launch_combine_project_dg<128>(tmA, o_part, lse_part, ws, o, ol, lse, B, Lq, H, G, slots, st);
+    case 64: return launch_combine_project_dg<64>(tmA, o_part, lse_part, ws, o, ol, lse, B, Lq, H, G, slots, st);
+    default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 }  // namespace mla

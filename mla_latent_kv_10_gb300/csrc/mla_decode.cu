@@ -227,6 +227,7 @@ struct DecodeShared {
   int abort;
   int peer_sent[4];              // pages the peer's exchange warp of each quadrant sent here (teardown)
   int lens[kPlanInKernelMaxB];   // validated sequence lengths (in-kernel plan)
+  int16_t qsrc[kSoftmaxThreads][2];  // softmax thread's q_cat column of each latent chunk (-1: zeros)
 };
 
 // All shared memory is dynamic: stage ring, exchange slots, then the small state.
@@ -681,10 +682,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             }
             if (lane == 0) {
               if (pc == 0) {  // the first segment's query, ahead of its first page
+                // latent boxes of 64 columns: this CTA's half of the latent
+                // (one group), or the first columns of each row's own
+                // group latent (several groups)
                 const int qy = sb * a.Lq * a.H + (int)rg * kRowsPerCta;
                 const int qx = a.G == 1 ? (int)r * 256 : 0;
-                mbar_arrive_expect_tx(bar(sh.q_lat), 4 * kQBoxBytes + kQRopeBytes);
-                for (int q = 0; q < 4; ++q)
+                const int nbox = a.G == 1 ? 4 : min(a.d_g, 256) / 64;
+                mbar_arrive_expect_tx(bar(sh.q_lat), nbox * kQBoxBytes + kQRopeBytes);
+                for (int q = 0; q < nbox; ++q)
                   tma_load_2d(xsend + q * kQBoxBytes, &tm_qlat, bar(sh.q_lat), qx + 64 * q, qy);
                 tma_load_2d(qrope, &tm_qrope, bar(sh.q_lat), a.d_g + 32 * (int)r, qy);
               }
@@ -868,6 +873,18 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     const int l = valid ? grow / a.H : 0;
     const int h = valid ? grow % a.H : 0;
     const int g = (h * a.G) / a.H;
+    // The CTA's latent half holds columns 256r .. 256r + 255 of the cache
+    // row; this thread fills tensor-memory columns for two 64-column chunks
+    // of it (128 * half + 64 * c).  A chunk inside the row's group latent
+    // (columns g*d_g .. (g+1)*d_g - 1) takes the query's values from column
+    // src_col(c) of its q_cat row; any other chunk is zero, so heads of
+    // other groups score nothing against this half.
+    // (kept in shared memory: the softmax loop has no registers to spare)
+    for (int c = 0; c < 2; ++c) {
+      const int col = 256 * (int)r + 128 * half + 64 * c - g * a.d_g;
+      sh.qsrc[threadIdx.x][c] = (int16_t)((valid && col >= 0 && col < a.d_g) ? col : -1);
+    }
+    auto src_col = [&sh](int c) -> int { return sh.qsrc[threadIdx.x][c]; };
     const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
     const uint32_t pair_bar = kBarPair0 + quad;
     const bool leader = (threadIdx.x == 0);
@@ -885,18 +902,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         tma_load_2d(qrope, &tm_qrope, bar(sh.q_tma), a.d_g + 32 * (int)r, b * a.Lq * a.H + (int)rg * kRowsPerCta);
         ++nq_tma;
       }
-      const uint4* lat = nullptr;
-      if (valid) {
-        const __nv_bfloat16* qrow = qrow_of(b);
-        if (a.G == 1) lat = reinterpret_cast<const uint4*>(qrow + r * 256 + 128 * half);
-        else if ((uint32_t)g == r) lat = reinterpret_cast<const uint4*>(qrow + 128 * half);
-      }
 #pragma unroll 1
       for (int c = 0; c < 2; ++c) {  // 32 columns (64 bf16) per round trip
+        const int sc = src_col(c);
+        const uint4* lat = sc >= 0 ? reinterpret_cast<const uint4*>(qrow_of(b) + sc) : nullptr;
         uint32_t w[32];
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          const uint4 v = lat ? lat[8 * c + k] : make_uint4(0, 0, 0, 0);
+          const uint4 v = lat ? lat[k] : make_uint4(0, 0, 0, 0);
           w[4 * k + 0] = v.x; w[4 * k + 1] = v.y; w[4 * k + 2] = v.z; w[4 * k + 3] = v.w;
         }
         tmem_st32(lane_base + kColQ + 64 * half + 32 * c, w);
@@ -909,11 +922,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     auto prefetch_q = [&](int b) {
       if (!valid) return;
       const char* qrow = reinterpret_cast<const char*>(qrow_of(b));
-      if (a.G == 1 || (uint32_t)g == r) {
-        const char* lat = qrow + (a.G == 1 ? r * 512 : 0) + half * 256;
-        asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(lat));
-        asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(lat + 128));
-      }
+      // the latent columns this thread will load (its group's, or for one
+      // group this CTA's half)
+      const char* lat = qrow + (a.G == 1 ? r * 512 + half * 256 : 0);
+      asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(lat));
+      asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(lat + 128));
       if (half == 0) asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(qrow + a.d_g * 2 + 64 * r));
     };
     auto prefetch_after = [&](const SegIter& at) {  // the sequence after the segment `at` just produced
@@ -928,15 +941,18 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       ok = mbar_wait(bar(sh.q_lat), 0, abort, lim);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) return;
-      const bool use = valid && (a.G == 1 || (uint32_t)g == r);
 #pragma unroll 1
       for (int c = 0; c < 2; ++c) {
         uint32_t w[32];
-        const uint32_t src = xsend + (2 * half + c) * kQBoxBytes + row * 128;
+        // the box that holds the chunk (the TMA loaded this CTA's half for
+        // one group, or the first columns of each row's group latent)
+        const int sc = src_col(c);
+        const int box = sc < 0 ? 0 : (a.G == 1 ? (sc - 256 * (int)r) / 64 : sc / 64);
+        const uint32_t src = xsend + box * kQBoxBytes + row * 128;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           ld_shared_v4(src + ((k ^ (row & 7)) << 4), w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
-          if (!use) w[4 * k] = w[4 * k + 1] = w[4 * k + 2] = w[4 * k + 3] = 0u;
+          if (sc < 0) w[4 * k] = w[4 * k + 1] = w[4 * k + 2] = w[4 * k + 3] = 0u;
         }
         tmem_st32(lane_base + kColQ + 64 * half + 32 * c, w);
       }
@@ -956,8 +972,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     uint32_t q = 0;
     while (cur.valid) {
       const uint32_t b = q & 1;
-      PageCursor nx = cur;
-      nx.advance(a);
       if (cur.seg_first()) {
         m_used = -INFINITY;
         l_part = 0.f;
@@ -1051,10 +1065,15 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         }
       }
       // every QK of this segment is done (S(q) was complete): the next
-      // segment's query may replace it
-      if (nx.valid && nx.seg_first()) {
-        load_q(nx.sb);
-        prefetch_after(nx.it);
+      // segment's query, if there is one, may replace it (the cursor copy
+      // lives only here, so it costs no registers across the loop)
+      if (cur.seg_last()) {
+        PageCursor nx = cur;
+        nx.advance(a);
+        if (nx.valid) {
+          load_q(nx.sb);
+          prefetch_after(nx.it);
+        }
       }
 
       // ---- end of segment: normalised latent partial and log-sum-exp
@@ -1090,7 +1109,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           tc_fence_before();
         }
       }
-      cur = nx;
+      cur.advance(a);
       ++q;
     }
     if (!ok) fail();
@@ -1273,7 +1292,7 @@ namespace {
 constexpr int kCachedDevices = 64;
 struct DecodeDeviceInfo {
   bool smem_set;
-  int units[2];  // clusters of 2 and of 4 CTAs; 0 = not known yet
+  int units[4];  // clusters of 2, 4, 6 and 8 CTAs; 0 = not known yet
 };
 std::mutex g_decode_mu;
 DecodeDeviceInfo g_decode_info[kCachedDevices];
@@ -1315,7 +1334,8 @@ static cudaError_t decode_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* a
 }
 
 int decode_max_units(int csize, int* units) {
-  const int slot = csize == 2 ? 0 : 1;
+  const int slot = csize / 2 - 1;
+  if (slot < 0 || slot > 3) return MLA_ERR_UNSUPPORTED;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_CUDA;
   const bool cached = dev >= 0 && dev < kCachedDevices;

@@ -8,8 +8,8 @@
 //   project: out[m,h,:]       = W_UV[h] . o_lat[m,h,:]        (M x d_g x 128 per head)
 //
 // m runs over the B*Lq query rows.  absorb: one CTA per (head, 128-row
-// block, 256 output columns); project: one CTA per (head, 128-row block,
-// 64 output columns).
+// block, up to 256 output columns); project: one CTA per (head, 128-row
+// block, 64 output columns).
 // Rows past M are zero-filled by the tensor copies and never stored.
 #include "mla_internal.h"
 #include "ptx.cuh"
@@ -39,16 +39,18 @@ __device__ __forceinline__ void store_row32_bf16(__nv_bfloat16* dst, const uint3
 constexpr int kBox = 16384;  // one 128 x 64 bf16 tile, 128-byte swizzled
 
 // ---------------------------------------------------------------- absorb
-// A = q_nope rows (K-major, 2 tiles of 64 k), B = 256 columns of W_UK[h]
-// (d rows x c columns, N-contiguous, i.e. MN-major: 4 tiles of 128 d x 64
-// c).  Two CTAs per head and per SM, all resident at once: the weight
-// loads of one overlap the MMAs and stores of the other.
+// A = q_nope rows (K-major, 2 tiles of 64 k), B = kCols = min(256, d_g)
+// columns of W_UK[h] (d rows x c columns, N-contiguous, i.e. MN-major:
+// kCols/64 tiles of 128 d x 64 c).  Two CTAs per SM, all resident at once:
+// the weight loads of one overlap the MMAs and stores of the other.
 constexpr int kAbsorbCols = 256;
+__host__ __device__ constexpr int absorb_cols(int dg) { return dg < kAbsorbCols ? dg : kAbsorbCols; }
 template <int DG>
 __global__ void __launch_bounds__(128)
     absorb_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const __nv_bfloat16* __restrict__ q_rope, __nv_bfloat16* __restrict__ q_cat,
                   int M, int H) {
+  constexpr int kCols = absorb_cols(DG);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint8_t* sA = smem;
@@ -56,7 +58,7 @@ __global__ void __launch_bounds__(128)
   __shared__ __align__(8) uint64_t bars[2];
   __shared__ uint32_t tmem_holder;
   __shared__ int abort_flag;
-  const int h = blockIdx.x, m0 = blockIdx.y * kRowsPerCta, n0 = blockIdx.z * kAbsorbCols;
+  const int h = blockIdx.x, m0 = blockIdx.y * kRowsPerCta, n0 = blockIdx.z * kCols;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t full = smem_u32(&bars[0]), done = smem_u32(&bars[1]);
   if (threadIdx.x == 0) {
@@ -67,10 +69,10 @@ __global__ void __launch_bounds__(128)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     // the weight tiles do not depend on the kernel before: start them now
-    for (int nb = 0; nb < kAbsorbCols / 64; ++nb) tma_prefetch_l2_3d(&tmB, n0 + nb * 64, 0, h);
+    for (int nb = 0; nb < kCols / 64; ++nb) tma_prefetch_l2_3d(&tmB, n0 + nb * 64, 0, h);
   }
   if (warp == 0) {
-    tmem_alloc(smem_u32(&tmem_holder), kAbsorbCols);
+    tmem_alloc(smem_u32(&tmem_holder), kCols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -82,13 +84,13 @@ __global__ void __launch_bounds__(128)
   griddep_launch_dependents();
 
   if (threadIdx.x == 0) {
-    mbar_arrive_expect_tx(full, 2 * kBox + (kAbsorbCols / 64) * kBox);
-    for (int nb = 0; nb < kAbsorbCols / 64; ++nb)
+    mbar_arrive_expect_tx(full, 2 * kBox + (kCols / 64) * kBox);
+    for (int nb = 0; nb < kCols / 64; ++nb)
       tma_load_3d(smem_u32(sB + nb * kBox), &tmB, full, n0 + nb * 64, 0, h);
     for (int kb = 0; kb < 2; ++kb) tma_load_3d(smem_u32(sA + kb * kBox), &tmA, full, kb * 64, h, m0);
     if (mbar_wait(full, 0, &abort_flag)) {
       tc_fence_after();
-      constexpr uint32_t idesc = idesc_bf16(128, kAbsorbCols, false, true);
+      constexpr uint32_t idesc = idesc_bf16(128, kCols, false, true);
 #pragma unroll
       for (int j = 0; j < 8; ++j) {  // K = 128 in steps of 16
         const uint64_t ad = sdesc_sw128(smem_u32(sA) + (j >> 2) * kBox + (j & 3) * 32, 16, 1024);
@@ -107,7 +109,7 @@ __global__ void __launch_bounds__(128)
     const int row = warp * 32 + lane, m = m0 + row;
     __nv_bfloat16* dst = q_cat + ((size_t)m * H + h) * (DG + kDr);
 #pragma unroll 1
-    for (int c = 0; c < kAbsorbCols / 32; ++c) {
+    for (int c = 0; c < kCols / 32; ++c) {
       uint32_t r[32];
       tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + c * 32, r);
       tmem_wait_ld();
@@ -124,7 +126,7 @@ __global__ void __launch_bounds__(128)
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, kAbsorbCols);
+    tmem_dealloc(tmem, kCols);
   }
 }
 
@@ -234,39 +236,49 @@ cudaError_t set_smem(K kernel, int bytes) {
 
 }  // namespace
 
+template <int DG>
+cudaError_t launch_absorb_dg(const CUtensorMap& tmA, const CUtensorMap& tmB, const __nv_bfloat16* qr,
+                             __nv_bfloat16* qc, int M, int H, cudaStream_t st) {
+  constexpr int kCols = absorb_cols(DG);
+  dim3 grid(H, (M + kRowsPerCta - 1) / kRowsPerCta, DG / kCols), block(128);
+  const int smem = 2 * kBox + (kCols / 64) * kBox + 1024;
+  cudaError_t e = set_smem(absorb_kernel<DG>, smem);
+  if (e != cudaSuccess) return e;
+  return launch_chained(absorb_kernel<DG>, grid, block, smem, st, tmA, tmB, qr, qc, M, H);
+}
+template <int DG>
+cudaError_t launch_project_dg(const CUtensorMap& tmA, const CUtensorMap& tmB, __nv_bfloat16* o, int M, int H,
+                              cudaStream_t st) {
+  dim3 grid(H, (M + kRowsPerCta - 1) / kRowsPerCta, kDhc / kProjectCols), block(128);
+  const int smem = 4 * (kBox + kProjectCols * 64 * 2) + 1024;
+  cudaError_t e = set_smem(project_kernel<DG>, smem);
+  if (e != cudaSuccess) return e;
+  return launch_chained(project_kernel<DG>, grid, block, smem, st, tmA, tmB, o, M, H);
+}
+
 cudaError_t launch_absorb(const CUtensorMap& tmA, const CUtensorMap& tmB, const void* q_rope,
                           void* q_cat, int M, int H, int d_g, cudaStream_t st) {
-  dim3 grid(H, (M + kRowsPerCta - 1) / kRowsPerCta, d_g / kAbsorbCols), block(128);
   const auto* qr = static_cast<const __nv_bfloat16*>(q_rope);
   auto* qc = static_cast<__nv_bfloat16*>(q_cat);
-  const int smem = 2 * kBox + (kAbsorbCols / 64) * kBox + 1024;
-  if (d_g == 512) {
-    cudaError_t e = set_smem(absorb_kernel<512>, smem);
-    if (e != cudaSuccess) return e;
-    return launch_chained(absorb_kernel<512>, grid, block, smem, st, tmA, tmB, qr, qc, M, H);
-  } else {
-    cudaError_t e = set_smem(absorb_kernel<256>, smem);
-    if (e != cudaSuccess) return e;
-    return launch_chained(absorb_kernel<256>, grid, block, smem, st, tmA, tmB, qr, qc, M, H);
+  switch (d_g) {
+    case 512: return launch_absorb_dg<512>(tmA, tmB, qr, qc, M, H, st);
+    case 256: return launch_absorb_dg<256>(tmA, tmB, qr, qc, M, H, st);
+    case 128: return launch_absorb_dg<128>(tmA, tmB, qr, qc, M, H, st);
+    case 64: return launch_absorb_dg<64>(tmA, tmB, qr, qc, M, H, st);
+    default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 cudaError_t launch_project(const CUtensorMap& tmA, const CUtensorMap& tmB, void* out, int M, int H,
                            int d_g, cudaStream_t st) {
-  dim3 grid(H, (M + kRowsPerCta - 1) / kRowsPerCta, kDhc / kProjectCols), block(128);
-  const int smem = 4 * (kBox + kProjectCols * 64 * 2) + 1024;
   auto* o = static_cast<__nv_bfloat16*>(out);
-  if (d_g == 512) {
-    cudaError_t e = set_smem(project_kernel<512>, smem);
-    if (e != cudaSuccess) return e;
-    return launch_chained(project_kernel<512>, grid, block, smem, st, tmA, tmB, o, M, H);
-  } else {
-    cudaError_t e = set_smem(project_kernel<256>, smem);
-    if (e != cudaSuccess) return e;
-    return launch_chained(project_kernel<256>, grid, block, smem, st, tmA, tmB, o, M, H);
+  switch (d_g) {
+    case 512: return launch_project_dg<512>(tmA, tmB, o, M, H, st);
+    case 256: return launch_project_dg<256>(tmA, tmB, o, M, H, st);
+    case 128: return launch_project_dg<128>(tmA, tmB, o, M, H, st);
+    case 64: return launch_project_dg<64>(tmA, tmB, o, M, H, st);
+    default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 }  // namespace mla

@@ -91,7 +91,7 @@ def test_decode_rejects_index_overflow(lib):
 
 @pytest.mark.parametrize("field,value,code", [
     ("d_hc", 64, -2), ("d_c", 256, -2), ("d_R", 32, -2), ("page_size", 16, -2),
-    ("G", 4, -2), ("Lq", 3, -2), ("H", 24, -2), ("H", 256, -2),
+    ("G", 3, -2), ("G", 16, -2), ("Lq", 5, -2), ("H", 24, -2), ("H", 256, -2),
     ("B", 0, -1), ("num_pages", 0, -1), ("scale", 0.0, -1), ("scale", float("nan"), -1),
     ("max_pages_per_seq", 0, -1)])
 def test_unsupported_or_invalid_dims(lib, field, value, code):

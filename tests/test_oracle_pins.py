@@ -319,7 +319,7 @@ def _brute_force(c, b, h):
 
 
 @pytest.mark.parametrize("B,Lq,H,G,lens", [(2, 1, 16, 1, [1, 70]), (2, 2, 16, 1, [2, 67]),
-                                           (1, 1, 32, 2, [130])])
+                                           (1, 1, 32, 2, [130]), (1, 3, 32, 4, [131]), (2, 4, 16, 8, [4, 66])])
 def test_oracle_matches_brute_force(B, Lq, H, G, lens):
     """Tiny inputs spanning one to three pages of a shuffled table: the oracle
     equals the key-by-key definition to fp64 rounding."""
@@ -432,7 +432,8 @@ def _brute_force_latent(c, q_cat, b, h):
 
 
 @pytest.mark.parametrize("B,Lq,H,G,lens,mag", [(2, 1, 16, 1, [1, 70], 1.0), (2, 2, 16, 1, [2, 67], 32.0),
-                                               (1, 1, 32, 2, [130], 16.0)])
+                                               (1, 1, 32, 2, [130], 16.0), (1, 4, 32, 4, [131], 8.0),
+                                               (2, 1, 16, 8, [5, 66], 1.0)])
 def test_latent_decode_matches_brute_force(B, Lq, H, G, lens, mag):
     """Tiny inputs over one to three shuffled pages, including queries whose
     scores reach the hundreds: the latent decode equals the key-by-key
@@ -472,3 +473,24 @@ def test_bf16_absorbed_query_limits_accuracy_at_large_logits():
     assert cos1 > 0.99999 and err1 < 5e-3
     cos32, err32 = cos_after_rounding(32.0)
     assert cos32 < 0.9999 and err32 > 2e-2
+
+
+
+@pytest.mark.parametrize("G", [4, 8])
+def test_grouped_latent_isolation_many_groups(G):
+    """G groups of H/G heads: changing latent slice j of the cache moves
+    exactly the heads of group j (contiguous blocks of H/G heads)."""
+    H = 32
+    c = make_case(B=1, Lq=1, H=H, G=G, seq_lens=[70], table="perm", seed=17 + G)
+    out_a, _, _ = oracle.decode(c.dims, **c.tensors())
+    d_g = D_C // G
+    for j in (0, G - 1):
+        cache2 = c.cache.clone()
+        cache2[:, :, j * d_g:(j + 1) * d_g] = torch.randn(cache2[:, :, j * d_g:(j + 1) * d_g].shape).to(torch.bfloat16)
+        t = c.tensors()
+        t.update(cache=cache2)
+        out_b, _, _ = oracle.decode(c.dims, **t)
+        moved = np.abs(out_a - out_b).max(axis=-1)[0, 0] > 1e-6
+        expect = np.zeros(H, dtype=bool)
+        expect[j * (H // G):(j + 1) * (H // G)] = True
+        np.testing.assert_array_equal(moved, expect)
