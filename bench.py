@@ -55,16 +55,29 @@ WORKLOAD_TEXT = {
 }
 
 
+DECODE_SOURCES = ("mla_latent_kv_10_gb300/csrc/mla_decode.cu", "mla_latent_kv_10_gb300/csrc/ptx.cuh",
+                  "mla_latent_kv_10_gb300/csrc/mla_internal.h", "include/mla.h")
+
+
+def decode_source_sha():
+    """sha256 over the decode kernel's translation unit: its .cu and every
+    header of this repository it includes, in a fixed order."""
+    import hashlib
+    h = hashlib.sha256()
+    for rel in DECODE_SOURCES:
+        h.update(rel.encode())
+        h.update(open(os.path.join(ROOT, rel), "rb").read())
+    return h.hexdigest()
+
+
 def decode_traffic(workload):
     """DRAM bytes per decode launch from the committed ncu summary of this
-    workload, if it was taken on the current decode source (else None)."""
-    import hashlib
+    workload, if it was taken on the current decode sources (else None)."""
     path = os.path.join(ROOT, "profiles", "decode_kernel_%s.json" % workload)
     if not os.path.exists(path):
         return None
     rec = json.load(open(path))
-    src = os.path.join(ROOT, rec["source"])
-    if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest() != rec["source_sha256"]:
+    if rec.get("sources_sha256") != decode_source_sha():
         return None
     return rec["dram_bytes_per_launch"]
 
