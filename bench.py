@@ -4,8 +4,9 @@ A step is the whole hot path on one batch of synthetic input:
     mla_absorb_q -> mla_decode_paged -> mla_combine_splits -> mla_project_uv
 (--fused runs mla_combine_project, the merge inside the W_UV projection,
 instead of the last two; it measured slightly slower in the step.)
-(mla_decode_paged is one kernel launch for B <= 448: the decode kernel
-computes its own split; larger batches add a plan kernel before it.)
+(mla_decode_paged is one kernel launch for B <= 448, or B <= 352 with
+grouped latents: the decode kernel computes its own split; larger batches
+add a plan kernel before it.)
 Each step is one CUDA-graph replay (the kernels chain by programmatic
 dependent launch); the decode kernel is also timed alone, by events around
 replays of a graph holding only it.

@@ -118,8 +118,9 @@ int mla_decode_num_slots(const mla_dims* dims, int* slots);
 
 /*
  * Number of kernels one mla_decode_paged call with these dims launches: 1
- * when B <= 448 (the decode kernel computes its own split of the work), 2
- * above that (a plan kernel runs first).  Host-only, launches nothing.
+ * when B <= 448 for G = 1, B <= 352 for G > 1 (the decode kernel computes
+ * its own split of the work, one sequence per thread), 2 above that (a plan
+ * kernel runs first).  Host-only, launches nothing.
  */
 int mla_decode_kernel_launches(const mla_dims* dims, int* launches);
 

@@ -159,7 +159,7 @@ int mla_decode_num_slots(const mla_dims* d, int* slots) {
   if (rc != MLA_OK) return rc;
   if (!slots) return MLA_ERR_INVALID_ARG;
   int units = 0;
-  if ((rc = decode_max_units(2 * row_blocks(d), &units)) != MLA_OK) return rc;
+  if ((rc = decode_max_units(decode_solo(d->G), decode_csize(d->Lq, d->H, d->G), &units)) != MLA_OK) return rc;
   *slots = d->B + units - 1;
   return MLA_OK;
 }
@@ -168,7 +168,7 @@ int mla_decode_kernel_launches(const mla_dims* d, int* launches) {
   int rc = check_dims(d);
   if (rc != MLA_OK) return rc;
   if (!launches) return MLA_ERR_INVALID_ARG;
-  *launches = d->B <= kPlanInKernelMaxB ? 1 : 2;
+  *launches = d->B <= decode_plan_max_b(d->G) ? 1 : 2;
   return MLA_OK;
 }
 
@@ -184,9 +184,10 @@ int mla_decode_paged(const mla_dims* d, const void* q_cat, const void* kv_cache,
       (reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u) ||
       (reinterpret_cast<uintptr_t>(lse_part) & 3u))
     return MLA_ERR_MISALIGNED;
-  const int csize = 2 * row_blocks(d);
+  const bool solo = decode_solo(d->G);
+  const int csize = decode_csize(d->Lq, d->H, d->G);
   int units = 0;
-  if ((rc = decode_max_units(csize, &units)) != MLA_OK) return rc;
+  if ((rc = decode_max_units(solo, csize, &units)) != MLA_OK) return rc;
   if (num_splits > 0 && num_splits < units) units = num_splits;
   auto st = static_cast<cudaStream_t>(stream);
   CUtensorMap tm, tm_rope, tm_qrope, tm_qlat;
@@ -203,7 +204,8 @@ int mla_decode_paged(const mla_dims* d, const void* q_cat, const void* kv_cache,
     const int d_q = kDc / d->G + kDr;
     cuuint64_t dims[2] = {(cuuint64_t)d_q, (cuuint64_t)d->B * d->Lq * d->H};
     cuuint64_t strides[1] = {(cuuint64_t)d_q * 2};
-    cuuint32_t box[2] = {32, kRowsPerCta};
+    // RoPE query boxes: 128 rows (pair mode) or the H/2 heads of one token (solo mode)
+    cuuint32_t box[2] = {32, solo ? (cuuint32_t)(d->H / 2) : (cuuint32_t)kRowsPerCta};
     if ((rc = make_map(&tm_qrope, q_cat, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B)) != MLA_OK) return rc;
     cuuint32_t lbox[2] = {64, kRowsPerCta};
     if ((rc = make_map(&tm_qlat, q_cat, 2, dims, strides, lbox)) != MLA_OK) return rc;
@@ -211,7 +213,7 @@ int mla_decode_paged(const mla_dims* d, const void* q_cat, const void* kv_cache,
   auto* ws = static_cast<WsHeader*>(workspace);
   // Small batches are split by the decode kernel itself (one launch);
   // larger ones by the separate plan kernel.
-  const bool in_kernel = d->B <= kPlanInKernelMaxB;
+  const bool in_kernel = d->B <= decode_plan_max_b(d->G);
   if (!in_kernel) {
     cudaError_t e = launch_plan(seq_lens, block_table, ws, d->B, d->Lq, d->max_pages_per_seq,
                                 d->num_pages, units, st);
@@ -238,7 +240,7 @@ int mla_decode_paged(const mla_dims* d, const void* q_cat, const void* kv_cache,
   a.seq_lens = seq_lens;
   a.wait_ns = decode_wait_limit_ns();
   a.stall_page = decode_stall_page();
-  return cuda_status(launch_decode(tm, tm_rope, tm_qrope, tm_qlat, a, units, csize, st));
+  return cuda_status(launch_decode(solo, tm, tm_rope, tm_qrope, tm_qlat, a, units, csize, st));
 }
 
 int mla_combine_splits(const mla_dims* d, const float* o_part, const float* lse_part,

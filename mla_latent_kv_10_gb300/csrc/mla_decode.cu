@@ -72,32 +72,50 @@ namespace {
 constexpr int kStages = 4;
 constexpr int kBoxBytes = kPage * 64 * 2;       // 64 tokens x 64 bf16 = 8 KiB, 128-byte swizzle
 constexpr int kRopeBoxBytes = kPage * 32 * 2;   // 64 tokens x 32 bf16 = 4 KiB, 64-byte swizzle
-constexpr int kStageBytes = 4 * kBoxBytes + kRopeBoxBytes;  // latent half + this CTA's RoPE half
 constexpr int kXRowBytes = kPage * 2;           // one query row's 64 partial scores, int16
 constexpr int kXQuadBytes = 32 * kXRowBytes;    // the 32 rows of one TMEM lane quadrant, 4 KiB
 constexpr int kXSlot = 4 * kXQuadBytes;         // exchange slot: 128 rows x 64 int16 = 16 KiB
 constexpr int kXScaleBytes = 32 * 4;            // a quadrant's 32 row scales (fp32), 128 B
 constexpr int kXQuadTx = kXQuadBytes + kXScaleBytes;  // bytes one quadrant's copy lands per page
 constexpr int kQBoxBytes = kRowsPerCta * 64 * 2;   // 128 query rows x 64 latent bf16, 16 KiB
-constexpr int kQRopeBytes = kRowsPerCta * 32 * 2;  // this CTA's 32 RoPE columns of 128 query rows
-// shared memory: stage ring | send slots (2) | receive slots (2) | RoPE
-// query tile | DecodeShared
-constexpr int kXOff = kStages * kStageBytes;
-constexpr int kRecvOff = kXOff + 2 * kXSlot;
-constexpr int kQRopeOff = kXOff + 4 * kXSlot;
-constexpr int kSmemShared = kQRopeOff + kQRopeBytes;
-static_assert(kStageBytes % 1024 == 0 && kXSlot % 1024 == 0 && kQRopeOff % 1024 == 0,
-              "swizzled tiles need aligned bases");
+constexpr int kQRopeBox = kRowsPerCta * 32 * 2;    // 32 RoPE columns of 128 query rows, 64-byte swizzle
+// Shared memory of the two modes of the kernel:
+//   pair (one latent group): a stage holds this CTA's latent half and its
+//        32 RoPE columns of a page; send slots (2) | receive slots (2) | the
+//        RoPE query tile (128 rows x this CTA's 32 columns) | DecodeShared.
+//   solo (2, 4 or 8 groups): a stage holds this CTA's latent half and all
+//        64 RoPE columns; P slots (2) | the RoPE query tile (128 rows x 64
+//        columns, two boxes) | DecodeShared.
+template <bool kSolo>
+struct Layout {
+  static constexpr int kRopeBoxes = kSolo ? 2 : 1;
+  static constexpr int kStageBytes = 4 * kBoxBytes + kRopeBoxes * kRopeBoxBytes;
+  static constexpr int kXOff = kStages * kStageBytes;                     // send slots (pair), P slots (solo)
+  static constexpr int kRecvOff = kSolo ? kXOff : kXOff + 2 * kXSlot;     // P is written here
+  static constexpr int kQRopeOff = kXOff + (kSolo ? 2 : 4) * kXSlot;
+  static constexpr int kQRopeBytes = kRopeBoxes * kQRopeBox;
+  static constexpr int kSmemShared = kQRopeOff + kQRopeBytes;
+  static_assert(kStageBytes % 1024 == 0 && kXSlot % 1024 == 0 && kQRopeOff % 1024 == 0,
+                "swizzled tiles need aligned bases");
+};
 static_assert(4 * kQBoxBytes == 4 * kXSlot, "the first query's latent half fills the four exchange slots");
 // warps 0-7: softmax warps (TMEM lane quadrant w & 3, key half w >> 2: 32
-// keys of every page, 128 columns of O, 64 columns of Q); warps 8-11:
-// exchange warps (one per quadrant, a whole score row per thread); warp 12:
-// TMA producer; warps 13, 14: QK and P.V issuers
+// keys of every page, 128 columns of O, 64 columns of Q); then, in pair
+// mode, warps 8-11: exchange warps (one per quadrant, a whole score row per
+// thread); then the TMA producer and the QK and P.V issuers (warps 12-14 in
+// pair mode, 8-10 in solo mode, which exchanges nothing).  15 warps leave
+// 128 registers a thread (four warps share an SM sub-partition's 64K); the
+// 11 of solo mode leave 168.
 constexpr int kSWarps = 8, kXWarps = 4;
 constexpr int kSoftmaxThreads = 32 * kSWarps, kXThreads = 32 * kXWarps;
-constexpr int kTmaWarp = kSWarps + kXWarps, kMmaWarp = kTmaWarp + 1, kPvWarp = kMmaWarp + 1;
-constexpr int kDecodeThreads = 32 * (kPvWarp + 1);
-static_assert(kPlanInKernelMaxB <= kDecodeThreads, "the in-kernel plan takes one thread per sequence");
+template <bool kSolo>
+struct Roles {
+  static constexpr int kX = kSolo ? 0 : kXWarps;  // exchange warps
+  static constexpr int kTma = kSWarps + kX, kMma = kTma + 1, kPv = kMma + 1;
+  static constexpr int kThreads = 32 * (kPv + 1);
+};
+static_assert(kPlanInKernelMaxB <= Roles<false>::kThreads && kPlanInKernelMaxBSolo <= Roles<true>::kThreads,
+              "the in-kernel plan takes one thread per sequence");
 // named barriers 1..4: the two softmax warps of a quadrant
 constexpr uint32_t kBarPair0 = 1;
 constexpr int kPlanWarpMaxB = 32;  // up to this batch one warp plans (lane = sequence)
@@ -231,8 +249,12 @@ struct DecodeShared {
 };
 
 // All shared memory is dynamic: stage ring, exchange slots, then the small state.
-constexpr int kDecodeSmem = kSmemShared + (int)((sizeof(DecodeShared) + 15) & ~size_t(15));
-static_assert(kDecodeSmem <= 232448, "decode kernel exceeds 227 KiB of shared memory");
+template <bool kSolo>
+constexpr int decode_smem() {
+  return Layout<kSolo>::kSmemShared + (int)((sizeof(DecodeShared) + 15) & ~size_t(15));
+}
+static_assert(decode_smem<false>() <= 232448 && decode_smem<true>() <= 232448,
+              "decode kernel exceeds 227 KiB of shared memory");
 
 __device__ __forceinline__ int clamp_len(int n, int lo, int hi) { return n < lo ? lo : (n > hi ? hi : n); }
 // units given to a sequence of np pages by the sequence-aligned split
@@ -528,16 +550,26 @@ __device__ void plan_in_warp(const DecodeArgs& a, int unit, bool writer, int n0,
   __syncwarp();
 }
 
-__global__ void __launch_bounds__(kDecodeThreads, 1)
+// kSolo: 2, 4 or 8 latent groups.  Every group latent lies inside one
+// latent half, so CTA r of the pair serves the heads whose group latent is
+// in its half (heads r*H/2 .. (r+1)*H/2 - 1) with their whole scores: it
+// loads all 64 RoPE columns and exchanges nothing with the peer.  Its
+// query rows are (l, h) for those heads, l-major.
+template <bool kSolo>
+__global__ void __launch_bounds__(Roles<kSolo>::kThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tm_cache, const __grid_constant__ CUtensorMap tm_rope,
                   const __grid_constant__ CUtensorMap tm_qrope, const __grid_constant__ CUtensorMap tm_qlat,
                   const DecodeArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* stages = smem;
-  const uint32_t xsend = smem_u32(smem + kXOff);     // send slots 0 and 1
-  const uint32_t xrecv = smem_u32(smem + kRecvOff);  // receive slots 0 and 1
-  const uint32_t qrope = smem_u32(smem + kQRopeOff);
-  DecodeShared& sh = *reinterpret_cast<DecodeShared*>(smem + kSmemShared);
+  using L = Layout<kSolo>;
+  constexpr int kStageBytes = L::kStageBytes;
+  const uint32_t xsend = smem_u32(smem + L::kXOff);     // send slots 0 and 1 (pair)
+  const uint32_t xrecv = smem_u32(smem + L::kRecvOff);  // receive slots (pair), P slots (solo)
+  const uint32_t qrope = smem_u32(smem + L::kQRopeOff);
+  DecodeShared& sh = *reinterpret_cast<DecodeShared*>(smem + L::kSmemShared);
+  constexpr int kXW = Roles<kSolo>::kX;
+  constexpr int kTmaWarp = Roles<kSolo>::kTma, kMmaWarp = Roles<kSolo>::kMma, kPvWarp = Roles<kSolo>::kPv;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // 128-byte-swizzled tiles need a 1024-byte aligned base; the whole cluster
@@ -591,7 +623,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     mbar_init(bar(sh.never), 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(sh.s_full[s]), 1);
-      mbar_init(bar(sh.s_free[s]), kSoftmaxThreads + kXThreads);
+      mbar_init(bar(sh.s_free[s]), kSoftmaxThreads + (kSolo ? 0 : kXThreads));
       mbar_init(bar(sh.p_full[s]), kSoftmaxThreads);
       mbar_init(bar(sh.o_done[s]), 1);
       mbar_init(bar(sh.can_send[s]), 1);  // one remote arrival from the peer
@@ -628,7 +660,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   if (a.plan_in_kernel && a.B <= kPlanWarpMaxB) {
     if (warp == 0) plan_in_warp(a, unit, unit == 0 && crank == 0, n_pre, sh.lens, &sh.rec);
   } else if (a.plan_in_kernel) {
-    int* scratch = reinterpret_cast<int*>(smem + kXOff);
+    int* scratch = reinterpret_cast<int*>(smem + L::kXOff);
     plan_in_block(a, unit, unit == 0 && crank == 0, scratch, scratch + 3 * a.B + 8, sh.lens, &sh.rec);
   } else if (threadIdx.x == 0) {
     sh.rec = ws_view(ws, a.B).rec[unit];
@@ -662,8 +694,17 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       it.init(sh.rec, lens, lens_raw);
       int sb, pa, pb;
       bool ok = true;
+      bool first_seg = true;
       while (ok && it.next(a, sb, pa, pb)) {
         const int32_t* bt = a.block_table + (size_t)sb * a.max_pages;
+        if (kSolo && !first_seg) {
+          // the query rows of this segment's sequence into L2, well before
+          // the softmax warps load them at the end of the segment before
+          const char* q0 = reinterpret_cast<const char*>(a.q_cat + (size_t)sb * a.Lq * a.H * (a.d_g + kDr));
+          const int lines = (a.Lq * a.H * (a.d_g + kDr) * 2 + 127) / 128;
+          for (int k = lane; k < lines; k += 32) asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(q0 + 128 * k));
+        }
+        first_seg = false;
         for (int c0 = pa; ok && c0 < pb; c0 += 32) {
           const int nc = min(32, pb - c0);
           const int mine = lane < nc ? bt[c0 + lane] : 0;
@@ -681,14 +722,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
               page = 0;
             }
             if (lane == 0) {
-              if (pc == 0) {  // the first segment's query, ahead of its first page
+              if (!kSolo && pc == 0) {  // the first segment's query, ahead of its first page
                 // latent boxes of 64 columns: this CTA's half of the latent
                 // (one group), or the first columns of each row's own
                 // group latent (several groups)
                 const int qy = sb * a.Lq * a.H + (int)rg * kRowsPerCta;
                 const int qx = a.G == 1 ? (int)r * 256 : 0;
                 const int nbox = a.G == 1 ? 4 : min(a.d_g, 256) / 64;
-                mbar_arrive_expect_tx(bar(sh.q_lat), nbox * kQBoxBytes + kQRopeBytes);
+                mbar_arrive_expect_tx(bar(sh.q_lat), nbox * kQBoxBytes + kQRopeBox);
                 for (int q = 0; q < nbox; ++q)
                   tma_load_2d(xsend + q * kQBoxBytes, &tm_qlat, bar(sh.q_lat), qx + 64 * q, qy);
                 tma_load_2d(qrope, &tm_qrope, bar(sh.q_lat), a.d_g + 32 * (int)r, qy);
@@ -698,9 +739,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
               for (int q = 0; q < 4; ++q)  // this CTA's latent half
                 tma_load_2d_hint(dst + q * kBoxBytes, &tm_cache, bar(sh.full[st]), (int)(r * 256 + q * 64),
                                  page * kPage, policy);
-              // this CTA's 32 RoPE columns
-              tma_load_2d_hint(dst + 4 * kBoxBytes, &tm_rope, bar(sh.full[st]), kDc + 32 * (int)r, page * kPage,
-                               policy);
+              // this CTA's 32 RoPE columns (all 64 in solo mode)
+              for (int q = 0; q < L::kRopeBoxes; ++q)
+                tma_load_2d_hint(dst + 4 * kBoxBytes + q * kRopeBoxBytes, &tm_rope, bar(sh.full[st]),
+                                 kDc + 32 * (kSolo ? q : (int)r), page * kPage, policy);
             }
             ++issued;
           }
@@ -727,8 +769,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       while (ok && c.valid) {
         if (c.seg_first()) {  // the segment's query (loaded after every QK before it finished)
           if (!(ok = mbar_wait(bar(sh.q_full), qc & 1, abort, lim))) break;
-          if (qc > 0 && !(ok = mbar_wait(bar(sh.q_tma), (qc - 1) & 1, abort, lim))) break;
-          if (qc == 0) {  // the first query left the exchange slots: the peer may send into them
+          // the RoPE query tile by TMA: every segment in solo mode, later ones in pair mode
+          const uint32_t nt = kSolo ? qc : qc - 1;
+          if ((kSolo || qc > 0) && !(ok = mbar_wait(bar(sh.q_tma), nt & 1, abort, lim))) break;
+          if (!kSolo && qc == 0) {  // the first query left the exchange slots: the peer may send into them
             mbar_arrive_remote_relaxed(mapa(bar(sh.can_send[0]), peer));
             mbar_arrive_remote_relaxed(mapa(bar(sh.can_send[1]), peer));
           }
@@ -751,8 +795,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                  kk > 0 ? 1u : 0u);
         }
 #pragma unroll
-        for (int kk = 0; kk < 2; ++kk)  // RoPE: 32 columns = 2 K steps (A = RoPE query tile)
-          mma_ss(tmem + kColS + 64 * b, qr0 + (uint64_t)(kk * 2), kr0 + (uint64_t)(kk * 2), idesc_qk, 1u);
+        for (int kk = 0; kk < 2 * L::kRopeBoxes; ++kk)  // RoPE: 32 columns = 2 K steps per box (A = RoPE query tile)
+          mma_ss(tmem + kColS + 64 * b, qr0 + (uint64_t)(((kk >> 1) * kQRopeBox + (kk & 1) * 32) >> 4),
+                 kr0 + (uint64_t)(((kk >> 1) * kRopeBoxBytes + (kk & 1) * 32) >> 4), idesc_qk, 1u);
         mma_commit(bar(sh.s_full[b]));
         ++pc;
         c.advance(a);
@@ -788,14 +833,16 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                  (acc || kk > 0) ? 1u : 0u);
         mma_commit(bar(sh.empty[p % kStages]));
         mma_commit(bar(sh.o_done[b]));
-        if (!(ok = mbar_wait(bar(sh.o_done[b]), (p >> 1) & 1, abort, lim))) break;
-        mbar_arrive_remote_relaxed(b ? peer_can_send1 : peer_can_send0);
+        if constexpr (!kSolo) {
+          if (!(ok = mbar_wait(bar(sh.o_done[b]), (p >> 1) & 1, abort, lim))) break;
+          mbar_arrive_remote_relaxed(b ? peer_can_send1 : peer_can_send0);
+        }
         c.advance(a);
       }
       if (!ok) fail();
     }
     __syncwarp();  // reconverge before the CTA-wide barrier of the teardown
-  } else if (warp >= kSWarps && warp < kSWarps + kXWarps) {
+  } else if (warp >= kSWarps && warp < kSWarps + kXW) {
     // ------------------------------------------------------------ exchange warps
     // Page p: own partial scores (S_b, fp32) -> 16-bit fixed point with a
     // per-row scale -> send slot b (one row per thread, 128-byte swizzled
@@ -809,7 +856,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     const uint32_t peer_scale = mapa(smem_u32(&sh.xscale_recv[0][0]), peer);
     const uint32_t peer_xfull0 = mapa(bar(sh.xfull[0][quad]), peer);
     const uint32_t peer_xfull1 = mapa(bar(sh.xfull[1][quad]), peer);
-    const int npages = sh.rec.end - sh.rec.start;
+    const int npages = kSolo ? 0 : sh.rec.end - sh.rec.start;  // solo mode: nothing to exchange
     bool ok = true;
     for (int p = 0; ok && p < npages; ++p) {
       const uint32_t b = p & 1;
@@ -867,11 +914,24 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     // After a failure the loops keep running without work, so every named
     // barrier still sees both warps.
     const int quad = warp & 3, half = warp >> 2;
-    const int row = quad * 32 + lane;              // TMEM lane = query row in this block
-    const int grow = (int)rg * kRowsPerCta + row;  // row of the (l, h) list
-    const bool valid = grow < a.rows;
-    const int l = valid ? grow / a.H : 0;
-    const int h = valid ? grow % a.H : 0;
+    const int row = quad * 32 + lane;  // TMEM lane = query row in this block
+    // this CTA's rows: every (l, h) in pair mode; in solo mode (l, h) for
+    // the heads h of its latent half, l-major
+    const int lrow = (int)rg * kRowsPerCta + row;    // index in this CTA's list
+    int l, h, grow;
+    bool valid;
+    if constexpr (kSolo) {
+      const int hh = a.H / 2;                        // heads per l in this CTA's list
+      valid = lrow < a.Lq * hh;
+      l = valid ? lrow / hh : 0;
+      h = valid ? (int)r * hh + lrow % hh : 0;
+      grow = l * a.H + h;                            // row of the (l, h) list of all heads
+    } else {
+      grow = lrow;
+      valid = grow < a.rows;
+      l = valid ? grow / a.H : 0;
+      h = valid ? grow % a.H : 0;
+    }
     const int g = (h * a.G) / a.H;
     // The CTA's latent half holds columns 256r .. 256r + 255 of the cache
     // row; this thread fills tensor-memory columns for two 64-column chunks
@@ -898,8 +958,21 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     auto load_q = [&](int b) {
       if (!ok) return;
       if (leader) {
-        mbar_arrive_expect_tx(bar(sh.q_tma), kQRopeBytes);
-        tma_load_2d(qrope, &tm_qrope, bar(sh.q_tma), a.d_g + 32 * (int)r, b * a.Lq * a.H + (int)rg * kRowsPerCta);
+        mbar_arrive_expect_tx(bar(sh.q_tma), L::kQRopeBytes);
+        if constexpr (kSolo) {
+          // all 64 RoPE columns, one run of hh rows (the CTA's heads of one
+          // token l) per box; runs past the last token read the next
+          // sequence's rows or the zero fill, which nobody uses
+          const int hh = a.H / 2;
+          for (int run = 0; run < kRowsPerCta / hh; ++run) {
+            const int lr = ((int)rg * kRowsPerCta) / hh + run;
+            for (int j = 0; j < 2; ++j)
+              tma_load_2d(qrope + j * kQRopeBox + run * hh * 64, &tm_qrope, bar(sh.q_tma), a.d_g + 32 * j,
+                          (b * a.Lq + lr) * a.H + (int)r * hh);
+          }
+        } else {
+          tma_load_2d(qrope, &tm_qrope, bar(sh.q_tma), a.d_g + 32 * (int)r, b * a.Lq * a.H + (int)rg * kRowsPerCta);
+        }
         ++nq_tma;
       }
 #pragma unroll 1
@@ -918,12 +991,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       tc_fence_before();
       mbar_arrive(bar(sh.q_full));
     };
-    // pull what this thread will load for sequence b into L2 ahead of use
+    // pair mode: pull what this thread will load for sequence b into L2
+    // ahead of use (solo mode: the producer warp does it)
     auto prefetch_q = [&](int b) {
       if (!valid) return;
       const char* qrow = reinterpret_cast<const char*>(qrow_of(b));
-      // the latent columns this thread will load (its group's, or for one
-      // group this CTA's half)
       const char* lat = qrow + (a.G == 1 ? r * 512 + half * 256 : 0);
       asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(lat));
       asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(lat + 128));
@@ -964,8 +1036,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     PageCursor cur;
     cur.init(sh.rec, a, lens, lens_raw);
     if (cur.valid) {
-      load_q_first();
-      prefetch_after(cur.it);
+      if constexpr (kSolo) {
+        load_q(cur.sb);
+      } else {
+        load_q_first();
+        prefetch_after(cur.it);
+      }
     }
     float m_used = -INFINITY, l_part = 0.f;
     int seg = 0, limit = 0;
@@ -981,32 +1057,41 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       }
       float s[32];  // raw scores (unscaled) of this thread's 32 keys
       float mt = -INFINITY;
-      // own partial (fp32, tensor memory) requested as soon as QK is done,
-      // while the peer's partial may still be on its way
       uint32_t v[32];
+      // solo mode: P slot b is free once P.V of page q-2 has read it (in
+      // pair mode the peer's copy into the slot already implied that)
+      if (kSolo && ok && q >= 2) ok = mbar_wait(bar(sh.o_done[b]), ((q - 2) >> 1) & 1, abort, lim);
       if (ok) ok = mbar_wait(bar(sh.s_full[b]), (q >> 1) & 1, abort, lim);
-      if (ok) ok = mbar_wait(bar(sh.xfull[b][quad]), (q >> 1) & 1, abort, lim);
+      if (!kSolo && ok) ok = mbar_wait(bar(sh.xfull[b][quad]), (q >> 1) & 1, abort, lim);
       ok = __all_sync(0xffffffffu, ok);
       if (ok) {
         tc_fence_after();
-        tmem_ld32(lane_base + kColS + 64 * b + 32 * half, v);
-        const uint32_t src = xrecv + b * kXSlot + row * kXRowBytes;  // the peer's, 16-bit
-        uint32_t pw[16];
+        tmem_ld32(lane_base + kColS + 64 * b + 32 * half, v);  // own scores (partial in pair mode), fp32
+        if constexpr (kSolo) {
+          tmem_wait_ld();
+          tc_fence_before();
+          mbar_arrive(bar(sh.s_free[b]));
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-          ld_shared_v4(src + (((4 * half + c) ^ (row & 7)) << 4), pw[4 * c], pw[4 * c + 1], pw[4 * c + 2],
-                       pw[4 * c + 3]);
-        const float down = sh.xscale_recv[b][row];
-        tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(bar(sh.s_free[b]));
-        // armed for page q+2 (sent by the peer only after our P.V of page q)
-        if (half == 0 && lane == 0) mbar_arrive_expect_tx(bar(sh.xfull[b][quad]), kXQuadTx);
+          for (int k = 0; k < 32; ++k) s[k] = __uint_as_float(v[k]);
+        } else {
+          const uint32_t src = xrecv + b * kXSlot + row * kXRowBytes;  // the peer's, 16-bit
+          uint32_t pw[16];
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const float2 y = unpack_fixed16x2(pw[k]);
-          s[2 * k] = fmaf(y.x, down, __uint_as_float(v[2 * k]));
-          s[2 * k + 1] = fmaf(y.y, down, __uint_as_float(v[2 * k + 1]));
+          for (int c = 0; c < 4; ++c)
+            ld_shared_v4(src + (((4 * half + c) ^ (row & 7)) << 4), pw[4 * c], pw[4 * c + 1], pw[4 * c + 2],
+                         pw[4 * c + 3]);
+          const float down = sh.xscale_recv[b][row];
+          tmem_wait_ld();
+          tc_fence_before();
+          mbar_arrive(bar(sh.s_free[b]));
+          // armed for page q+2 (sent by the peer only after our P.V of page q)
+          if (half == 0 && lane == 0) mbar_arrive_expect_tx(bar(sh.xfull[b][quad]), kXQuadTx);
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const float2 y = unpack_fixed16x2(pw[k]);
+            s[2 * k] = fmaf(y.x, down, __uint_as_float(v[2 * k]));
+            s[2 * k + 1] = fmaf(y.y, down, __uint_as_float(v[2 * k + 1]));
+          }
         }
         const int key0 = cur.i * kPage + 32 * half;
         if (limit < key0 + 32) {  // keys this row may not see
@@ -1072,7 +1157,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         nx.advance(a);
         if (nx.valid) {
           load_q(nx.sb);
-          prefetch_after(nx.it);
+          if constexpr (!kSolo) prefetch_after(nx.it);
         }
       }
 
@@ -1103,7 +1188,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                                 __uint_as_float(v[4 * k + 2]) * inv, __uint_as_float(v[4 * k + 3]) * inv);
             }
           }
-          if (valid && r == 0 && half == 0)
+          if (valid && (kSolo || r == 0) && half == 0)
             a.lse_part[(size_t)seg * a.rows + grow] =
                 l_sum > 0.f ? (m_used + lg2(l_sum)) * 0.69314718055994531f : -INFINITY;
           tc_fence_before();
@@ -1120,18 +1205,23 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   // work waits (ignoring the abort flag) until it is done: after a normal
   // run these waits return at once; after an abort they keep copies and
   // MMAs from landing in memory that is about to be released.
+  // A drain that gives up (nothing in flight should take 100 ms) is
+  // recorded as a timeout too, by the thread that gave up.
   __syncthreads();
+  auto drain = [&](uint32_t b, uint32_t parity) {
+    if (!mbar_wait_quiet(b, parity)) set_status(a.ws, MLA_ERR_TIMEOUT);
+  };
   if (warp == kTmaWarp && lane == 0) {
     for (uint32_t k = issued > (uint32_t)kStages ? issued - kStages : 0; k < issued; ++k)
-      mbar_wait_quiet(bar(sh.full[k % kStages]), (k / kStages) & 1);
-    if (issued > 0) mbar_wait_quiet(bar(sh.q_lat), 0);
+      drain(bar(sh.full[k % kStages]), (k / kStages) & 1);
+    if (!kSolo && issued > 0) drain(bar(sh.q_lat), 0);  // the first query's copies
   } else if ((warp == kMmaWarp || warp == kPvWarp) && lane == 0) {
     const int d = warp == kMmaWarp ? 0 : 1;
     mma_commit(bar(sh.drain[d]));
-    mbar_wait_quiet(bar(sh.drain[d]), 0);
+    drain(bar(sh.drain[d]), 0);
   } else if (threadIdx.x == 0 && nq_tma > 0) {
-    mbar_wait_quiet(bar(sh.q_tma), (nq_tma - 1) & 1);
-  } else if (warp >= kSWarps && warp < kSWarps + kXWarps && lane == 0) {
+    drain(bar(sh.q_tma), (nq_tma - 1) & 1);
+  } else if (warp >= kSWarps && warp < kSWarps + kXW && lane == 0) {
     bulk_wait_read_all();  // this thread's copies have read their send slot
     st_cluster_u32(mapa(smem_u32(&sh.peer_sent[warp - kSWarps]), peer), (uint32_t)sent);
   }
@@ -1139,9 +1229,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   cluster_sync();  // every copy of the pair issued, the counts of pages sent visible
   // partial scores the peer sent here but this CTA never read (after an
   // abort): its last two pages of each quadrant may still be in flight
-  if (warp >= kSWarps && warp < kSWarps + kXWarps && lane == 0) {
+  if (warp >= kSWarps && warp < kSWarps + kXW && lane == 0) {
     const int qd = warp - kSWarps, n = sh.peer_sent[qd];
-    for (int p = n > 2 ? n - 2 : 0; p < n; ++p) mbar_wait_quiet(bar(sh.xfull[p & 1][qd]), (p >> 1) & 1);
+    for (int p = n > 2 ? n - 2 : 0; p < n; ++p) drain(bar(sh.xfull[p & 1][qd]), (p >> 1) & 1);
   }
   __syncwarp();
   if (warp == kMmaWarp) {
@@ -1283,23 +1373,24 @@ cudaError_t launch_plan(const int32_t* seq_lens, const int32_t* block_table, WsH
   return cudaGetLastError();
 }
 
-// Per-device facts of the decode launch, found once per device and process:
-// whether the kernel's shared-memory limit has been raised there, and how
-// many clusters of 2 and of 4 CTAs fit at once.  Calls may come from several
-// host threads and for several devices, so the table is guarded by a mutex
-// (never held across a CUDA call).  Devices past the table are not cached.
+// Per-device facts of the decode launch, found once per device and process
+// for each mode of the kernel: whether its shared-memory limit has been
+// raised there, and how many clusters of 2, 4, 6 and 8 CTAs fit at once.
+// Calls may come from several host threads and for several devices, so the
+// table is guarded by a mutex (never held across a CUDA call).  Devices past
+// the table are not cached.
 namespace {
 constexpr int kCachedDevices = 64;
 struct DecodeDeviceInfo {
-  bool smem_set;
-  int units[4];  // clusters of 2, 4, 6 and 8 CTAs; 0 = not known yet
+  bool smem_set[2];
+  int units[2][4];  // [solo][clusters of 2, 4, 6, 8 CTAs]; 0 = not known yet
 };
 std::mutex g_decode_mu;
 DecodeDeviceInfo g_decode_info[kCachedDevices];
-}  // namespace
 
-static cudaError_t decode_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, int units,
-                                 int csize, cudaStream_t st) {
+template <bool kSolo>
+cudaError_t decode_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, int units, int csize,
+                          cudaStream_t st) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -1307,20 +1398,21 @@ static cudaError_t decode_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* a
   bool set = false;
   if (cached) {
     std::lock_guard<std::mutex> lock(g_decode_mu);
-    set = g_decode_info[dev].smem_set;
+    set = g_decode_info[dev].smem_set[kSolo];
   }
   if (!set) {  // the attribute is per device
-    e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecodeSmem);
+    e = cudaFuncSetAttribute(decode_kernel<kSolo>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             decode_smem<kSolo>());
     if (e != cudaSuccess) return e;
     if (cached) {
       std::lock_guard<std::mutex> lock(g_decode_mu);
-      g_decode_info[dev].smem_set = true;
+      g_decode_info[dev].smem_set[kSolo] = true;
     }
   }
   cfg = cudaLaunchConfig_t{};
   cfg.gridDim = dim3(units * csize);
-  cfg.blockDim = dim3(kDecodeThreads);
-  cfg.dynamicSmemBytes = kDecodeSmem;
+  cfg.blockDim = dim3(Roles<kSolo>::kThreads);
+  cfg.dynamicSmemBytes = decode_smem<kSolo>();
   cfg.stream = st;
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = csize;
@@ -1333,41 +1425,52 @@ static cudaError_t decode_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* a
   return cudaSuccess;
 }
 
-int decode_max_units(int csize, int* units) {
+template <bool kSolo>
+int decode_max_units_mode(int csize, int* units) {
   const int slot = csize / 2 - 1;
-  if (slot < 0 || slot > 3) return MLA_ERR_UNSUPPORTED;
+  if (slot < 0 || slot > 3 || (csize & 1)) return MLA_ERR_UNSUPPORTED;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_CUDA;
   const bool cached = dev >= 0 && dev < kCachedDevices;
   if (cached) {
     std::lock_guard<std::mutex> lock(g_decode_mu);
-    if (g_decode_info[dev].units[slot] > 0) {
-      *units = g_decode_info[dev].units[slot];
+    if (g_decode_info[dev].units[kSolo][slot] > 0) {
+      *units = g_decode_info[dev].units[kSolo][slot];
       return MLA_OK;
     }
   }
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[2];
-  if (decode_config(cfg, attr, 1, csize, nullptr) != cudaSuccess) return MLA_ERR_CUDA;
+  if (decode_config<kSolo>(cfg, attr, 1, csize, nullptr) != cudaSuccess) return MLA_ERR_CUDA;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, decode_kernel, &cfg) != cudaSuccess || n < 1) return MLA_ERR_CUDA;
+  if (cudaOccupancyMaxActiveClusters(&n, decode_kernel<kSolo>, &cfg) != cudaSuccess || n < 1) return MLA_ERR_CUDA;
   if (n > kMaxUnits) n = kMaxUnits;  // the workspace holds per-unit records for at most this many
   if (cached) {
     std::lock_guard<std::mutex> lock(g_decode_mu);
-    g_decode_info[dev].units[slot] = n;
+    g_decode_info[dev].units[kSolo][slot] = n;
   }
   *units = n;
   return MLA_OK;
 }
+}  // namespace
 
-cudaError_t launch_decode(const CUtensorMap& tm_cache, const CUtensorMap& tm_rope, const CUtensorMap& tm_qrope,
-                          const CUtensorMap& tm_qlat, const DecodeArgs& a, int units, int csize, cudaStream_t st) {
-  cudaLaunchConfig_t cfg;
-  cudaLaunchAttribute attr[2];
-  cudaError_t e = decode_config(cfg, attr, units, csize, st);
-  if (e != cudaSuccess) return e;
-  return cudaLaunchKernelEx(&cfg, decode_kernel, tm_cache, tm_rope, tm_qrope, tm_qlat, a);
+int decode_max_units(bool solo, int csize, int* units) {
+  return solo ? decode_max_units_mode<true>(csize, units) : decode_max_units_mode<false>(csize, units);
 }
 
+cudaError_t launch_decode(bool solo, const CUtensorMap& tm_cache, const CUtensorMap& tm_rope,
+                          const CUtensorMap& tm_qrope, const CUtensorMap& tm_qlat, const DecodeArgs& a, int units,
+                          int csize, cudaStream_t st) {
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[2];
+  if (solo) {
+    cudaError_t e = decode_config<true>(cfg, attr, units, csize, st);
+    if (e != cudaSuccess) return e;
+    return cudaLaunchKernelEx(&cfg, decode_kernel<true>, tm_cache, tm_rope, tm_qrope, tm_qlat, a);
+  }
+  cudaError_t e = decode_config<false>(cfg, attr, units, csize, st);
+  if (e != cudaSuccess) return e;
+  return cudaLaunchKernelEx(&cfg, decode_kernel<false>, tm_cache, tm_rope, tm_qrope, tm_qlat, a);
+}
 
 }  // namespace mla

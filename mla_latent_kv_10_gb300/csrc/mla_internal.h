@@ -77,7 +77,7 @@ struct DecodeArgs {
   WsHeader* ws;
   int B, Lq, H, G, d_g, max_pages, num_pages, causal, rows;  // rows = Lq*H
   float scale_log2;   // scale * log2(e)
-  int plan_in_kernel; // 1: every CTA computes the split itself (B <= kPlanInKernelMaxB)
+  int plan_in_kernel; // 1: every CTA computes the split itself (B <= decode_plan_max_b)
   int units;
   const int32_t* seq_lens;
   unsigned long long wait_ns;  // wall-clock limit of each pipeline wait inside the kernel
@@ -88,7 +88,10 @@ struct DecodeArgs {
 // issuer stalls (normally -1, never).
 unsigned long long decode_wait_limit_ns();
 int decode_stall_page();
-constexpr int kPlanInKernelMaxB = 448;  // one sequence per decode-kernel thread (its block size)
+// the decode kernel plans its own split for batches up to these sizes (one
+// sequence a thread; its blocks have 480 threads in pair mode, for one
+// latent group, and 352 in solo mode, for grouped latents)
+constexpr int kPlanInKernelMaxB = 448, kPlanInKernelMaxBSolo = 352;
 
 // launchers (return cudaError_t of the launch)
 cudaError_t launch_absorb(const CUtensorMap& tmA, const CUtensorMap& tmB, const void* q_rope,
@@ -101,8 +104,12 @@ cudaError_t launch_plan(const int32_t* seq_lens, const int32_t* block_table, WsH
 // RoPE columns (32 x 64 boxes, 64-byte swizzle); tm_qrope: q_cat rows
 // (32 x 128 boxes, 64-byte swizzle); tm_qlat: q_cat rows (64 x 128 boxes,
 // 128-byte swizzle)
-cudaError_t launch_decode(const CUtensorMap& tm_cache, const CUtensorMap& tm_rope, const CUtensorMap& tm_qrope,
-                          const CUtensorMap& tm_qlat, const DecodeArgs& a, int units, int csize, cudaStream_t st);
+// solo: the kernel mode for 2, 4 or 8 latent groups (each CTA of a pair
+// serves the heads of its latent half, no exchange; tm_qrope then has boxes
+// of 32 x H/2); otherwise the pair mode for one group.
+cudaError_t launch_decode(bool solo, const CUtensorMap& tm_cache, const CUtensorMap& tm_rope,
+                          const CUtensorMap& tm_qrope, const CUtensorMap& tm_qlat, const DecodeArgs& a, int units,
+                          int csize, cudaStream_t st);
 // Launch with programmatic stream serialization: the kernel may start its
 // set-up while the kernel before it on the stream finishes (every kernel of
 // this library waits for its predecessor before touching global memory).
@@ -129,6 +136,14 @@ cudaError_t launch_combine(const float* o_part, const float* lse_part, const WsH
 cudaError_t launch_combine_project(const CUtensorMap& tmA, const float* o_part, const float* lse_part,
                                    const WsHeader* ws, void* out, void* o_lat, float* lse, int B, int Lq, int H,
                                    int G, int slots, cudaStream_t st);
-int decode_max_units(int csize, int* units);  // clusters of csize CTAs resident at once
+int decode_max_units(bool solo, int csize, int* units);  // clusters of csize CTAs resident at once
+// CTAs per cluster of the decode launch: a pair per 128 query rows of a
+// sequence (in solo mode each CTA of the pair holds half the heads)
+inline bool decode_solo(int G) { return G > 1; }
+inline int decode_plan_max_b(int G) { return decode_solo(G) ? kPlanInKernelMaxBSolo : kPlanInKernelMaxB; }
+inline int decode_csize(int Lq, int H, int G) {
+  const int rows_per_cta = decode_solo(G) ? Lq * (H / 2) : Lq * H;
+  return 2 * ((rows_per_cta + kRowsPerCta - 1) / kRowsPerCta);
+}
 
 }  // namespace mla

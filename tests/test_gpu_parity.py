@@ -84,15 +84,18 @@ def test_decode_step_small(name):
     check_case(c, got, sample_pairs(c, heads))
 
 
-@pytest.mark.parametrize("B,Lq,launches", [(448, 2, 1), (449, 2, 2), (600, 1, 2)])
-def test_decode_large_batch(B, Lq, launches):
-    """Batches at the largest size the decode kernel splits by itself (448),
-    just above it and well above it (split by the separate plan kernel):
-    ragged lengths, shuffled pages, every sequence checked on a few heads."""
+@pytest.mark.parametrize("B,Lq,G,launches", [(448, 2, 1, 1), (449, 2, 1, 2), (600, 1, 1, 2),
+                                             (352, 1, 2, 1), (353, 2, 2, 2)])
+def test_decode_large_batch(B, Lq, G, launches):
+    """Batches at the largest size the decode kernel splits by itself (448
+    for one latent group, 352 for grouped latents, whose kernel has fewer
+    threads), just above it and well above it (split by the separate plan
+    kernel): ragged lengths, shuffled pages, every sequence checked on a few
+    heads of both latent halves."""
     rng = np.random.default_rng(B)
     lens = [int(x) for x in rng.integers(Lq, 200, size=B)]
     lens[0], lens[-1] = Lq, 64
-    c = make_case(B=B, Lq=Lq, H=16, seq_lens=lens, table="perm", seed=47 + B)
+    c = make_case(B=B, Lq=Lq, H=16, G=G, seq_lens=lens, table="perm", seed=47 + B)
     assert mla.mla_decode_kernel_launches(c.dims) == launches
     got = run_gpu(c)
     assert got["status"] == 0
