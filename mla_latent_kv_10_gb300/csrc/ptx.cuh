@@ -117,20 +117,6 @@ __device__ __forceinline__ void griddep_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// ------------------------------------------------------------------ registers
-// Move a warpgroup's per-thread register allocation down or up (every warp of
-// the warpgroup executes the same instruction).  An increase waits until
-// other warpgroups have released enough of the CTA's launch allocation, so
-// the caller must keep the sum within it.
-template <uint32_t N>
-__device__ __forceinline__ void setmaxnreg_inc() {
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
-}
-template <uint32_t N>
-__device__ __forceinline__ void setmaxnreg_dec() {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
-}
-
 // ------------------------------------------------------------------ cluster
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
@@ -153,24 +139,8 @@ __device__ __forceinline__ uint32_t mapa(uint32_t local_addr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_addr), "r"(rank));
   return r;
 }
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float4 v) {
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y),
-               "f"(v.z), "f"(v.w)
-               : "memory");
-}
 __device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-// Asynchronous 16-byte store into another CTA of the cluster; its bytes are
-// counted (complete_tx) on the mbarrier `cluster_bar`, which must live in the
-// destination CTA.
-__device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, uint32_t a, uint32_t b, uint32_t c,
-                                            uint32_t d, uint32_t cluster_bar) {
-  asm volatile(
-      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
-          cluster_addr),
-      "r"(a), "r"(b), "r"(c), "r"(d), "r"(cluster_bar)
-      : "memory");
 }
 __device__ __forceinline__ void cluster_arrive() {
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
@@ -313,15 +283,6 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
       : "memory");
 }
-// Arrive on the mbarrier at the same shared-memory offset in every CTA of
-// `cta_mask` (cluster ranks) once every tcgen05 op issued so far by this
-// thread is done.
-__device__ __forceinline__ void mma_commit_multicast(uint32_t bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
-      "h"(cta_mask)
-      : "memory");
-}
 // Instruction descriptor, kind::f16: f16 A and B, fp32 accumulator, K-major.
 __host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
   return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
@@ -384,20 +345,6 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       : "memory");
 }
 
-// forms chosen by the array size
-template <int N>
-__device__ __forceinline__ void tmem_ldn(uint32_t taddr, uint32_t (&r)[N]) {
-  static_assert(N == 16 || N == 32, "16 or 32 columns");
-  if constexpr (N == 32) tmem_ld32(taddr, r);
-  else tmem_ld16(taddr, r);
-}
-template <int N>
-__device__ __forceinline__ void tmem_stn(uint32_t taddr, const uint32_t (&r)[N]) {
-  static_assert(N == 8 || N == 16 || N == 32, "8, 16 or 32 columns");
-  if constexpr (N == 32) tmem_st32(taddr, r);
-  else if constexpr (N == 16) tmem_st16(taddr, r);
-  else tmem_st8(taddr, r);
-}
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
