@@ -238,6 +238,65 @@ int mla_combine_project(const mla_dims* dims, const float* o_part,
                         void* o_lat, float* lse, void* stream);
 
 /*
+ * ---- The decompress branch, for long query chunks.
+ * The MLA operator write-up §3 (the plugin's prefill threshold of 256 query
+ * tokens) and §6 (long chunks decompress K and V and run ordinary attention;
+ * short ones stay in the latent space): callers with Lq >= the threshold
+ * take mla_decompress_kv + mla_prefill_attend; mla_decode_paged serves
+ * Lq <= 4.  Both calls accept any 1 <= Lq <= max_pages_per_seq * 64; the
+ * other dims are as for the decode (G in {1, 2, 4, 8}).
+ */
+#define MLA_PREFILL_THRESHOLD 256
+
+/*
+ * Bytes of ONE of the two buffers mla_decompress_kv writes (k_nope or v):
+ * B * H * max_pages_per_seq * 64 * d_hc bf16 values.
+ */
+int mla_decompressed_kv_size(const mla_dims* dims, size_t* bytes);
+
+/*
+ * mla_decompress_kv — per-head keys and values from the latent cache (the
+ * write-up's §1: MLA stores c and recovers K and V by the up-projections;
+ * §4: K = c . W_UK^T, the same orientation as the absorption):
+ *     k_nope[b,h,s,:] = W_UK[h] . c_g(h)[s],   v[b,h,s,:] = W_UV[h] . c_g(h)[s]
+ * for every cached token s < seq_lens[b] (read through block_table as in
+ * mla_decode_paged), and zeros for the rest of the sequence's last page.
+ * k_nope, v: bf16 [B, H, max_pages_per_seq * 64, d_hc], caller-allocated
+ * (mla_decompressed_kv_size bytes each); rows past the last page are not
+ * written.  workspace: at least 32 bytes whose first int is the sticky
+ * status word (a decode workspace will do), zeroed once by the caller; bad
+ * table entries (MLA_ERR_BAD_TABLE) and lengths (MLA_ERR_BAD_SEQLEN: outside
+ * [Lq, max_pages_per_seq * 64]) are recorded there and clamped, never
+ * dereferenced.  fp32 accumulation on the tensor cores, bf16 out.
+ * Errors: MLA_ERR_INVALID_ARG / UNSUPPORTED / MISALIGNED (16 bytes for the
+ * tensors, 4 for the index arrays and workspace) / WORKSPACE / CUDA.
+ */
+int mla_decompress_kv(const mla_dims* dims, const void* kv_cache,
+                      const int32_t* block_table, const int32_t* seq_lens,
+                      const void* W_UK, const void* W_UV, void* k_nope, void* v,
+                      void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * mla_prefill_attend — causal attention of Lq new tokens over the
+ * decompressed keys and values (the write-up's §4 "path A", the
+ * non-absorbed form):
+ *     out[b,l,h,:] = sum_s p_s v[b,h,s,:],
+ *     p = softmax_s((q_nope[b,l,h] . k_nope[b,h,s] + q_rope[b,l,h] . k_R[s]) * scale)
+ * over the keys s <= seq_lens[b] - Lq + l (the new tokens are the last Lq of
+ * the sequence), k_R[s] read from the cache row (columns 512..575).  lse
+ * (fp32 [B,Lq,H]) receives the natural log-sum-exp of the scaled scores.
+ * q_nope bf16 [B,Lq,H,d_hc], q_rope bf16 [B,Lq,H,d_R]; k_nope, v as written
+ * by mla_decompress_kv; out bf16 [B,Lq,H,d_hc]; workspace, block_table,
+ * seq_lens and errors as for mla_decompress_kv.  fp32 scores, fp32 online
+ * softmax, bf16 weights P, fp32 accumulation.
+ */
+int mla_prefill_attend(const mla_dims* dims, const void* q_nope, const void* q_rope,
+                       const void* kv_cache, const int32_t* block_table,
+                       const int32_t* seq_lens, const void* k_nope, const void* v,
+                       void* out, float* lse, void* workspace, size_t ws_bytes,
+                       void* stream);
+
+/*
  * Synchronise `stream`, then return the sticky device status of `workspace`
  * (MLA_OK or the first device error recorded since the workspace was zeroed).
  */

@@ -17,6 +17,8 @@ __all__ = [
     "mla_decode_workspace_size", "mla_decode_num_slots", "mla_decode_kernel_launches",
     "launches_per_step", "mla_get_device_status", "mla_set_timeout_test",
     "mla_status_string", "make_dims", "DecodeBuffers", "decode_step",
+    "mla_decompressed_kv_size", "mla_decompress_kv", "mla_prefill_attend", "PrefillBuffers", "prefill_step",
+    "PREFILL_THRESHOLD",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -64,6 +66,9 @@ def load_library():
         "mla_combine_project": [DP, P, P, P, S, P, P, P, P, P],
         "mla_get_device_status": [P, P],
         "mla_set_timeout_test": [ctypes.c_longlong, I],
+        "mla_decompressed_kv_size": [DP, ctypes.POINTER(S)],
+        "mla_decompress_kv": [DP, P, P, P, P, P, P, P, P, S, P],
+        "mla_prefill_attend": [DP, P, P, P, P, P, P, P, P, P, P, S, P],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -215,3 +220,53 @@ def decode_step(dims, bufs: DecodeBuffers, q_nope, q_rope, W_UK, W_UV, cache, bl
         mla_combine_splits(dims, bufs.o_part, bufs.lse_part, bufs.workspace, bufs.o_lat, bufs.lse, stream)
         mla_project_uv(dims, bufs.o_lat, W_UV, bufs.out, stream)
     return bufs.out
+
+
+PREFILL_THRESHOLD = 256  # mirror of MLA_PREFILL_THRESHOLD: from this many new tokens on, the decompress branch
+
+
+def mla_decompressed_kv_size(dims) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load_library().mla_decompressed_kv_size(_dims(dims), ctypes.byref(n)), "mla_decompressed_kv_size")
+    return n.value
+
+
+def mla_decompress_kv(dims, kv_cache, block_table, seq_lens, W_UK, W_UV, k_nope, v, workspace, stream=None):
+    _check(load_library().mla_decompress_kv(
+        _dims(dims), _ptr(kv_cache), _ptr(block_table), _ptr(seq_lens), _ptr(W_UK), _ptr(W_UV), _ptr(k_nope),
+        _ptr(v), _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)),
+        "mla_decompress_kv")
+
+
+def mla_prefill_attend(dims, q_nope, q_rope, kv_cache, block_table, seq_lens, k_nope, v, out, lse, workspace,
+                       stream=None):
+    _check(load_library().mla_prefill_attend(
+        _dims(dims), _ptr(q_nope), _ptr(q_rope), _ptr(kv_cache), _ptr(block_table), _ptr(seq_lens), _ptr(k_nope),
+        _ptr(v), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)), "mla_prefill_attend")
+
+
+class PrefillBuffers:
+    """Device buffers of the decompress branch for fixed dims (torch
+    allocations; the library itself never allocates)."""
+
+    def __init__(self, dims: dict, device="cuda"):
+        import torch
+        self.dims = dict(dims)
+        B, Lq, H = dims["B"], dims["Lq"], dims["H"]
+        S = dims["max_pages"] * dims["page_size"]
+        assert mla_decompressed_kv_size(dims) == B * H * S * dims["d_hc"] * 2
+        self.k_nope = torch.empty(B, H, S, dims["d_hc"], dtype=torch.bfloat16, device=device)
+        self.v = torch.empty(B, H, S, dims["d_hc"], dtype=torch.bfloat16, device=device)
+        self.out = torch.empty(B, Lq, H, dims["d_hc"], dtype=torch.bfloat16, device=device)
+        self.lse = torch.empty(B, Lq, H, dtype=torch.float32, device=device)
+        self.workspace = torch.zeros(32, dtype=torch.uint8, device=device)  # the status word
+
+
+def prefill_step(dims, bufs: PrefillBuffers, q_nope, q_rope, W_UK, W_UV, cache, block_table, seq_lens,
+                 stream=None):
+    """The decompress branch of one layer: per-head keys and values from the
+    latent cache, then causal attention of the Lq new tokens over them."""
+    mla_decompress_kv(dims, cache, block_table, seq_lens, W_UK, W_UV, bufs.k_nope, bufs.v, bufs.workspace, stream)
+    mla_prefill_attend(dims, q_nope, q_rope, cache, block_table, seq_lens, bufs.k_nope, bufs.v, bufs.out, bufs.lse,
+                       bufs.workspace, stream)

@@ -60,6 +60,22 @@ int check_dims(const mla_dims* d) {
   return MLA_OK;
 }
 
+// The decompress branch accepts any number of new tokens (up to the cached
+// length); its tensor views index rows in int32.
+int check_dims_prefill(const mla_dims* d) {
+  if (!d) return MLA_ERR_INVALID_ARG;
+  if (d->Lq < 1) return MLA_ERR_INVALID_ARG;
+  mla_dims one = *d;
+  one.Lq = 1;
+  int rc = check_dims(&one);
+  if (rc != MLA_OK) return rc;
+  if (d->Lq > d->max_pages_per_seq * kPage) return MLA_ERR_INVALID_ARG;
+  if ((long long)d->B * d->Lq >= (1LL << 31) || (long long)d->B * d->H * d->max_pages_per_seq * kPage >= (1LL << 31))
+    return MLA_ERR_UNSUPPORTED;
+  if (d->B > 65535) return MLA_ERR_UNSUPPORTED;  // grid z
+  return MLA_OK;
+}
+
 constexpr unsigned long long kDefaultWaitNs = 2000000000ull;  // 2 s
 std::atomic<unsigned long long> g_wait_ns{kDefaultWaitNs};
 std::atomic<int> g_stall_page{-1};
@@ -280,6 +296,93 @@ int mla_combine_project(const mla_dims* d, const float* o_part, const float* lse
   return cuda_status(launch_combine_project(tA, o_part, lse_part, static_cast<const WsHeader*>(workspace), out,
                                             o_lat, lse, d->B, d->Lq, d->H, d->G, slots,
                                             static_cast<cudaStream_t>(stream)));
+}
+
+int mla_decompressed_kv_size(const mla_dims* d, size_t* bytes) {
+  int rc = check_dims_prefill(d);
+  if (rc != MLA_OK) return rc;
+  if (!bytes) return MLA_ERR_INVALID_ARG;
+  *bytes = (size_t)d->B * d->H * d->max_pages_per_seq * kPage * kDhc * 2;
+  return MLA_OK;
+}
+
+int mla_decompress_kv(const mla_dims* d, const void* kv_cache, const int32_t* block_table,
+                      const int32_t* seq_lens, const void* W_UK, const void* W_UV, void* k_nope, void* v,
+                      void* workspace, size_t ws_bytes, void* stream) {
+  int rc = check_dims_prefill(d);
+  if (rc != MLA_OK) return rc;
+  if (!kv_cache || !block_table || !seq_lens || !W_UK || !W_UV || !k_nope || !v) return MLA_ERR_INVALID_ARG;
+  if (!workspace || ws_bytes < sizeof(WsHeader)) return MLA_ERR_WORKSPACE;
+  if (!aligned16(kv_cache) || !aligned16(W_UK) || !aligned16(W_UV) || !aligned16(k_nope) || !aligned16(v) ||
+      (reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 3u))
+    return MLA_ERR_MISALIGNED;
+  const int H = d->H, dg = kDc / d->G;
+  CUtensorMap tC, tK, tV;
+  {
+    cuuint64_t dims[2] = {(cuuint64_t)kRow, (cuuint64_t)d->num_pages * kPage};
+    cuuint64_t strides[1] = {(cuuint64_t)kRow * 2};
+    cuuint32_t box[2] = {64, kPage};
+    if ((rc = make_map(&tC, kv_cache, 2, dims, strides, box)) != MLA_OK) return rc;
+  }
+  {
+    cuuint64_t dims[3] = {(cuuint64_t)dg, (cuuint64_t)kDhc, (cuuint64_t)H};
+    cuuint64_t strides[2] = {(cuuint64_t)dg * 2, (cuuint64_t)kDhc * dg * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)kDhc, 1};
+    if ((rc = make_map(&tK, W_UK, 3, dims, strides, box)) != MLA_OK) return rc;
+    if ((rc = make_map(&tV, W_UV, 3, dims, strides, box)) != MLA_OK) return rc;
+  }
+  return cuda_status(launch_decompress(tC, tK, tV, block_table, seq_lens, k_nope, v,
+                                       static_cast<WsHeader*>(workspace), d->B, H, d->G, d->Lq,
+                                       d->max_pages_per_seq, d->num_pages, decode_wait_limit_ns(),
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+int mla_prefill_attend(const mla_dims* d, const void* q_nope, const void* q_rope, const void* kv_cache,
+                       const int32_t* block_table, const int32_t* seq_lens, const void* k_nope, const void* v,
+                       void* out, float* lse, void* workspace, size_t ws_bytes, void* stream) {
+  int rc = check_dims_prefill(d);
+  if (rc != MLA_OK) return rc;
+  if (!q_nope || !q_rope || !kv_cache || !block_table || !seq_lens || !k_nope || !v || !out || !lse)
+    return MLA_ERR_INVALID_ARG;
+  if (!workspace || ws_bytes < sizeof(WsHeader)) return MLA_ERR_WORKSPACE;
+  if (!aligned16(q_nope) || !aligned16(q_rope) || !aligned16(kv_cache) || !aligned16(k_nope) || !aligned16(v) ||
+      !aligned16(out) || (reinterpret_cast<uintptr_t>(lse) & 3u) ||
+      (reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 3u))
+    return MLA_ERR_MISALIGNED;
+  const int H = d->H;
+  const cuuint64_t rows_q = (cuuint64_t)d->B * d->Lq, rows_kv = (cuuint64_t)d->B * H * d->max_pages_per_seq * kPage;
+  CUtensorMap tQN, tQR, tK, tV, tC;
+  {
+    cuuint64_t dims[2] = {(cuuint64_t)H * kDhc, rows_q};
+    cuuint64_t strides[1] = {(cuuint64_t)H * kDhc * 2};
+    cuuint32_t box[2] = {64, kRowsPerCta};
+    if ((rc = make_map(&tQN, q_nope, 2, dims, strides, box)) != MLA_OK) return rc;
+  }
+  {
+    cuuint64_t dims[2] = {(cuuint64_t)H * kDr, rows_q};
+    cuuint64_t strides[1] = {(cuuint64_t)H * kDr * 2};
+    cuuint32_t box[2] = {64, kRowsPerCta};
+    if ((rc = make_map(&tQR, q_rope, 2, dims, strides, box)) != MLA_OK) return rc;
+  }
+  {
+    cuuint64_t dims[2] = {(cuuint64_t)kDhc, rows_kv};
+    cuuint64_t strides[1] = {(cuuint64_t)kDhc * 2};
+    cuuint32_t box[2] = {64, kPage};
+    if ((rc = make_map(&tK, k_nope, 2, dims, strides, box)) != MLA_OK) return rc;
+    if ((rc = make_map(&tV, v, 2, dims, strides, box)) != MLA_OK) return rc;
+  }
+  {
+    cuuint64_t dims[2] = {(cuuint64_t)kRow, (cuuint64_t)d->num_pages * kPage};
+    cuuint64_t strides[1] = {(cuuint64_t)kRow * 2};
+    cuuint32_t box[2] = {64, kPage};
+    if ((rc = make_map(&tC, kv_cache, 2, dims, strides, box)) != MLA_OK) return rc;
+  }
+  return cuda_status(launch_prefill_attend(tQN, tQR, tK, tV, tC, block_table, seq_lens, out, lse,
+                                           static_cast<WsHeader*>(workspace), d->B, d->Lq, H,
+                                           d->max_pages_per_seq, d->num_pages, d->scale, decode_wait_limit_ns(),
+                                           static_cast<cudaStream_t>(stream)));
 }
 
 int mla_get_device_status(const void* workspace, void* stream) {

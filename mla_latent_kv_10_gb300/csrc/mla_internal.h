@@ -137,6 +137,20 @@ cudaError_t launch_combine_project(const CUtensorMap& tmA, const float* o_part, 
                                    const WsHeader* ws, void* out, void* o_lat, float* lse, int B, int Lq, int H,
                                    int G, int slots, cudaStream_t st);
 int decode_max_units(bool solo, int csize, int* units);  // clusters of csize CTAs resident at once
+// The decompress branch (mla_prefill.cu).  tmC: cache rows (64 x 64 boxes,
+// 128-byte swizzle); tmWK, tmWV: W_UK, W_UV as [H, 128, d_g] (64 x 128 x 1
+// boxes); tmQN, tmQR: q_nope, q_rope as [B*Lq rows, H*128 / H*64 columns]
+// (64 x 128 boxes); tmK, tmV: k_nope, v as [B*H*S rows, 128 columns]
+// (64 x 64 boxes).
+cudaError_t launch_decompress(const CUtensorMap& tmC, const CUtensorMap& tmWK, const CUtensorMap& tmWV,
+                              const int32_t* block_table, const int32_t* seq_lens, void* k_nope, void* v,
+                              WsHeader* ws, int B, int H, int G, int Lq, int max_pages, int num_pages,
+                              unsigned long long wait_ns, cudaStream_t st);
+cudaError_t launch_prefill_attend(const CUtensorMap& tmQN, const CUtensorMap& tmQR, const CUtensorMap& tmK,
+                                  const CUtensorMap& tmV, const CUtensorMap& tmC, const int32_t* block_table,
+                                  const int32_t* seq_lens, void* out, float* lse, WsHeader* ws, int B, int Lq,
+                                  int H, int max_pages, int num_pages, float scale, unsigned long long wait_ns,
+                                  cudaStream_t st);
 // CTAs per cluster of the decode launch: a pair per 128 query rows of a
 // sequence (in solo mode each CTA of the pair holds half the heads)
 inline bool decode_solo(int G) { return G > 1; }
