@@ -135,3 +135,45 @@ def test_timeout_test_hook_arguments(lib):
     assert lib.mla_set_timeout_test(0, -2) == -1
     assert lib.mla_set_timeout_test(1000, 3) == 0
     assert lib.mla_set_timeout_test(0, -1) == 0
+
+
+def prefill(lib, d, qn=A16, qr=A16, cache=A16, bt=A16, sl=A16, k=A16, v=A16, out=A16, lse=A16, ws=A16, wsb=32):
+    return lib.mla_prefill_attend(ctypes.byref(d), qn, qr, cache, bt, sl, k, v, out, lse, ws, wsb, None)
+
+
+def decompress(lib, d, cache=A16, bt=A16, sl=A16, wk=A16, wv=A16, k=A16, v=A16, ws=A16, wsb=32):
+    return lib.mla_decompress_kv(ctypes.byref(d), cache, bt, sl, wk, wv, k, v, ws, wsb, None)
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("d_hc", 64, -2), ("G", 3, -2), ("H", 24, -2), ("B", 0, -1), ("Lq", 0, -1), ("scale", 0.0, -1),
+    ("Lq", 1 << 20, -1)])  # more new tokens than the table can hold
+def test_decompress_branch_checks_dims(lib, field, value, code):
+    d = dims()
+    setattr(d, field, value)
+    n = ctypes.c_size_t()
+    assert lib.mla_decompressed_kv_size(ctypes.byref(d), ctypes.byref(n)) == code
+    assert decompress(lib, d) == code
+    assert prefill(lib, d) == code
+
+
+def test_decompress_branch_accepts_long_chunks_and_sizes_its_buffers(lib):
+    """Lq beyond the decode's 4 is fine for the decompress branch, up to the
+    cached length; each of k_nope and v holds B*H*max_pages*64*d_hc bf16."""
+    d = dims(Lq=300, max_pages=8)
+    n = ctypes.c_size_t()
+    assert lib.mla_decompressed_kv_size(ctypes.byref(d), ctypes.byref(n)) == 0
+    assert n.value == d.B * d.H * 8 * 64 * 128 * 2
+    assert mla.PREFILL_THRESHOLD == 256
+
+
+def test_decompress_branch_checks_pointers_alignment_and_workspace(lib):
+    d = dims(Lq=130, max_pages=4)
+    assert decompress(lib, d, cache=None) == -1
+    assert decompress(lib, d, k=A8) == -3
+    assert decompress(lib, d, ws=None) == -4
+    assert decompress(lib, d, wsb=16) == -4
+    assert prefill(lib, d, lse=None) == -1
+    assert prefill(lib, d, qn=A8) == -3
+    assert prefill(lib, d, bt=P(0x10002)) == -3
+    assert prefill(lib, d, wsb=8) == -4
