@@ -53,6 +53,7 @@ WORKLOAD_TEXT = {
     "long": "long-context decode B=16 Lq=1 H=128 seq U[32768,65536] shuffled pages",
     "spec": "speculative decode B=64 Lq=2 causal H=128 seq U[1024,16384] shuffled pages",
     "gla": "grouped-latent decode G=2 B=32 Lq=1 H=128 seq 8192 contiguous",
+    "prefill": "decompress branch: a 1024-token chunk after 3072 cached tokens, B=1 H=128",
 }
 
 
@@ -266,6 +267,120 @@ def cpu_baseline(case, budget_s=12.0):
                       "fraction of the step's work they cover" % (n_pairs, total_t)}
 
 
+def prefill_accounting(seq, Lq, H, G, max_pages):
+    """Algorithmic FLOPs and bytes of the decompress branch: the up-projections
+    of every cached token (K and V: 2 * 2 * 128 * d_g per token and head)
+    and causal attention (2 * (128 + 64) + 2 * 128 per visible (query, key)
+    pair and head); bytes: the cache rows, both weights, K and V written
+    (whole pages) and read (the pages some query sees), queries in, output
+    out."""
+    d_g = 512 // G
+    tok = sum(seq)
+    pages = sum((n + 63) // 64 for n in seq)
+    dec_flops = tok * H * 2 * 2 * 128 * d_g
+    pairs = sum(sum(n - Lq + l + 1 for l in range(Lq)) for n in seq)
+    att_flops = pairs * H * (2 * 192 + 2 * 128)
+    kv = pages * 64 * H * 128 * 2 * 2
+    dec_bytes = tok * 1152 + 2 * H * 128 * d_g * 2 + kv
+    att_bytes = kv + pages * 64 * 64 * 2 + len(seq) * Lq * H * (192 + 128) * 2 + len(seq) * Lq * H * 4
+    return dec_flops, att_flops, dec_bytes, att_bytes
+
+
+def run_prefill(args, world, rank, local):
+    """The decompress branch timed as a step: mla_decompress_kv then
+    mla_prefill_attend, one CUDA-graph replay per step, each kernel also
+    timed alone (graphs of one launch)."""
+    import torch
+    import mla_latent_kv_10_gb300 as mla
+    from mla_latent_kv_10_gb300.inputs import workload
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    mla.load_library()
+    case = workload("prefill")
+    d = case.dims
+    seq = case.seq_lens.tolist()
+    t = {k: v.to(dev) for k, v in case.tensors().items()}
+    bufs = mla.PrefillBuffers(d, dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def dec():
+        mla.mla_decompress_kv(d, t["cache"], t["block_table"], t["seq_lens"], t["W_UK"], t["W_UV"], bufs.k_nope,
+                              bufs.v, bufs.workspace)
+
+    def att():
+        mla.mla_prefill_attend(d, t["q_nope"], t["q_rope"], t["cache"], t["block_table"], t["seq_lens"],
+                               bufs.k_nope, bufs.v, bufs.out, bufs.lse, bufs.workspace)
+
+    for _ in range(args.warmup):
+        dec()
+        att()
+    torch.cuda.synchronize(dev)
+    status = mla.mla_get_device_status(bufs.workspace, stream)
+    if status != 0:
+        raise SystemExit("device status after warm-up: %s" % mla.mla_status_string(status))
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    graphs = {k: torch.cuda.CUDAGraph() for k in ("step", "dec", "att")}
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graphs["step"], stream=side):
+            dec()
+            att()
+        with torch.cuda.graph(graphs["dec"], stream=side):
+            dec()
+        with torch.cuda.graph(graphs["att"], stream=side):
+            att()
+    stream.wait_stream(side)
+    torch.cuda.synchronize(dev)
+    for g in graphs.values():
+        for _ in range(max(3, args.warmup)):
+            g.replay()
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    ms = {}
+    for k in ("step", "dec", "att"):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            graphs[k].replay()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms[k] = e0.elapsed_time(e1) / args.steps
+    clocks = sampler.stop()
+    status = mla.mla_get_device_status(bufs.workspace, stream)
+    peaks, peak_src = load_peaks()
+    dec_flops, att_flops, dec_bytes, att_bytes = prefill_accounting(seq, d["Lq"], d["H"], d["G"], d["max_pages"])
+    if rank != 0:
+        return
+    tf = lambda f, m: f / (m * 1e-3) / 1e12
+    line = {
+        "metric": "MLA prefill (decompress branch) TFLOP/s", "value": tf(dec_flops + att_flops, ms["step"]),
+        "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms["step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) cache and queries, N(0,1/d_g) weights)",
+        "config": {"workload": WORKLOAD_TEXT["prefill"], "B": d["B"], "Lq": d["Lq"], "H": d["H"], "G": d["G"],
+                   "seq_len": seq, "l2": "K and V (%.0f MB each) exceed L2" % (bufs.k_nope.numel() * 2 / 1e6)},
+        "kernels": {
+            "decompress": {"ms": ms["dec"], "tflops": tf(dec_flops, ms["dec"]),
+                           "tensor_frac": tf(dec_flops, ms["dec"]) / peaks["bf16_tflops"],
+                           "gbs": dec_bytes / (ms["dec"] * 1e-3) / 1e9, "flops": dec_flops, "bytes": dec_bytes},
+            "attend": {"ms": ms["att"], "tflops": tf(att_flops, ms["att"]),
+                       "tensor_frac": tf(att_flops, ms["att"]) / peaks["bf16_tflops"],
+                       "gbs": att_bytes / (ms["att"] * 1e-3) / 1e9, "flops": att_flops, "bytes": att_bytes},
+            "timing": "events around replays of one-launch graphs",
+        },
+        "roofline": {"bound": "tensor", "achieved": tf(att_flops, ms["att"]), "peak": peaks["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": tf(att_flops, ms["att"]) / peaks["bf16_tflops"], "traffic": None,
+                     "kernel": "prefill_attn_kernel", "peak_source": peak_src},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+        "device_status": mla.mla_status_string(status),
+    }
+    print(json.dumps(line))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -278,6 +393,13 @@ def main():
     ap.add_argument("--fused", action="store_true", help="one fused combine + projection launch")
     args = ap.parse_args()
     world, rank, local = dist_env()
+    if args.workload == "prefill":
+        if args.impl == "reference":
+            if rank == 0:
+                print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the decode "
+                                  "workloads; the prefill line is a supplementary measurement"}))
+            return
+        return run_prefill(args, world, rank, local)
     if args.impl == "reference":
         return run_reference(args, world, rank)
 

@@ -73,12 +73,14 @@ constexpr int kTile = 64 * 64 * 2;  // a 64-row x 64-column bf16 box, 128-byte s
 // ---------------------------------------------------------------- decompress
 // One CTA per (head h, two pages of sequence b): M = 128 tokens, N = 128
 // output values, K = d_g latent columns streamed in 64-column chunks
-// through a 3-slot ring.  A slot holds the two pages' rows of the chunk
+// through a 2-slot ring.  A slot holds the two pages' rows of the chunk
 // (two 64-row boxes, 16 KiB) and the chunk of W_UK[h] and of W_UV[h]
 // (128 x 64 each, K-major, 16 KiB each).  D_K in tensor-memory columns
 // 0..127, D_V in 128..255.  Thread 0 issues copies and MMAs; the four warps
-// (tensor-memory lane = token) store the rows.
-constexpr int kDcSlots = 3, kDcSlot = 2 * kTile + 2 * 2 * kTile;  // 48 KiB
+// (tensor-memory lane = token) store the rows.  Two slots (96 KiB) let two
+// CTAs share an SM, so one's copies overlap the other's MMAs and stores
+// (three slots, one CTA per SM, measured 35 % slower).
+constexpr int kDcSlots = 2, kDcSlot = 2 * kTile + 2 * 2 * kTile;  // 48 KiB
 constexpr int kDcSmem = kDcSlots * kDcSlot + 1024;
 template <int DG>
 __global__ void __launch_bounds__(128)
@@ -215,7 +217,8 @@ __global__ void __launch_bounds__(128)
 //              and v (two boxes) into a 3-stage ring;
 //   warp 5     MMA issuer (lane 0): S(p+1) = Q . K^T is issued before
 //              P(p) . V so that the tensor pipe works while the softmax
-//              does.
+//              does.  (Two softmax threads per row, 32 keys each, measured
+//              4 % slower.)
 // Tensor memory: O (128 columns) | S0, S1 (64 each).
 constexpr int kAtStages = 3;
 constexpr int kAtQ = 3 * 2 * kTile;              // 128 rows x 192 columns: three 128 x 64 boxes, 48 KiB

@@ -34,6 +34,8 @@ WORKLOADS = {
     "spec": dict(index=4, B=64, Lq=2, H=128, G=1, seq_range=(1024, 16384), table="perm"),
     # grouped latent (GLA): G=2 groups of 64 heads, 256-d latent each + shared k_R
     "gla": dict(index=5, B=32, Lq=1, H=128, G=2, seq_lens=[8192] * 32, table="contig"),
+    # a long query chunk (the decompress branch): 1024 new tokens after 3072 cached ones, H=128
+    "prefill": dict(index=6, B=1, Lq=1024, H=128, G=1, seq_lens=[4096], table="contig"),
 }
 
 
