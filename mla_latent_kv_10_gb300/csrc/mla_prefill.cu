@@ -207,7 +207,7 @@ __global__ void __launch_bounds__(128)
 }
 
 // ---------------------------------------------------------------- attend
-// One CTA per (128 query rows of head h of sequence b), 192 threads:
+// One CTA per (128 query rows of head h of sequence b), 224 threads:
 //   warps 0-3  softmax: thread = query row = tensor-memory lane; the whole
 //              row's 64 keys of a page, online softmax in fp32 (O is
 //              rescaled only when the row maximum has grown by 2^8),
@@ -215,10 +215,11 @@ __global__ void __launch_bounds__(128)
 //   warp 4     TMA producer (lane 0): the query tile once, then per page
 //              the 64 keys' k_nope (two boxes), k_R (from the cache row)
 //              and v (two boxes) into a 3-stage ring;
-//   warp 5     MMA issuer (lane 0): S(p+1) = Q . K^T is issued before
-//              P(p) . V so that the tensor pipe works while the softmax
-//              does.  (Two softmax threads per row, 32 keys each, measured
-//              4 % slower.)
+//   warps 5, 6 the QK and the P.V issuers (lane 0 each): S(p+1) = Q . K^T
+//              waits only for its page and score buffer, so the tensor pipe
+//              works while the softmax does.  (One thread issuing both,
+//              QK(p+2) queued behind P(p) . V, measured slower; two softmax
+//              threads per row, 32 keys each, measured 4 % slower.)
 // Tensor memory: O (128 columns) | S0, S1 (64 each).
 constexpr int kAtStages = 3;
 constexpr int kAtQ = 3 * 2 * kTile;              // 128 rows x 192 columns: three 128 x 64 boxes, 48 KiB
@@ -244,7 +245,7 @@ __device__ __forceinline__ float at_ex2(float x) {
   return y;
 }
 
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(224, 1)
     prefill_attn_kernel(const __grid_constant__ CUtensorMap tmQN, const __grid_constant__ CUtensorMap tmQR,
                         const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                         const __grid_constant__ CUtensorMap tmC, const AtArgs a) {
@@ -272,7 +273,7 @@ __global__ void __launch_bounds__(192, 1)
     abort_flag = 0;
     for (int s = 0; s < kAtStages; ++s) {
       mbar_init(bar(full[s]), 1);
-      mbar_init(bar(empty[s]), 1);
+      mbar_init(bar(empty[s]), 2);  // the K half (QK done) and the V half (P.V done)
     }
     mbar_init(bar(q_full), 1);
     for (int s = 0; s < 2; ++s) {
@@ -281,7 +282,7 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(bar(p_full[s]), 128);
       mbar_init(bar(o_done[s]), 1);
     }
-    mbar_init(bar(drain), 1);
+    mbar_init(bar(drain), 2);
     fence_mbar_init();
     tma_prefetch_desc(&tmQN);
     tma_prefetch_desc(&tmQR);
@@ -329,38 +330,42 @@ __global__ void __launch_bounds__(192, 1)
     }
     __syncwarp();
   } else if (warp == 5) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ QK issuer
+    // S(p & 1) = Q . K(p)^T once page p landed and the softmax has read
+    // S(p - 2); the stage's K half is free once these MMAs are done.
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16(128, 64, false, false);
-      constexpr uint32_t idesc_pv = idesc_bf16(128, 128, false, true);
-      auto qk = [&](int p) {  // S(p & 1) = Q . K(p)^T: 12 K steps of 16 over 192 columns
+      bool ok = mbar_wait(bar(q_full), 0, abort, lim);
+      for (int p = 0; ok && p < npg; ++p) {
         const int st = p % kAtStages;
+        if (!(ok = mbar_wait(bar(full[st]), (p / kAtStages) & 1, abort, lim))) break;
+        if (p >= 2 && !(ok = mbar_wait(bar(s_free[p & 1]), ((p - 2) >> 1) & 1, abort, lim))) break;
+        tc_fence_after();
 #pragma unroll
-        for (int j = 0; j < 12; ++j) {
+        for (int j = 0; j < 12; ++j) {  // 12 K steps of 16 over 192 columns
           const uint64_t ad = sdesc_sw128(sQ + (j >> 2) * 2 * kTile + (j & 3) * 32, 16, 1024);
           const uint64_t bd = sdesc_sw128(sK(st) + (j >> 2) * kTile + (j & 3) * 32, 16, 1024);
           mma_ss(tmem + 128 + 64 * (p & 1), ad, bd, idesc_qk, j > 0 ? 1u : 0u);
         }
         mma_commit(bar(s_full[p & 1]));
-      };
-      bool ok = mbar_wait(bar(q_full), 0, abort, lim) && mbar_wait(bar(full[0]), 0, abort, lim);
-      if (ok) {
-        tc_fence_after();
-        qk(0);
+        mma_commit(bar(empty[st]));
       }
+      if (!ok) fail();
+    }
+    __syncwarp();
+  } else if (warp == 6) {
+    // ------------------------------------------------------------ P.V issuer
+    // O += P(p) . V(p) once the softmax has written P(p); the stage's V half
+    // and P slot p & 1 are free once these MMAs are done.
+    if (lane == 0) {
+      constexpr uint32_t idesc_pv = idesc_bf16(128, 128, false, true);
+      bool ok = true;
       for (int p = 0; ok && p < npg; ++p) {
-        if (p + 1 < npg) {
-          const int st = (p + 1) % kAtStages;
-          if (!(ok = mbar_wait(bar(full[st]), ((p + 1) / kAtStages) & 1, abort, lim))) break;
-          if (p + 1 >= 2 && !(ok = mbar_wait(bar(s_free[(p + 1) & 1]), ((p - 1) >> 1) & 1, abort, lim))) break;
-          tc_fence_after();
-          qk(p + 1);
-        }
         if (!(ok = mbar_wait(bar(p_full[p & 1]), (p >> 1) & 1, abort, lim))) break;
         tc_fence_after();
         const int st = p % kAtStages;
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {  // O += P(p) . V(p): 64 keys = 4 K steps
+        for (int kk = 0; kk < 4; ++kk) {  // 64 keys = 4 K steps
           const uint64_t ad = sdesc_sw128(sP(p & 1) + kk * 32, 16, 1024);
           const uint64_t bd = sdesc_sw128(sV(st) + kk * 2048, kTile, 1024);
           mma_ss(tmem, ad, bd, idesc_pv, (p > 0 || kk > 0) ? 1u : 0u);
@@ -482,7 +487,7 @@ __global__ void __launch_bounds__(192, 1)
     for (int p = issued > kAtStages ? issued - kAtStages : 0; p < issued; ++p)
       if (!mbar_wait_quiet(bar(full[p % kAtStages]), (p / kAtStages) & 1)) set_status(a.ws, MLA_ERR_TIMEOUT);
     if (!mbar_wait_quiet(bar(q_full), 0)) set_status(a.ws, MLA_ERR_TIMEOUT);
-  } else if (warp == 5 && lane == 0) {
+  } else if ((warp == 5 || warp == 6) && lane == 0) {  // each issuer's MMAs done
     mma_commit(bar(drain));
     if (!mbar_wait_quiet(bar(drain), 0)) set_status(a.ws, MLA_ERR_TIMEOUT);
   }
@@ -550,7 +555,7 @@ cudaError_t launch_prefill_attend(const CUtensorMap& tmQN, const CUtensorMap& tm
   a.num_pages = num_pages;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.wait_ns = wait_ns;
-  dim3 grid((Lq + kRowsPerCta - 1) / kRowsPerCta, H, B), block(192);
+  dim3 grid((Lq + kRowsPerCta - 1) / kRowsPerCta, H, B), block(224);
   prefill_attn_kernel<<<grid, block, kAtSmem, st>>>(tmQN, tmQR, tmK, tmV, tmC, a);
   return cudaGetLastError();
 }
