@@ -155,7 +155,13 @@ int mla_decode_workspace_size(const mla_dims* dims, size_t* bytes);
  * log-sum-exp lse = log sum_s exp(score_s) (-inf for an empty range).
  *
  * q_cat    bf16 [B,Lq,H,d_g+d_R] (from mla_absorb_q), 16-byte aligned
- * kv_cache bf16 [num_pages, P, d_c+d_R], 16-byte aligned
+ * kv_cache bf16 [num_pages, P, d_c+d_R], 16-byte aligned.  Whole pages are
+ *          read: the rows of a sequence's last page past its end take part
+ *          in the tensor-core products with weight 0, so they must hold
+ *          finite values of the cache's usual size (zeros, or rows left
+ *          from earlier sequences); a NaN there would reach the output
+ *          (0 * NaN), a huge value would coarsen the partial scores' 16-bit
+ *          scale.  (The decompress branch has no such condition.)
  * block_table int32 [B, max_pages_per_seq]; entries past ceil(n/P) unused
  * seq_lens int32 [B]
  * o_part  fp32 scratch of slots * Lq*H * d_c floats for mla_combine_splits

@@ -334,3 +334,65 @@ def test_fused_combine_project_without_optional_outputs():
     mla.mla_combine_project(c.dims, bufs.o_part, bufs.lse_part, bufs.workspace, t["W_UV"], bufs.out)
     assert mla.mla_get_device_status(bufs.workspace) == 0
     assert torch.equal(bufs.out.cpu(), ref["out"])
+
+
+# ---------------------------------------------------------------- cache rows past a sequence's end
+
+def _fill_tails(c, value=None, seed=0):
+    """Fill every cache row past a sequence's end on its last page: with
+    `value`, or (value None) with stale rows of another part of the cache,
+    as a page pool that is reused would hold."""
+    gen = torch.Generator().manual_seed(seed)
+    for b in range(c.dims["B"]):
+        n = int(c.seq_lens[b])
+        if n % 64:
+            page = int(c.block_table[b, (n - 1) // 64])
+            if value is None:
+                src = torch.randint(0, c.dims["num_pages"], (64 - n % 64,), generator=gen)
+                c.cache[page, n % 64:, :] = c.cache[src, torch.arange(64 - n % 64) % 64, :]
+            else:
+                c.cache[page, n % 64:, :] = value
+
+
+def _tail_case(shape):
+    if shape == "mla":
+        return make_case(B=3, Lq=1, H=128, seq_lens=[70, 1, 333], table="perm", seed=61)
+    if shape == "mla_lq2":
+        return make_case(B=2, Lq=2, H=64, seq_lens=[130, 7], table="perm", seed=62)
+    return make_case(B=2, Lq=1, H=128, G=2, seq_lens=[100, 513], table="perm", seed=63)
+
+
+@pytest.mark.parametrize("shape", ["mla", "mla_lq2", "gla"])
+def test_decode_with_stale_rows_past_sequence_end(shape):
+    """The decode reads whole pages: rows past a sequence's end take part in
+    the MMAs (masked, weight 0).  With stale rows there (a reused page pool)
+    the results match the oracle, which reads only the sequence's own rows.
+    (Such rows must hold finite values of the cache's usual size: a NaN
+    there would reach O through 0 * NaN, and a huge value would set the
+    16-bit exchange's row scale.)"""
+    c = _tail_case(shape)
+    _fill_tails(c, None, seed=5)
+    got = run_gpu(c)
+    assert got["status"] == 0
+    check_case(c, got, sample_pairs(c, 8))
+
+
+@pytest.mark.parametrize("value", [float("nan"), 3e38, -3e38])
+@pytest.mark.parametrize("shape", ["mla", "mla_lq2", "gla"])
+def test_decompress_branch_ignores_anything_past_sequence_end(shape, value):
+    """The decompress branch writes zeros for K and V past a sequence's end
+    and masks those scores, so even NaN or huge values in the cache rows
+    there leave out and lse equal to the oracle's."""
+    c = _tail_case(shape)
+    _fill_tails(c, value)
+    t = {k: v.cuda() for k, v in c.tensors().items()}
+    bufs = mla.PrefillBuffers(c.dims)
+    mla.prefill_step(c.dims, bufs, t["q_nope"], t["q_rope"], t["W_UK"], t["W_UV"], t["cache"], t["block_table"],
+                     t["seq_lens"])
+    assert mla.mla_get_device_status(bufs.workspace) == 0
+    pairs = sample_pairs(c, 8)
+    ref_out, _, ref_lse = oracle.decode(c.dims, **c.tensors(), sel=pairs)
+    bi = np.array([p[0] for p in pairs])
+    hi = np.array([p[1] for p in pairs])
+    assert_close(bufs.out.cpu().to(torch.float64).numpy()[bi, :, hi], ref_out[bi, :, hi], "prefill out")
+    assert_close(bufs.lse.cpu().to(torch.float64).numpy()[bi, :, hi], ref_lse[bi, :, hi], "prefill lse")
