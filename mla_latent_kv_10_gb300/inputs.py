@@ -11,6 +11,14 @@ Shapes and distributions follow the MLA operator write-up
 key, 576 bf16) and the 64-token page; the DeepSeek-V2/V3 dims of §3
 (128 heads, 128-d content head) set H and d_hc.  Queries and cache entries are
 N(0, 1); the projection matrices are N(0, 1/d_g) so logits have unit scale.
+
+An FP8 cache (kv="fp8") is drawn as its bytes: per latent code a random
+sign, an exponent field from a rounded normal (mean 13, sd 1.5, clipped to
+0..15) and a uniform mantissa (never the NaN pattern), so the code values
+spread over the E4M3 range as those of a Gaussian block scaled to fill it
+do; per token and 128-column block a scale 2^k, k uniform in -8..-6 (the
+latent then has about the size of the bf16 cache's); the RoPE key N(0, 1)
+in bf16.  Row layout: 512 codes | 64 bf16 | 4 fp32 scales (656 bytes).
 """
 from __future__ import annotations
 
@@ -21,6 +29,7 @@ import torch
 
 D_HC, D_C, D_R, PAGE = 128, 512, 64, 64
 SEED_BASE = 20261200
+FP8_ROW = D_C + 2 * D_R + 4 * (D_C // 128)  # bytes of an FP8 cache row
 
 # name -> (index, spec).  Index i gives seed SEED_BASE + i.
 WORKLOADS = {
@@ -45,7 +54,7 @@ class Case:
     dims: dict
     q_nope: torch.Tensor       # bf16 [B,Lq,H,d_hc]
     q_rope: torch.Tensor       # bf16 [B,Lq,H,d_R]
-    cache: torch.Tensor        # bf16 [num_pages,P,d_c+d_R]
+    cache: torch.Tensor        # bf16 [num_pages,P,d_c+d_R], or uint8 [num_pages,P,656] (FP8)
     W_UK: torch.Tensor         # bf16 [H,d_hc,d_g]
     W_UV: torch.Tensor         # bf16 [H,d_hc,d_g]
     block_table: torch.Tensor  # int32 [B,max_pages] (-1 = unused)
@@ -61,7 +70,7 @@ class Case:
 def make_case(name: str = "custom", *, B: int, Lq: int = 1, H: int = 128, G: int = 1,
               seq_lens=None, seq_range=None, table: str = "contig", seed: int,
               max_pages: int | None = None, extra_pages: int = 0,
-              q_zero: bool = False, causal: int = 1) -> Case:
+              q_zero: bool = False, causal: int = 1, kv: str = "bf16") -> Case:
     """Draw one synthetic decode problem.
 
     seq_lens: explicit list of lengths, or seq_range=(lo, hi) inclusive uniform.
@@ -69,6 +78,7 @@ def make_case(name: str = "custom", *, B: int, Lq: int = 1, H: int = 128, G: int
     pool of all needed pages handed out in a seeded random order).
     extra_pages: unused pages appended to the pool (never referenced).
     q_zero: all-zero queries (uniform attention), a test special case.
+    kv: "bf16" (rows of 576 bf16) or "fp8" (rows of 656 bytes, see above).
     """
     gen = torch.Generator(device="cpu").manual_seed(int(seed))
     if seq_lens is None:
@@ -99,7 +109,12 @@ def make_case(name: str = "custom", *, B: int, Lq: int = 1, H: int = 128, G: int
     if q_zero:
         q_nope.zero_()
         q_rope.zero_()
-    cache = normal((num_pages, PAGE, D_C + D_R), 1.0)
+    if kv == "bf16":
+        cache = normal((num_pages, PAGE, D_C + D_R), 1.0)
+    elif kv == "fp8":
+        cache = fp8_cache(gen, num_pages)
+    else:
+        raise ValueError(kv)
     w_std = 1.0 / math.sqrt(d_g)
     W_UK = normal((H, D_HC, d_g), w_std)
     W_UV = normal((H, D_HC, d_g), w_std)
@@ -122,7 +137,29 @@ def make_case(name: str = "custom", *, B: int, Lq: int = 1, H: int = 128, G: int
                 scale=1.0 / math.sqrt(D_HC + D_R), causal=int(causal))
     return Case(name=name, dims=dims, q_nope=q_nope, q_rope=q_rope, cache=cache,
                 W_UK=W_UK, W_UV=W_UV, block_table=bt, seq_lens=seq.to(torch.int32),
-                meta=dict(seed=int(seed), table=table))
+                meta=dict(seed=int(seed), table=table, kv=kv))
+
+
+def fp8_rows(codes: torch.Tensor, rope: torch.Tensor, scales: torch.Tensor) -> torch.Tensor:
+    """Pack FP8 cache rows: codes uint8 [..., 512], rope bf16 [..., 64],
+    scales fp32 [..., 4] -> uint8 [..., 656]."""
+    lead = codes.shape[:-1]
+    return torch.cat([codes, rope.contiguous().view(torch.uint8).reshape(*lead, 2 * D_R),
+                      scales.contiguous().view(torch.uint8).reshape(*lead, 16)], dim=-1).contiguous()
+
+
+def fp8_cache(gen: torch.Generator, num_pages: int) -> torch.Tensor:
+    """Random FP8 cache pages (uint8 [num_pages, P, 656]); see the module text."""
+    shape = (num_pages, PAGE, D_C)
+    sign = torch.randint(0, 2, shape, generator=gen, dtype=torch.int32)
+    expo = torch.randn(shape, generator=gen).mul_(1.5).add_(13.0).round_().clamp_(0, 15).to(torch.int32)
+    mant = torch.randint(0, 8, shape, generator=gen, dtype=torch.int32)
+    mant = torch.where((expo == 15) & (mant == 7), torch.full_like(mant, 6), mant)  # 0x7f / 0xff are NaN
+    codes = (sign * 128 + expo * 8 + mant).to(torch.uint8)
+    k = torch.randint(-8, -5, (num_pages, PAGE, D_C // 128), generator=gen, dtype=torch.int32)
+    scales = torch.pow(2.0, k.to(torch.float32))
+    rope = torch.randn((num_pages, PAGE, D_R), generator=gen, dtype=torch.float32).to(torch.bfloat16)
+    return fp8_rows(codes, rope, scales)
 
 
 def workload(name: str, **override) -> Case:

@@ -37,6 +37,10 @@ def load():
         lib.mla_oracle_project_uv.argtypes = [I] * 4 + [_u16p] * 2 + [_f64p]
         lib.mla_oracle_lse_merge.argtypes = [I] * 3 + [_f64p] * 4
         lib.mla_oracle_num_threads.restype = I
+        lib.mla_oracle_e4m3.argtypes = [I]
+        lib.mla_oracle_e4m3.restype = D
+        lib.mla_oracle_dequant_fp8.argtypes = [ctypes.c_long, I, I, I, ctypes.POINTER(ctypes.c_uint8), _f64p]
+        lib.mla_oracle_dequant_fp8.restype = I
         _lib = lib
     return _lib
 
@@ -172,6 +176,60 @@ def lse_merge(o_part, lse):
     o, L = np.empty((R, D)), np.empty(R)
     load().mla_oracle_lse_merge(S, R, D, _p(o_part, _f64p), _p(lse, _f64p), _p(o, _f64p), _p(L, _f64p))
     return o, L
+
+
+def e4m3(code: int) -> float:
+    """Value of one FP8 E4M3 code (OCP 8-bit floating point; NaN for 0x7f, 0xff)."""
+    return load().mla_oracle_e4m3(int(code))
+
+
+FP8_ROW_BYTES = 512 + 2 * 64 + 4 * 4  # 512 codes | 64 bf16 RoPE key | 4 fp32 scales
+
+
+def dequant_fp8(cache8, d_c: int = 512, d_R: int = 64, blk: int = 128):
+    """FP8 cache rows (uint8 tensor / array [..., 656]) -> (latent float64
+    [..., d_c] = e4m3(code) * scale of the code's blk-column block, RoPE key
+    as bf16 bits uint16 [..., d_R])."""
+    a = cache8 if isinstance(cache8, np.ndarray) else cache8.detach().to("cpu").contiguous().numpy()
+    a = np.ascontiguousarray(a, dtype=np.uint8)
+    lead = a.shape[:-1]
+    n = int(np.prod(lead)) if lead else 1
+    assert a.shape[-1] == d_c + 2 * d_R + 4 * (d_c // blk), a.shape
+    lat = np.empty(lead + (d_c,))
+    rc = load().mla_oracle_dequant_fp8(n, d_c, d_R, blk, _p(a, ctypes.POINTER(ctypes.c_uint8)), _p(lat, _f64p))
+    if rc != 0:
+        raise ValueError("bad FP8 layout")
+    rope = np.ascontiguousarray(a[..., d_c:d_c + 2 * d_R]).view(np.uint16)
+    return lat, rope
+
+
+def fp8_as_bf16_cache(cache8, d_c: int = 512, d_R: int = 64, blk: int = 128) -> np.ndarray:
+    """The bf16 cache (bits, uint16 [..., d_c + d_R]) holding exactly the
+    dequantised latent of an FP8 cache and its RoPE key.  Every E4M3 value
+    times a power-of-two scale has at most 4 significant bits, so it is a
+    bf16 value unless it leaves the bf16 range; this is checked, never
+    rounded."""
+    lat, rope = dequant_fp8(cache8, d_c, d_R, blk)
+    f32 = lat.astype(np.float32)
+    if not np.array_equal(f32.astype(np.float64), lat, equal_nan=True):
+        raise ValueError("dequantised latent not exact in fp32")
+    u = f32.view(np.uint32)
+    if np.any(u & 0xFFFF):
+        raise ValueError("dequantised latent not exact in bf16 (a scale outside the power-of-two range)")
+    return np.ascontiguousarray(np.concatenate([(u >> 16).astype(np.uint16), rope], axis=-1))
+
+
+def decode_fp8(dims, q_nope, q_rope, W_UK, W_UV, cache, block_table, seq_lens, sel=None, nthreads=0):
+    """decode() over an FP8 cache (uint8 [num_pages, P, 656]): the attention
+    of the dequantised latent, c = e4m3(code) * scale, and the bf16 RoPE key."""
+    return decode(dims, q_nope, q_rope, W_UK, W_UV, fp8_as_bf16_cache(cache), block_table, seq_lens,
+                  sel=sel, nthreads=nthreads)
+
+
+def decode_latent_fp8(dims, q_cat, cache, block_table, seq_lens, sel=None, nthreads=0):
+    """decode_latent() over an FP8 cache (uint8 [num_pages, P, 656])."""
+    return decode_latent(dims, q_cat, fp8_as_bf16_cache(cache), block_table, seq_lens, sel=sel,
+                         nthreads=nthreads)
 
 
 def default_scale(d_hc: int = 128, d_R: int = 64) -> float:

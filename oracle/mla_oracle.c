@@ -42,6 +42,40 @@ static double bf16_to_double(uint16_t v) {
   return (double)f;
 }
 
+/*
+ * One FP8 code, OCP 8-bit floating point E4M3 ("OFP8" specification): bit 7
+ * sign, bits 6..3 exponent with bias 7, bits 2..0 mantissa.  Exponent 0
+ * holds the subnormals m/8 * 2^-6; S.1111.111 is NaN; there are no
+ * infinities.  Returns the value in double (NaN for the two NaN codes).
+ */
+double mla_oracle_e4m3(int code) {
+  const int s = (code >> 7) & 1, e = (code >> 3) & 15, m = code & 7;
+  if (e == 15 && m == 7) return NAN;
+  const double v = e == 0 ? ldexp((double)m / 8.0, -6) : ldexp(1.0 + (double)m / 8.0, e - 7);
+  return s ? -v : v;
+}
+
+/*
+ * Latent of FP8 cache rows (the reading of the low-precision cache the MLA
+ * operator write-up names in its introduction and §5 tail: codes
+ * dequantised on load).  Row r of `rows` (row_bytes each) holds d_c E4M3
+ * codes, then d_R bf16 (the RoPE key, not read here), then d_c / blk fp32
+ * scales; latent[r][i] = e4m3(code[i]) * scale[i / blk], in double.
+ */
+int mla_oracle_dequant_fp8(long n_rows, int d_c, int d_R, int blk, const uint8_t* rows, double* latent) {
+  if (blk < 1 || d_c % blk != 0) return -1;
+  const long row_bytes = d_c + 2L * d_R + 4L * (d_c / blk);
+  for (long r = 0; r < n_rows; ++r) {
+    const uint8_t* row = rows + r * row_bytes;
+    for (int i = 0; i < d_c; ++i) {
+      float sc;
+      memcpy(&sc, row + d_c + 2 * d_R + 4 * (i / blk), sizeof sc);
+      latent[r * d_c + i] = mla_oracle_e4m3(row[i]) * (double)sc;
+    }
+  }
+  return 0;
+}
+
 /* Pointer to the cache row (d_c + d_R bf16) of token s of sequence b. */
 static const uint16_t* cache_row(const uint16_t* cache, const int32_t* block_table,
                                  int max_pages, int P, int row_w, int b, int s) {
