@@ -23,7 +23,12 @@ queries, outputs), TFLOP/s, tokens/s and the decode kernel's roofline ride
 along.  `--impl reference` times the fp64 CPU oracle on a bounded sample of
 the same workload instead.
 
-Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+--kv fp8 runs the same step over the FP8 cache (mla_decode_paged_fp8: E4M3
+latent codes with power-of-two block scales, bf16 RoPE key, 656 B a token);
+`value` then counts those bytes.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--kv bf16|fp8]
+                       [--impl ours|reference]
 For N > 1 launch with torchrun; each rank runs its own batch (weak scaling, no
 collective on the data path).
 """
@@ -57,6 +62,11 @@ WORKLOAD_TEXT = {
 }
 
 
+def workload_text(args):
+    text = WORKLOAD_TEXT[args.workload]
+    return text + ", FP8 E4M3 cache" if getattr(args, "kv", "bf16") == "fp8" else text
+
+
 DECODE_SOURCES = ("mla_latent_kv_10_gb300/csrc/mla_decode.cu", "mla_latent_kv_10_gb300/csrc/ptx.cuh",
                   "mla_latent_kv_10_gb300/csrc/mla_internal.h", "include/mla.h")
 
@@ -72,10 +82,11 @@ def decode_source_sha():
     return h.hexdigest()
 
 
-def decode_traffic(workload):
+def decode_traffic(workload, kv="bf16"):
     """DRAM bytes per decode launch from the committed ncu summary of this
     workload, if it was taken on the current decode sources (else None)."""
-    path = os.path.join(ROOT, "profiles", "decode_kernel_%s.json" % workload)
+    name = workload if kv == "bf16" else "%s_%s" % (workload, kv)
+    path = os.path.join(ROOT, "profiles", "decode_kernel_%s.json" % name)
     if not os.path.exists(path):
         return None
     rec = json.load(open(path))
@@ -145,7 +156,7 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def roofline_entry(dec_bytes, dec_flops, dec_ms, peaks, traffic, peak_src):
+def roofline_entry(dec_bytes, dec_flops, dec_ms, peaks, traffic, peak_src, kernel="mla_decode_paged"):
     """The binding roof of the decode kernel: the larger of its HBM fraction
     (algorithmic bytes / time against the measured copy bandwidth) and its
     tensor fraction (algorithmic FLOPs / time against the measured bf16
@@ -158,7 +169,7 @@ def roofline_entry(dec_bytes, dec_flops, dec_ms, peaks, traffic, peak_src):
     else:
         ach, peak, unit, bound = gbs, hbm, "GB/s", "hbm"
     return {"bound": bound, "achieved": ach, "peak": peak, "unit": unit, "frac": ach / peak,
-            "traffic": traffic, "peak_source": peak_src, "kernel": "mla_decode_paged"}
+            "traffic": traffic, "peak_source": peak_src, "kernel": kernel}
 
 
 def max_over_ranks(value, dist, device):
@@ -195,13 +206,18 @@ def run_reference(args, world, rank):
     from mla_latent_kv_10_gb300 import accounting as acc
     from mla_latent_kv_10_gb300.inputs import workload
 
-    case = workload(args.workload)
+    case = workload(args.workload, kv=args.kv)
     d = case.dims
     seq = case.seq_lens.tolist()
     B, H = d["B"], d["H"]
-    kv_bytes = acc.latent_kv_bytes(seq)
+    kv_bytes = acc.latent_kv_bytes(seq, kv=args.kv)
     step_flops = acc.step_flops(seq, d["Lq"], H, d["G"])
     nt = oracle.num_threads()
+    ref_decode = oracle.decode_fp8 if args.kv == "fp8" else oracle.decode
+    tensors = case.tensors()
+    if args.kv == "fp8":  # read the FP8 rows once, outside the timed calls
+        tensors["cache"] = oracle.fp8_as_bf16_cache(case.cache)
+        ref_decode = oracle.decode
     rng = np.random.default_rng(0)
     # size one step's sample so the whole run stays within minutes
     pairs_per_step = max(nt, 1)
@@ -212,7 +228,7 @@ def run_reference(args, world, rank):
         hs = rng.integers(0, H, pairs_per_step)
         sel = list(zip(bs.tolist(), hs.tolist()))
         t0 = time.perf_counter()
-        oracle.decode(d, **case.tensors(), sel=sel, nthreads=nt)
+        ref_decode(d, **tensors, sel=sel, nthreads=nt)
         dt = time.perf_counter() - t0
         frac = sum(seq[b] for b, _ in sel) / (sum(seq) * H)
         if i >= args.warmup:
@@ -226,17 +242,20 @@ def run_reference(args, world, rank):
         "ms_per_step": 1e3 * total / work,  # time the oracle would take for one whole step
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "tflops": step_flops * work / total / 1e12,
-        "config": {"workload": WORKLOAD_TEXT[args.workload], "step": "fused" if args.fused else "four calls", "B": B, "Lq": d["Lq"], "H": H, "G": d["G"],
+        "config": {"workload": workload_text(args), "step": "fused" if args.fused else "four calls", "B": B,
+                   "Lq": d["Lq"], "H": H, "G": d["G"], "kv": args.kv,
                    "parallelism": "replicas" if world > 1 else "single"},
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": nt, "kind": "oracle",
                          "sample": "%d random (sequence, head) pairs per step; metric scaled by the "
-                                   "fraction of the step's work they cover" % pairs_per_step},
+                                   "fraction of the step's work they cover%s" % (
+                                       pairs_per_step, "; the FP8 rows dequantised once before the timed "
+                                       "calls" if args.kv == "fp8" else "")},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
 
 
-def cpu_baseline(case, budget_s=12.0):
+def cpu_baseline(case, budget_s=12.0, kv="bf16"):
     """Oracle on a bounded sample of the workload, scaled to GB/s."""
     import numpy as np
     import oracle
@@ -247,18 +266,21 @@ def cpu_baseline(case, budget_s=12.0):
     nt = oracle.num_threads()
     B, H = d["B"], d["H"]
     rng = np.random.default_rng(1)
-    kv_bytes = acc.latent_kv_bytes(seq)
+    kv_bytes = acc.latent_kv_bytes(seq, kv=kv)
+    tensors = case.tensors()
+    if kv == "fp8":  # the FP8 rows read once (the oracle's reading), then the same decode
+        tensors["cache"] = oracle.fp8_as_bf16_cache(case.cache)
     n_pairs = nt
     sel = list(zip(rng.integers(0, B, n_pairs).tolist(), rng.integers(0, H, n_pairs).tolist()))
     t0 = time.perf_counter()
-    oracle.decode(d, **case.tensors(), sel=sel, nthreads=nt)
+    oracle.decode(d, **tensors, sel=sel, nthreads=nt)
     t1 = time.perf_counter() - t0
     rounds = max(1, int(budget_s / max(t1, 1e-3)) - 1)
     total_t, frac = t1, sum(seq[b] for b, _ in sel) / (sum(seq) * H)
     if rounds > 1 and t1 < budget_s / 2:
         sel2 = list(zip(rng.integers(0, B, n_pairs * rounds).tolist(), rng.integers(0, H, n_pairs * rounds).tolist()))
         t0 = time.perf_counter()
-        oracle.decode(d, **case.tensors(), sel=sel2, nthreads=nt)
+        oracle.decode(d, **tensors, sel=sel2, nthreads=nt)
         total_t += time.perf_counter() - t0
         frac += sum(seq[b] for b, _ in sel2) / (sum(seq) * H)
         n_pairs += len(sel2)
@@ -391,9 +413,12 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--splits", type=int, default=0)
     ap.add_argument("--fused", action="store_true", help="one fused combine + projection launch")
+    ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8"], help="cache format of the decode")
     args = ap.parse_args()
     world, rank, local = dist_env()
     if args.workload == "prefill":
+        if args.kv != "bf16":
+            raise SystemExit("the decompress branch reads the bf16 cache")
         if args.impl == "reference":
             if rank == 0:
                 print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the decode "
@@ -418,29 +443,32 @@ def main():
     mla.load_library()
 
     # every rank decodes a replica of the same batch (weak scaling)
-    case = workload(args.workload)
+    fp8 = args.kv == "fp8"
+    case = workload(args.workload, kv=args.kv)
     d = case.dims
     seq = case.seq_lens.tolist()
     B, Lq, H, G = d["B"], d["Lq"], d["H"], d["G"]
     t = {k: v.to(dev) for k, v in case.tensors().items()}
-    cache_bytes = t["cache"].numel() * 2
+    cache_bytes = t["cache"].numel() * t["cache"].element_size()
     copies = max(1, math.ceil(2.2 * L2_BYTES / cache_bytes))
     caches = [t["cache"]] + [t["cache"].clone() for _ in range(copies - 1)]
     bufs = mla.DecodeBuffers(d, dev)
     stream = torch.cuda.current_stream(dev)
 
-    kv_bytes = acc.latent_kv_bytes(seq)
-    step_bytes = acc.step_bytes(seq, Lq, H, G)
+    kv_bytes = acc.latent_kv_bytes(seq, kv=args.kv)
+    step_bytes = acc.step_bytes(seq, Lq, H, G, kv=args.kv)
     step_flops = acc.step_flops(seq, Lq, H, G)
-    dec_bytes = acc.decode_bytes(seq, Lq, H, G)
+    dec_bytes = acc.decode_bytes(seq, Lq, H, G, kv=args.kv)
     dec_flops = acc.decode_flops(seq, Lq, H, G, causal=bool(d["causal"]))
 
     def pre():
         mla.mla_absorb_q(d, t["q_nope"], t["q_rope"], t["W_UK"], bufs.q_cat)
 
+    decode = mla.mla_decode_paged_fp8 if fp8 else mla.mla_decode_paged
+
     def dec(c):
-        mla.mla_decode_paged(d, bufs.q_cat, caches[c], t["block_table"], t["seq_lens"], args.splits,
-                             bufs.o_part, bufs.lse_part, bufs.workspace)
+        decode(d, bufs.q_cat, caches[c], t["block_table"], t["seq_lens"], args.splits, bufs.o_part,
+               bufs.lse_part, bufs.workspace)
 
     def post():
         if not args.fused:
@@ -580,13 +608,18 @@ def main():
         "value": job_rate(world, kv_bytes, ms) / 1e9,
         "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic (seeded N(0,1) cache and queries, N(0,1/d_g) weights)",
-        "config": {"workload": WORKLOAD_TEXT[args.workload], "step": "fused" if args.fused else "four calls", "B": B, "Lq": Lq, "H": H, "G": G,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp8 e4m3 cache, f16 latent products, fp32 accumulation" if fp8 else "bf16",
+        "data": ("synthetic (seeded random E4M3 codes, power-of-two block scales and N(0,1) RoPE key; "
+                 "N(0,1) queries, N(0,1/d_g) weights)" if fp8 else
+                 "synthetic (seeded N(0,1) cache and queries, N(0,1/d_g) weights)"),
+        "config": {"workload": workload_text(args), "step": "fused" if args.fused else "four calls", "B": B,
+                   "Lq": Lq, "H": H, "G": G, "kv": args.kv,
                    "seq_len_mean": sum(seq) / len(seq), "page_size": 64,
                    "parallelism": "replicas" if world > 1 else "single",
                    "l2": "inputs larger than L2: %d rotating cache copies (%.0f MB)" % (copies, copies * cache_bytes / 1e6)},
-        "value_counts": "latent KV cache bytes read per step (%d B) over the step time" % kv_bytes,
+        "value_counts": "latent KV cache bytes read per step (%d B, %d B a token) over the step time"
+                        % (kv_bytes, acc.row_bytes(args.kv)),
         "step_gbs": job_rate(world, step_bytes, ms) / 1e9,
         "step_bytes": step_bytes,
         "tflops": job_rate(world, step_flops, ms) / 1e12,
@@ -599,7 +632,8 @@ def main():
                           "ms_single_launch_graph": dec_ms_one,
                           "timing": "mean per launch over %d-launch graphs (events around each replay); "
                                     "ms_single_launch_graph: events around one-launch graphs" % DEC_CHAIN},
-        "roofline": roofline_entry(dec_bytes, dec_flops, dec_ms, peaks, decode_traffic(args.workload), peak_src),
+        "roofline": roofline_entry(dec_bytes, dec_flops, dec_ms, peaks, decode_traffic(args.workload, args.kv),
+                                   peak_src, kernel="mla_decode_paged_fp8" if fp8 else "mla_decode_paged"),
         "e2e": {"value": job_rate(world, kv_bytes, e2e_ms) / 1e9, "unit": "GB/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": mla.launches_per_step(case.dims, fused=args.fused) * args.steps,
@@ -613,7 +647,7 @@ def main():
         "device_status": mla.mla_status_string(status),
     }
     if not args.no_cpu_baseline and world == 1:
-        line["cpu_baseline"] = cpu_baseline(case)
+        line["cpu_baseline"] = cpu_baseline(case, kv=args.kv)
     print(json.dumps(line))
     if pg:
         pg.destroy_process_group()

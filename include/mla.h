@@ -86,7 +86,9 @@ typedef enum mla_status {
   MLA_ERR_CUDA = -5,         /* a CUDA runtime / driver call failed        */
   MLA_ERR_BAD_TABLE = -6,    /* device: block_table entry out of range     */
   MLA_ERR_BAD_SEQLEN = -8,   /* device: seq_len < Lq or > max_pages*P      */
-  MLA_ERR_TIMEOUT = -7       /* device: a bounded pipeline wait gave up    */
+  MLA_ERR_TIMEOUT = -7,      /* device: a bounded pipeline wait gave up    */
+  MLA_ERR_RANGE = -9         /* device (FP8 cache): a scale or a query value
+                                outside the range of the f16 arithmetic    */
 } mla_status;
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -180,6 +182,45 @@ int mla_decode_paged(const mla_dims* dims, const void* q_cat,
                      const int32_t* seq_lens, int num_splits, float* o_part,
                      float* lse_part, void* workspace, size_t ws_bytes,
                      void* stream);
+
+/*
+ * mla_decode_paged_fp8 — mla_decode_paged over a latent cache stored in FP8
+ * with the latent dequantised on load.
+ *
+ * Source: the MLA operator write-up (nxmr.cn/news/151634), introduction and
+ * the tail of §5: a low-precision (NVFP4) KV cache read with 16-byte vector
+ * loads from 16-byte aligned pages.  The pages fix neither the format nor
+ * the scales; this entry takes the plainest FP8 reading: OCP e4m3 codes
+ * (bias 7, no infinities, 0x7f/0xff NaN) with one power-of-two scale per
+ * token and 128-column block of the latent; the RoPE key stays bf16.
+ *
+ * kv_cache_fp8: [num_pages, P, 656] bytes, 16-byte aligned; row of a token:
+ *   bytes   0..511  e4m3 codes of c_KV (group g's latent is codes
+ *                   g*d_g .. (g+1)*d_g - 1)
+ *   bytes 512..639  k_R, 64 bf16
+ *   bytes 640..655  4 fp32 scales; scale j applies to codes 128j..128j+127
+ * The latent the attention sees is c[i] = e4m3(code[i]) * scale[i / 128];
+ * everything else (arguments, outputs, split, errors) is as for
+ * mla_decode_paged, whose o_part, lse_part and workspace this call fills in
+ * the same form (merge them with mla_combine_splits or mla_combine_project).
+ *
+ * The latent products run on f16 tensor-core operands: the dequantised
+ * value is exact in f16 when the scale is 0 or a power of two in
+ * [2^-15, 2^7] (another value in that range is rounded to f16 once); the
+ * query's latent part (q_cat[..., 0:d_g], bf16) is converted to f16, exact
+ * within +-65504; the softmax weights are rounded to f16 (bf16 in
+ * mla_decode_paged).  A scale that is neither 0 nor in that range, on any
+ * row of a page the call reads (rows past a sequence's end included: they
+ * enter the products with weight 0, and an infinite value would turn that
+ * into NaN), or a query value beyond 65504, sets MLA_ERR_RANGE in the status
+ * word.  Codes past a sequence's end must not be NaN (0x7f, 0xff); zero
+ * filled rows are fine.
+ */
+int mla_decode_paged_fp8(const mla_dims* dims, const void* q_cat,
+                         const void* kv_cache_fp8, const int32_t* block_table,
+                         const int32_t* seq_lens, int num_splits, float* o_part,
+                         float* lse_part, void* workspace, size_t ws_bytes,
+                         void* stream);
 
 /*
  * mla_combine_splits — merge the split partials of mla_decode_paged by

@@ -13,7 +13,7 @@ import os
 
 __all__ = [
     "MLAError", "Dims", "load_library", "library_path",
-    "mla_absorb_q", "mla_decode_paged", "mla_combine_splits", "mla_project_uv", "mla_combine_project",
+    "mla_absorb_q", "mla_decode_paged", "mla_decode_paged_fp8", "mla_combine_splits", "mla_project_uv", "mla_combine_project",
     "mla_decode_workspace_size", "mla_decode_num_slots", "mla_decode_kernel_launches",
     "launches_per_step", "mla_get_device_status", "mla_set_timeout_test",
     "mla_status_string", "make_dims", "DecodeBuffers", "decode_step",
@@ -61,6 +61,7 @@ def load_library():
         "mla_decode_kernel_launches": [DP, ctypes.POINTER(I)],
         "mla_decode_workspace_size": [DP, ctypes.POINTER(S)],
         "mla_decode_paged": [DP, P, P, P, P, I, P, P, P, S, P],
+        "mla_decode_paged_fp8": [DP, P, P, P, P, I, P, P, P, S, P],
         "mla_combine_splits": [DP, P, P, P, S, P, P, P],
         "mla_project_uv": [DP, P, P, P, P],
         "mla_combine_project": [DP, P, P, P, S, P, P, P, P, P],
@@ -155,6 +156,16 @@ def mla_decode_paged(dims, q_cat, kv_cache, block_table, seq_lens, num_splits, o
         _stream(stream)), "mla_decode_paged")
 
 
+def mla_decode_paged_fp8(dims, q_cat, kv_cache_fp8, block_table, seq_lens, num_splits, o_part, lse_part,
+                         workspace, stream=None):
+    """kv_cache_fp8: uint8 [num_pages, 64, 656] rows of 512 e4m3 codes, the
+    bf16 RoPE key and four fp32 scales (see include/mla.h)."""
+    _check(load_library().mla_decode_paged_fp8(
+        _dims(dims), _ptr(q_cat), _ptr(kv_cache_fp8), _ptr(block_table), _ptr(seq_lens), int(num_splits),
+        _ptr(o_part), _ptr(lse_part), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)), "mla_decode_paged_fp8")
+
+
 def mla_combine_splits(dims, o_part, lse_part, workspace, o_lat, lse=None, stream=None):
     _check(load_library().mla_combine_splits(
         _dims(dims), _ptr(o_part), _ptr(lse_part), _ptr(workspace),
@@ -205,14 +216,16 @@ class DecodeBuffers:
 
 
 def decode_step(dims, bufs: DecodeBuffers, q_nope, q_rope, W_UK, W_UV, cache, block_table, seq_lens,
-                num_splits=0, stream=None, fused=False):
+                num_splits=0, stream=None, fused=False, fp8=False):
     """The whole hot path of one layer's decode step: absorb, paged decode,
     then combine and project (or, with ``fused``, the fused combine +
-    project, which also writes o_lat and lse).  All tensors on the device;
+    project, which also writes o_lat and lse).  With ``fp8`` the cache is
+    the FP8 layout of mla_decode_paged_fp8.  All tensors on the device;
     results land in ``bufs``."""
     mla_absorb_q(dims, q_nope, q_rope, W_UK, bufs.q_cat, stream)
-    mla_decode_paged(dims, bufs.q_cat, cache, block_table, seq_lens, num_splits, bufs.o_part,
-                     bufs.lse_part, bufs.workspace, stream)
+    decode = mla_decode_paged_fp8 if fp8 else mla_decode_paged
+    decode(dims, bufs.q_cat, cache, block_table, seq_lens, num_splits, bufs.o_part, bufs.lse_part,
+           bufs.workspace, stream)
     if fused:
         mla_combine_project(dims, bufs.o_part, bufs.lse_part, bufs.workspace, W_UV, bufs.out, bufs.o_lat,
                             bufs.lse, stream)

@@ -8,11 +8,22 @@ Only work the method needs is credited: cache rows of visible tokens, the
 absorbed query, the latent output and its log-sum-exp.  Split-KV partials,
 padding rows of a page and the zero blocks of the grouped-latent query are
 implementation overhead and are not counted.
+
+kv="fp8": the cache row is the FP8 one of mla_decode_paged_fp8, 512 E4M3
+codes + 64 bf16 RoPE key + 4 fp32 scales = 656 bytes a token.
 """
 from __future__ import annotations
 
 BF16 = 2
 FP32 = 4
+FP8_ROW_BYTES = 512 + 64 * BF16 + 4 * FP32
+
+
+def row_bytes(kv: str = "bf16", d_c: int = 512, d_R: int = 64) -> int:
+    """Cache bytes of one token in one layer for a cache format."""
+    if kv == "fp8":
+        return d_c + d_R * BF16 + (d_c // 128) * FP32
+    return (d_c + d_R) * BF16
 
 
 def bytes_per_token(d_c: int = 512, d_R: int = 64, elem_bytes: int = BF16) -> int:
@@ -38,18 +49,18 @@ def compression_ratio(d_c: int = 512, d_R: int = 64, heads: int = 128, head_dim:
     return 1.0 - bytes_per_token(d_c, d_R) / mha_bytes_per_token(heads, head_dim)
 
 
-def latent_kv_bytes(seq_lens, d_c: int = 512, d_R: int = 64) -> int:
+def latent_kv_bytes(seq_lens, d_c: int = 512, d_R: int = 64, kv: str = "bf16") -> int:
     """Latent KV cache bytes one decode step of one layer reads: every cached
     row of every sequence once (the new tokens' rows included)."""
-    return sum(int(n) for n in seq_lens) * bytes_per_token(d_c, d_R)
+    return sum(int(n) for n in seq_lens) * row_bytes(kv, d_c, d_R)
 
 
-def decode_bytes(seq_lens, Lq: int, H: int, G: int = 1, d_c: int = 512, d_R: int = 64) -> int:
+def decode_bytes(seq_lens, Lq: int, H: int, G: int = 1, d_c: int = 512, d_R: int = 64, kv: str = "bf16") -> int:
     """Algorithmic HBM bytes of mla_decode_paged + mla_combine_splits: every
     visible cache row once, q_cat in, o_lat (bf16) and lse (fp32) out."""
     d_g = d_c // G
     B = len(seq_lens)
-    cache = sum(int(n) for n in seq_lens) * bytes_per_token(d_c, d_R)
+    cache = sum(int(n) for n in seq_lens) * row_bytes(kv, d_c, d_R)
     q = B * Lq * H * (d_g + d_R) * BF16
     o = B * Lq * H * d_g * BF16 + B * Lq * H * FP32
     return cache + q + o
@@ -78,11 +89,11 @@ def project_bytes(B: int, Lq: int, H: int, d_hc: int = 128, d_g: int = 512) -> i
     return (H * d_hc * d_g + B * Lq * H * d_g + B * Lq * H * d_hc) * BF16
 
 
-def step_bytes(seq_lens, Lq: int, H: int, G: int = 1) -> int:
+def step_bytes(seq_lens, Lq: int, H: int, G: int = 1, kv: str = "bf16") -> int:
     """One whole decode step of one layer: absorb, decode+combine, project."""
     B = len(seq_lens)
     d_g = 512 // G
-    return (absorb_bytes(B, Lq, H, d_g=d_g) + decode_bytes(seq_lens, Lq, H, G)
+    return (absorb_bytes(B, Lq, H, d_g=d_g) + decode_bytes(seq_lens, Lq, H, G, kv=kv)
             + project_bytes(B, Lq, H, d_g=d_g))
 
 

@@ -28,15 +28,16 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// bf16 tensor map (128-byte swizzle unless told otherwise); dims innermost
-// first; strides in bytes for dims 1..rank-1.
+// Tensor map (bf16 and 128-byte swizzle unless told otherwise); dims
+// innermost first; strides in bytes for dims 1..rank-1.
 int make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
              const cuuint64_t* strides, const cuuint32_t* box,
-             CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
+             CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B,
+             CUtensorMapDataType type = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   auto fn = encode_fn();
   if (!fn) return MLA_ERR_CUDA;
   cuuint32_t elem[3] = {1, 1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides,
+  CUresult r = fn(m, type, rank, const_cast<void*>(base), dims, strides,
                   box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_CUDA;
@@ -112,6 +113,7 @@ const char* mla_status_string(int s) {
     case MLA_ERR_BAD_TABLE: return "MLA_ERR_BAD_TABLE";
     case MLA_ERR_BAD_SEQLEN: return "MLA_ERR_BAD_SEQLEN";
     case MLA_ERR_TIMEOUT: return "MLA_ERR_TIMEOUT";
+    case MLA_ERR_RANGE: return "MLA_ERR_RANGE";
     default: return "MLA_ERR_UNKNOWN";
   }
 }
@@ -175,7 +177,8 @@ int mla_decode_num_slots(const mla_dims* d, int* slots) {
   if (rc != MLA_OK) return rc;
   if (!slots) return MLA_ERR_INVALID_ARG;
   int units = 0;
-  if ((rc = decode_max_units(decode_solo(d->G), decode_csize(d->Lq, d->H, d->G), &units)) != MLA_OK) return rc;
+  if ((rc = decode_max_units(decode_solo(d->G), false, decode_csize(d->Lq, d->H, d->G), &units)) != MLA_OK)
+    return rc;
   *slots = d->B + units - 1;
   return MLA_OK;
 }
@@ -188,9 +191,14 @@ int mla_decode_kernel_launches(const mla_dims* d, int* launches) {
   return MLA_OK;
 }
 
-int mla_decode_paged(const mla_dims* d, const void* q_cat, const void* kv_cache,
-                     const int32_t* block_table, const int32_t* seq_lens, int num_splits,
-                     float* o_part, float* lse_part, void* workspace, size_t ws_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+// mla_decode_paged and mla_decode_paged_fp8: the same kernel, with the
+// cache rows in bf16 or FP8.
+int decode_paged(const mla_dims* d, const void* q_cat, const void* kv_cache, bool fp8,
+                 const int32_t* block_table, const int32_t* seq_lens, int num_splits, float* o_part,
+                 float* lse_part, void* workspace, size_t ws_bytes, void* stream) {
   int rc = check_dims(d);
   if (rc != MLA_OK) return rc;
   if (!q_cat || !kv_cache || !block_table || !seq_lens || !o_part || !lse_part || num_splits < 0)
@@ -203,18 +211,42 @@ int mla_decode_paged(const mla_dims* d, const void* q_cat, const void* kv_cache,
   const bool solo = decode_solo(d->G);
   const int csize = decode_csize(d->Lq, d->H, d->G);
   int units = 0;
-  if ((rc = decode_max_units(solo, csize, &units)) != MLA_OK) return rc;
+  if ((rc = decode_max_units(solo, false, csize, &units)) != MLA_OK) return rc;
+  if (fp8) {  // never more units than mla_decode_num_slots counts on
+    int units8 = 0;
+    if ((rc = decode_max_units(solo, true, csize, &units8)) != MLA_OK) return rc;
+    if (units8 < units) units = units8;
+  }
   if (num_splits > 0 && num_splits < units) units = num_splits;
   auto st = static_cast<cudaStream_t>(stream);
-  CUtensorMap tm, tm_rope, tm_qrope, tm_qlat;
-  {
-    cuuint64_t dims[2] = {(cuuint64_t)kRow, (cuuint64_t)d->num_pages * kPage};
+  CUtensorMap tm, tm_rope, tm_qrope, tm_qlat, tm_scale;
+  const cuuint64_t rows = (cuuint64_t)d->num_pages * kPage;
+  if (fp8) {
+    // the same rows seen as bytes (codes), bf16 (RoPE key) and fp32 (scales)
+    const cuuint64_t strides[1] = {(cuuint64_t)kRowBytesFp8};
+    const cuuint64_t dims8[2] = {(cuuint64_t)kRowBytesFp8, rows};
+    const cuuint32_t box8[2] = {64, kPage};
+    if ((rc = make_map(&tm, kv_cache, 2, dims8, strides, box8, CU_TENSOR_MAP_SWIZZLE_NONE,
+                       CU_TENSOR_MAP_DATA_TYPE_UINT8)) != MLA_OK)
+      return rc;
+    const cuuint64_t dims16[2] = {(cuuint64_t)kRowBytesFp8 / 2, rows};
+    const cuuint32_t rbox[2] = {32, kPage};
+    if ((rc = make_map(&tm_rope, kv_cache, 2, dims16, strides, rbox, CU_TENSOR_MAP_SWIZZLE_64B)) != MLA_OK)
+      return rc;
+    const cuuint64_t dims32[2] = {(cuuint64_t)kRowBytesFp8 / 4, rows};
+    const cuuint32_t sbox[2] = {4, kPage};
+    if ((rc = make_map(&tm_scale, kv_cache, 2, dims32, strides, sbox, CU_TENSOR_MAP_SWIZZLE_NONE,
+                       CU_TENSOR_MAP_DATA_TYPE_FLOAT32)) != MLA_OK)
+      return rc;
+  } else {
+    cuuint64_t dims[2] = {(cuuint64_t)kRow, rows};
     cuuint64_t strides[1] = {(cuuint64_t)kRow * 2};
     cuuint32_t box[2] = {64, kPage};
     if ((rc = make_map(&tm, kv_cache, 2, dims, strides, box)) != MLA_OK) return rc;
     cuuint32_t rbox[2] = {32, kPage};
     if ((rc = make_map(&tm_rope, kv_cache, 2, dims, strides, rbox, CU_TENSOR_MAP_SWIZZLE_64B)) != MLA_OK)
       return rc;
+    tm_scale = tm;  // not read
   }
   {
     const int d_q = kDc / d->G + kDr;
@@ -256,7 +288,24 @@ int mla_decode_paged(const mla_dims* d, const void* q_cat, const void* kv_cache,
   a.seq_lens = seq_lens;
   a.wait_ns = decode_wait_limit_ns();
   a.stall_page = decode_stall_page();
-  return cuda_status(launch_decode(solo, tm, tm_rope, tm_qrope, tm_qlat, a, units, csize, st));
+  return cuda_status(launch_decode(solo, fp8, tm, tm_rope, tm_qrope, tm_qlat, tm_scale, a, units, csize, st));
+}
+}  // namespace
+
+extern "C" {
+
+int mla_decode_paged(const mla_dims* d, const void* q_cat, const void* kv_cache,
+                     const int32_t* block_table, const int32_t* seq_lens, int num_splits,
+                     float* o_part, float* lse_part, void* workspace, size_t ws_bytes, void* stream) {
+  return decode_paged(d, q_cat, kv_cache, false, block_table, seq_lens, num_splits, o_part, lse_part, workspace,
+                      ws_bytes, stream);
+}
+
+int mla_decode_paged_fp8(const mla_dims* d, const void* q_cat, const void* kv_cache_fp8,
+                         const int32_t* block_table, const int32_t* seq_lens, int num_splits,
+                         float* o_part, float* lse_part, void* workspace, size_t ws_bytes, void* stream) {
+  return decode_paged(d, q_cat, kv_cache_fp8, true, block_table, seq_lens, num_splits, o_part, lse_part, workspace,
+                      ws_bytes, stream);
 }
 
 int mla_combine_splits(const mla_dims* d, const float* o_part, const float* lse_part,

@@ -53,6 +53,13 @@
 //     sequences yields one partial (o, lse) per sequence, stored in slot
 //     b + unit (o chunk-major, [slot][column/4][row][4] fp32).  mla_combine.cu
 //     merges them, alone or inside the W_UV projection.
+//   * FP8 cache (mla_decode_paged_fp8): rows of 512 E4M3 codes, the bf16
+//     RoPE key and four fp32 power-of-two scales (656 bytes).  The codes and
+//     scales land in a raw slot, the RoPE columns in a ring slot; a
+//     dequantising warp writes code * scale as f16 into the stage, in the
+//     layout the bf16 cache's tiles have, so the latent K steps and P.V run
+//     as f16 MMAs (query and P in f16), the RoPE K steps as bf16 MMAs into
+//     the same fp32 scores.  HBM bytes per token: 656 against 1152.
 //   * Every wait is bounded (wall clock).  A wait that gives up records
 //     MLA_ERR_TIMEOUT in the workspace status word and raises the abort flag
 //     of both CTAs of the pair; every role then leaves its loop, and the
@@ -86,16 +93,33 @@ constexpr int kQRopeBox = kRowsPerCta * 32 * 2;    // 32 RoPE columns of 128 que
 //   solo (2, 4 or 8 groups): a stage holds this CTA's latent half and all
 //        64 RoPE columns; P slots (2) | the RoPE query tile (128 rows x 64
 //        columns, two boxes) | DecodeShared.
-template <bool kSolo>
+// FP8 cache (kFp8): a stage holds only the dequantised latent half (f16);
+// the page's raw codes and scales land in one of two raw slots (freed by the
+// dequantising warp once read) and its RoPE columns in a ring of their own
+// (freed by the QK MMAs), both ahead of the stage:
+//   f16 stages (3) | RoPE ring (3) | raw slots (2) | as above from the send slots on.
+constexpr int kStagesFp8 = 3;
+constexpr int kRawSlots = 2;
+constexpr int kRawBoxBytes = kPage * 64;                 // 64 tokens x 64 codes, unswizzled, 4 KiB
+constexpr int kRawScaleBytes = kPage * 16;               // 64 tokens x 4 fp32 scales, 1 KiB
+constexpr int kRawSlotBytes = 4 * kRawBoxBytes + kRawScaleBytes;
+template <bool kSolo, bool kFp8>
 struct Layout {
+  static constexpr int kNStages = kFp8 ? kStagesFp8 : kStages;
   static constexpr int kRopeBoxes = kSolo ? 2 : 1;
-  static constexpr int kStageBytes = 4 * kBoxBytes + kRopeBoxes * kRopeBoxBytes;
-  static constexpr int kXOff = kStages * kStageBytes;                     // send slots (pair), P slots (solo)
+  static constexpr int kRopeBytes = kRopeBoxes * kRopeBoxBytes;  // a page's RoPE columns of this CTA
+  static constexpr int kStageBytes = 4 * kBoxBytes + (kFp8 ? 0 : kRopeBytes);
+  static constexpr int kRopeRingOff = kNStages * kStageBytes;
+  static constexpr int kRawOff = kRopeRingOff + (kFp8 ? kNStages * kRopeBytes : 0);
+  static constexpr int kXOff = kRawOff + (kFp8 ? kRawSlots * kRawSlotBytes : 0);  // send slots (pair), P slots (solo)
   static constexpr int kRecvOff = kSolo ? kXOff : kXOff + 2 * kXSlot;     // P is written here
   static constexpr int kQRopeOff = kXOff + (kSolo ? 2 : 4) * kXSlot;
   static constexpr int kQRopeBytes = kRopeBoxes * kQRopeBox;
   static constexpr int kSmemShared = kQRopeOff + kQRopeBytes;
-  static_assert(kStageBytes % 1024 == 0 && kXSlot % 1024 == 0 && kQRopeOff % 1024 == 0,
+  // the RoPE columns of the page in stage st
+  static constexpr int rope_off(int st) { return kFp8 ? kRopeRingOff + st * kRopeBytes : st * kStageBytes + 4 * kBoxBytes; }
+  static_assert(kStageBytes % 1024 == 0 && kXSlot % 1024 == 0 && kQRopeOff % 1024 == 0 && kRawOff % 1024 == 0 &&
+                    kRawSlotBytes % 1024 == 0 && kRopeBytes % 512 == 0,
                 "swizzled tiles need aligned bases");
 };
 static_assert(4 * kQBoxBytes == 4 * kXSlot, "the first query's latent half fills the four exchange slots");
@@ -103,18 +127,21 @@ static_assert(4 * kQBoxBytes == 4 * kXSlot, "the first query's latent half fills
 // keys of every page, 128 columns of O, 64 columns of Q); then, in pair
 // mode, warps 8-11: exchange warps (one per quadrant, a whole score row per
 // thread); then the TMA producer and the QK and P.V issuers (warps 12-14 in
-// pair mode, 8-10 in solo mode, which exchanges nothing).  15 warps leave
-// 128 registers a thread (four warps share an SM sub-partition's 64K); the
-// 11 of solo mode leave 168.
+// pair mode, 8-10 in solo mode, which exchanges nothing); with an FP8 cache
+// one more warp dequantises the pages.  15 or 16 warps leave 128 registers
+// a thread (four warps share an SM sub-partition's 64K); the 11 or 12 of
+// solo mode leave 168.
 constexpr int kSWarps = 8, kXWarps = 4;
 constexpr int kSoftmaxThreads = 32 * kSWarps, kXThreads = 32 * kXWarps;
-template <bool kSolo>
+template <bool kSolo, bool kFp8>
 struct Roles {
   static constexpr int kX = kSolo ? 0 : kXWarps;  // exchange warps
   static constexpr int kTma = kSWarps + kX, kMma = kTma + 1, kPv = kMma + 1;
-  static constexpr int kThreads = 32 * (kPv + 1);
+  static constexpr int kDq = kFp8 ? kPv + 1 : -1;  // dequantising warp
+  static constexpr int kThreads = 32 * (kPv + 1 + (kFp8 ? 1 : 0));
 };
-static_assert(kPlanInKernelMaxB <= Roles<false>::kThreads && kPlanInKernelMaxBSolo <= Roles<true>::kThreads,
+static_assert(kPlanInKernelMaxB <= Roles<false, false>::kThreads &&
+                  kPlanInKernelMaxBSolo <= Roles<true, false>::kThreads,
               "the in-kernel plan takes one thread per sequence");
 // named barriers 1..4: the two softmax warps of a quadrant
 constexpr uint32_t kBarPair0 = 1;
@@ -212,6 +239,63 @@ __device__ __forceinline__ void set_status(WsHeader* ws, int code) {
   atomicCAS(&ws->status, 0, code);
 }
 
+// FP8 cache, the dequantising warp: lane j's 16 codes of each of the eight
+// 512-byte sweeps of raw box q (rows 8*it + j/4, codes 16*(j%4) ...).
+__device__ __forceinline__ void load_codes(uint32_t raw, int q, int lane, uint4 (&w)[8]) {
+#pragma unroll
+  for (int it = 0; it < 8; ++it) {
+    const uint32_t a = raw + q * kRawBoxBytes + it * 512 + lane * 16;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(w[it].x), "=r"(w[it].y), "=r"(w[it].z), "=r"(w[it].w) : "r"(a));
+  }
+}
+// ... and the scale of 128-column block `blk` of those eight rows
+__device__ __forceinline__ void load_scales(uint32_t raw, int blk, int lane, float (&sc)[8]) {
+#pragma unroll
+  for (int it = 0; it < 8; ++it) {
+    const uint32_t a = raw + 4 * kRawBoxBytes + (it * 8 + (lane >> 2)) * 16 + 4 * blk;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(sc[it]) : "r"(a));
+  }
+}
+// Box q's codes (loaded by load_codes) times their rows' scales (sc[it],
+// the box's block) as f16 into the stage, in the 128-byte swizzled K-major
+// layout.  Returns true if a scale is neither 0 nor a value in [2^-15, 2^7]
+// (its products may leave the f16 range).
+__device__ __forceinline__ bool dequant_box(const uint4 (&w)[8], const float (&sc)[8], int q, uint32_t dst, int lane) {
+  bool bad = false;
+#pragma unroll
+  for (int it = 0; it < 8; ++it) {
+    const int row = it * 8 + (lane >> 2);
+    const float s = sc[it];
+    bad |= !(s == 0.f || (s >= 0x1p-15f && s <= 0x1p7f));
+    const uint32_t s2 = pack_f16x2(s, s);
+    const uint32_t cw[4] = {w[it].x, w[it].y, w[it].z, w[it].w};
+    uint32_t h[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      h[2 * k] = mul_f16x2(e4m3x2_to_f16x2(cw[k]), s2);
+      h[2 * k + 1] = mul_f16x2(e4m3x2_to_f16x2(cw[k] >> 16), s2);
+    }
+    const uint32_t drow = dst + q * kBoxBytes + row * 128;
+    const int c0 = 2 * (lane & 3);
+    st_shared_v4(drow + ((c0 ^ (row & 7)) << 4), h[0], h[1], h[2], h[3]);
+    st_shared_v4(drow + (((c0 + 1) ^ (row & 7)) << 4), h[4], h[5], h[6], h[7]);
+  }
+  return bad;
+}
+
+// A query chunk (64 bf16) to f16 for the f16 MMAs of an FP8 cache; true if
+// a value lies beyond the f16 range (it becomes infinite).
+__device__ __forceinline__ bool query_to_f16(uint32_t (&w)[32]) {
+  bool over = false;
+#pragma unroll
+  for (int k = 0; k < 32; ++k) {
+    const uint32_t h = bf16x2_to_f16x2(w[k]);
+    over |= ((h & 0x7fffu) == 0x7c00u) || ((h & 0x7fff0000u) == 0x7c000000u);
+    w[k] = h;
+  }
+  return over;
+}
+
 // Shared state of one decode CTA (at the end of dynamic shared memory).
 // Per score buffer / receive slot b (page parity):
 //   s_full   QK(p) wrote the own partial scores into S_b
@@ -231,10 +315,16 @@ __device__ __forceinline__ void set_status(WsHeader* ws, int code) {
 //   q_tma    a later segment's RoPE query tile landed
 //   drain    [QK, P.V]: every MMA the issuing thread started is done
 //            (teardown after an abort)
+// Per page, FP8 cache only (stage st = page % 3, raw slot = page % 2):
+//   raw_full   the page's codes, scales and RoPE columns landed
+//   raw_empty  the dequantising warp read the raw slot
+//   full[st]   the dequantised latent is in stage st (an arrival of that warp)
+//   rope_empty QK of the page is done: its RoPE ring slot is free
 struct DecodeShared {
   float xscale_send[2][kRowsPerCta];  // 2^-k of each row's 16-bit partial: ours (copied to the peer)
   float xscale_recv[2][kRowsPerCta];  // and the peer's
   uint64_t full[kStages], empty[kStages];
+  uint64_t raw_full[kRawSlots], raw_empty[kRawSlots], rope_empty[kStagesFp8];  // FP8 cache only
   uint64_t q_full, q_tma, q_lat, drain[2];
   uint64_t never;                // testing: a barrier nothing completes (see DecodeArgs::stall_page)
   uint64_t s_full[2], s_free[2], p_full[2], o_done[2], can_send[2];
@@ -249,11 +339,12 @@ struct DecodeShared {
 };
 
 // All shared memory is dynamic: stage ring, exchange slots, then the small state.
-template <bool kSolo>
+template <bool kSolo, bool kFp8>
 constexpr int decode_smem() {
-  return Layout<kSolo>::kSmemShared + (int)((sizeof(DecodeShared) + 15) & ~size_t(15));
+  return Layout<kSolo, kFp8>::kSmemShared + (int)((sizeof(DecodeShared) + 15) & ~size_t(15));
 }
-static_assert(decode_smem<false>() <= 232448 && decode_smem<true>() <= 232448,
+static_assert(decode_smem<false, false>() <= 232448 && decode_smem<true, false>() <= 232448 &&
+                  decode_smem<false, true>() <= 232448 && decode_smem<true, true>() <= 232448,
               "decode kernel exceeds 227 KiB of shared memory");
 
 __device__ __forceinline__ int clamp_len(int n, int lo, int hi) { return n < lo ? lo : (n > hi ? hi : n); }
@@ -555,21 +646,23 @@ __device__ void plan_in_warp(const DecodeArgs& a, int unit, bool writer, int n0,
 // in its half (heads r*H/2 .. (r+1)*H/2 - 1) with their whole scores: it
 // loads all 64 RoPE columns and exchanges nothing with the peer.  Its
 // query rows are (l, h) for those heads, l-major.
-template <bool kSolo>
-__global__ void __launch_bounds__(Roles<kSolo>::kThreads, 1)
+template <bool kSolo, bool kFp8>
+__global__ void __launch_bounds__(Roles<kSolo, kFp8>::kThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tm_cache, const __grid_constant__ CUtensorMap tm_rope,
                   const __grid_constant__ CUtensorMap tm_qrope, const __grid_constant__ CUtensorMap tm_qlat,
-                  const DecodeArgs a) {
+                  const __grid_constant__ CUtensorMap tm_scale, const DecodeArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* stages = smem;
-  using L = Layout<kSolo>;
+  using L = Layout<kSolo, kFp8>;
+  using R = Roles<kSolo, kFp8>;
   constexpr int kStageBytes = L::kStageBytes;
+  constexpr int NS = L::kNStages;
   const uint32_t xsend = smem_u32(smem + L::kXOff);     // send slots 0 and 1 (pair)
   const uint32_t xrecv = smem_u32(smem + L::kRecvOff);  // receive slots (pair), P slots (solo)
   const uint32_t qrope = smem_u32(smem + L::kQRopeOff);
   DecodeShared& sh = *reinterpret_cast<DecodeShared*>(smem + L::kSmemShared);
-  constexpr int kXW = Roles<kSolo>::kX;
-  constexpr int kTmaWarp = Roles<kSolo>::kTma, kMmaWarp = Roles<kSolo>::kMma, kPvWarp = Roles<kSolo>::kPv;
+  constexpr int kXW = R::kX;
+  constexpr int kTmaWarp = R::kTma, kMmaWarp = R::kMma, kPvWarp = R::kPv, kDqWarp = R::kDq;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // 128-byte-swizzled tiles need a 1024-byte aligned base; the whole cluster
@@ -611,9 +704,16 @@ __global__ void __launch_bounds__(Roles<kSolo>::kThreads, 1)
   if (threadIdx.x == kTmaWarp * 32) {
     sh.abort = 0;
     for (int q = 0; q < 4; ++q) sh.peer_sent[q] = 0;
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < NS; ++s) {
       mbar_init(bar(sh.full[s]), 1);
       mbar_init(bar(sh.empty[s]), 1);
+    }
+    if constexpr (kFp8) {
+      for (int s = 0; s < kRawSlots; ++s) {
+        mbar_init(bar(sh.raw_full[s]), 1);
+        mbar_init(bar(sh.raw_empty[s]), 1);
+      }
+      for (int s = 0; s < NS; ++s) mbar_init(bar(sh.rope_empty[s]), 1);
     }
     mbar_init(bar(sh.q_full), kSoftmaxThreads);
     mbar_init(bar(sh.q_tma), 1);
@@ -636,6 +736,7 @@ __global__ void __launch_bounds__(Roles<kSolo>::kThreads, 1)
     tma_prefetch_desc(&tm_rope);
     tma_prefetch_desc(&tm_qrope);
     tma_prefetch_desc(&tm_qlat);
+    if constexpr (kFp8) tma_prefetch_desc(&tm_scale);
   }
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(&sh.tmem), kTmemCols);
@@ -682,6 +783,7 @@ __global__ void __launch_bounds__(Roles<kSolo>::kThreads, 1)
   uint32_t issued = 0;  // TMA producer: pages whose copies were issued
   uint32_t nq_tma = 0;  // thread 0: RoPE query tiles loaded by TMA for later segments
   int sent = 0;         // exchange warps: pages copied to the peer
+  bool bad_scale = false;  // FP8: a scale outside the exact f16 range was read
 
   if (warp == kTmaWarp) {
     // ------------------------------------------------------------ TMA producer
@@ -710,9 +812,15 @@ __global__ void __launch_bounds__(Roles<kSolo>::kThreads, 1)
           const int mine = lane < nc ? bt[c0 + lane] : 0;
           for (int j = 0; j < nc; ++j) {
             const uint32_t pc = issued;
-            const int st = pc % kStages;
-            if (pc >= (uint32_t)kStages) {
-              ok = mbar_wait(bar(sh.empty[st]), ((pc / kStages) - 1) & 1, abort, lim);
+            const int st = pc % NS;
+            if constexpr (kFp8) {  // the raw slot read by the dequantising warp, the RoPE slot by QK
+              if (pc >= (uint32_t)kRawSlots)
+                ok = mbar_wait(bar(sh.raw_empty[pc % kRawSlots]), ((pc / kRawSlots) - 1) & 1, abort, lim);
+              if (ok && pc >= (uint32_t)NS) ok = mbar_wait(bar(sh.rope_empty[st]), ((pc / NS) - 1) & 1, abort, lim);
+              ok = __all_sync(0xffffffffu, ok);
+              if (!ok) break;
+            } else if (pc >= (uint32_t)NS) {
+              ok = mbar_wait(bar(sh.empty[st]), ((pc / NS) - 1) & 1, abort, lim);
               ok = __all_sync(0xffffffffu, ok);
               if (!ok) break;
             }
@@ -734,15 +842,30 @@ __global__ void __launch_bounds__(Roles<kSolo>::kThreads, 1)
                   tma_load_2d(xsend + q * kQBoxBytes, &tm_qlat, bar(sh.q_lat), qx + 64 * q, qy);
                 tma_load_2d(qrope, &tm_qrope, bar(sh.q_lat), a.d_g + 32 * (int)r, qy);
               }
-              const uint32_t dst = smem_u32(stages + st * kStageBytes);
-              mbar_arrive_expect_tx(bar(sh.full[st]), bytes);
-              for (int q = 0; q < 4; ++q)  // this CTA's latent half
-                tma_load_2d_hint(dst + q * kBoxBytes, &tm_cache, bar(sh.full[st]), (int)(r * 256 + q * 64),
-                                 page * kPage, policy);
-              // this CTA's 32 RoPE columns (all 64 in solo mode)
-              for (int q = 0; q < L::kRopeBoxes; ++q)
-                tma_load_2d_hint(dst + 4 * kBoxBytes + q * kRopeBoxBytes, &tm_rope, bar(sh.full[st]),
-                                 kDc + 32 * (kSolo ? q : (int)r), page * kPage, policy);
+              if constexpr (kFp8) {
+                // this CTA's 256 codes of each row (four 64-byte boxes), the
+                // rows' four scales, and the RoPE columns into the ring slot
+                const uint32_t raw = smem_u32(smem + L::kRawOff + (pc % kRawSlots) * kRawSlotBytes);
+                const uint32_t rb = bar(sh.raw_full[pc % kRawSlots]);
+                mbar_arrive_expect_tx(rb, kRawSlotBytes + L::kRopeBytes);
+                for (int q = 0; q < 4; ++q)
+                  tma_load_2d_hint(raw + q * kRawBoxBytes, &tm_cache, rb, (int)(r * 256 + q * 64), page * kPage,
+                                   policy);
+                tma_load_2d_hint(raw + 4 * kRawBoxBytes, &tm_scale, rb, kFp8ScaleByte / 4, page * kPage, policy);
+                for (int q = 0; q < L::kRopeBoxes; ++q)
+                  tma_load_2d_hint(smem_u32(smem + L::rope_off(st)) + q * kRopeBoxBytes, &tm_rope, rb,
+                                   kFp8RopeByte / 2 + 32 * (kSolo ? q : (int)r), page * kPage, policy);
+              } else {
+                const uint32_t dst = smem_u32(stages + st * kStageBytes);
+                mbar_arrive_expect_tx(bar(sh.full[st]), bytes);
+                for (int q = 0; q < 4; ++q)  // this CTA's latent half
+                  tma_load_2d_hint(dst + q * kBoxBytes, &tm_cache, bar(sh.full[st]), (int)(r * 256 + q * 64),
+                                   page * kPage, policy);
+                // this CTA's 32 RoPE columns (all 64 in solo mode)
+                for (int q = 0; q < L::kRopeBoxes; ++q)
+                  tma_load_2d_hint(dst + 4 * kBoxBytes + q * kRopeBoxBytes, &tm_rope, bar(sh.full[st]),
+                                   kDc + 32 * (kSolo ? q : (int)r), page * kPage, policy);
+              }
             }
             ++issued;
           }
@@ -760,7 +883,10 @@ __global__ void __launch_bounds__(Roles<kSolo>::kThreads, 1)
     // page and score buffer, P.Vs for the softmax.  Every dependence between
     // the streams goes through an mbarrier.
     if (lane == 0) {
+      // the latent K steps in f16 when the cache is FP8 (dequantised tile,
+      // f16 query); the RoPE K steps always in bf16; one fp32 accumulator
       constexpr uint32_t idesc_qk = idesc_bf16(128, 64, false, false);
+      constexpr uint32_t idesc_qk_lat = kFp8 ? idesc_f16(128, 64, false, false) : idesc_qk;
       const uint64_t qr0 = sdesc_sw64(qrope, 512);
       PageCursor c;
       c.init(sh.rec, a, lens, lens_raw);
@@ -780,18 +906,18 @@ __global__ void __launch_bounds__(Roles<kSolo>::kThreads, 1)
           tc_fence_after();
         }
         const uint32_t b = pc & 1;
-        const int st = pc % kStages;
+        const int st = pc % NS;
         if (pc == (uint32_t)a.stall_page && !(ok = mbar_wait(bar(sh.never), 0, abort, lim))) break;
-        if (!(ok = mbar_wait(bar(sh.full[st]), (pc / kStages) & 1, abort, lim))) break;
+        if (!(ok = mbar_wait(bar(sh.full[st]), (pc / NS) & 1, abort, lim))) break;
         if (pc >= 2 && !(ok = mbar_wait(bar(sh.s_free[b]), ((pc - 2) >> 1) & 1, abort, lim))) break;
         tc_fence_after();
         const uint32_t sbase = smem_u32(stages + st * kStageBytes);
         const uint64_t kd0 = sdesc_sw128(sbase, 16, 1024);
-        const uint64_t kr0 = sdesc_sw64(sbase + 4 * kBoxBytes, 512);
+        const uint64_t kr0 = sdesc_sw64(smem_u32(smem + L::rope_off(st)), 512);
 #pragma unroll
         for (int kk = 0; kk < 16; ++kk) {  // latent: boxes 0..3, 4 K steps each (A = Q in tensor memory)
           const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-          mma_ts(tmem + kColS + 64 * b, tmem + kColQ + kk * 8, kd0 + (uint64_t)(off >> 4), idesc_qk,
+          mma_ts(tmem + kColS + 64 * b, tmem + kColQ + kk * 8, kd0 + (uint64_t)(off >> 4), idesc_qk_lat,
                  kk > 0 ? 1u : 0u);
         }
 #pragma unroll
@@ -799,6 +925,7 @@ __global__ void __launch_bounds__(Roles<kSolo>::kThreads, 1)
           mma_ss(tmem + kColS + 64 * b, qr0 + (uint64_t)(((kk >> 1) * kQRopeBox + (kk & 1) * 32) >> 4),
                  kr0 + (uint64_t)(((kk >> 1) * kRopeBoxBytes + (kk & 1) * 32) >> 4), idesc_qk, 1u);
         mma_commit(bar(sh.s_full[b]));
+        if constexpr (kFp8) mma_commit(bar(sh.rope_empty[st]));
         ++pc;
         c.advance(a);
       }
@@ -814,7 +941,7 @@ __global__ void __launch_bounds__(Roles<kSolo>::kThreads, 1)
     // tensor-core commit straight to the peer costs a cluster-scope
     // release, over a thousand cycles on the critical loop).
     if (lane == 0) {
-      constexpr uint32_t idesc_pv = idesc_bf16(128, 256, false, true);
+      constexpr uint32_t idesc_pv = kFp8 ? idesc_f16(128, 256, false, true) : idesc_bf16(128, 256, false, true);
       const uint32_t peer_can_send0 = mapa(bar(sh.can_send[0]), peer);
       const uint32_t peer_can_send1 = mapa(bar(sh.can_send[1]), peer);
       PageCursor c;
@@ -826,12 +953,12 @@ __global__ void __launch_bounds__(Roles<kSolo>::kThreads, 1)
         if (!(ok = mbar_wait(bar(sh.p_full[b]), (p >> 1) & 1, abort, lim))) break;
         tc_fence_after();
         const uint64_t pd0 = sdesc_sw128(xrecv + b * kXSlot, 16, 1024);
-        const uint64_t vd0 = sdesc_sw128(smem_u32(stages + (p % kStages) * kStageBytes), kBoxBytes, 1024);
+        const uint64_t vd0 = sdesc_sw128(smem_u32(stages + (p % NS) * kStageBytes), kBoxBytes, 1024);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)  // 64 tokens = 4 K steps
           mma_ss(tmem + kColO, pd0 + (uint64_t)(kk * 2), vd0 + (uint64_t)((kk * 2048) >> 4), idesc_pv,
                  (acc || kk > 0) ? 1u : 0u);
-        mma_commit(bar(sh.empty[p % kStages]));
+        mma_commit(bar(sh.empty[p % NS]));
         mma_commit(bar(sh.o_done[b]));
         if constexpr (!kSolo) {
           if (!(ok = mbar_wait(bar(sh.o_done[b]), (p >> 1) & 1, abort, lim))) break;
@@ -841,6 +968,47 @@ __global__ void __launch_bounds__(Roles<kSolo>::kThreads, 1)
       }
       if (!ok) fail();
     }
+    __syncwarp();  // reconverge before the CTA-wide barrier of the teardown
+  } else if (kFp8 && warp == kDqWarp) {
+    // ------------------------------------------------------------ dequantising warp (FP8 cache)
+    // Page p: raw slot p % 2 (this CTA's 256 codes of each of the 64 rows,
+    // four unswizzled 64 x 64-byte boxes, and the rows' four scales) ->
+    // stage p % 3 as f16, c = code value * scale of its 128-column block,
+    // in the 128-byte-swizzled K-major layout the TMA gives the bf16 cache.
+    // The product is exact for power-of-two scales in [2^-15, 2^7].  Lane j
+    // reads 16 codes (a contiguous 512-byte sweep per warp: 8 rows) and
+    // writes their 32 bytes to two 16-byte chunks of the row.
+    PageCursor c;
+    c.init(sh.rec, a, lens, lens_raw);
+    bool ok = true;
+    for (uint32_t pc = 0; ok && c.valid; ++pc) {
+      const int st = pc % NS, rs = pc % kRawSlots;
+      ok = mbar_wait(bar(sh.raw_full[rs]), (pc / kRawSlots) & 1, abort, lim);
+      if (ok && pc >= (uint32_t)NS) ok = mbar_wait(bar(sh.empty[st]), ((pc / NS) - 1) & 1, abort, lim);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      const uint32_t raw = smem_u32(smem + L::kRawOff + rs * kRawSlotBytes);
+      const uint32_t dst = smem_u32(stages + st * kStageBytes);
+      // box by box, all eight loads of a box issued before their first use
+      // (their shared-memory latencies overlap); the scales of this lane's
+      // eight rows, block 2r for boxes 0-1, 2r + 1 for boxes 2-3
+#pragma unroll 1
+      for (int q = 0; q < 4; ++q) {
+        float sc[8];
+        uint4 w[8];
+        load_scales(raw, 2 * (int)r + (q >> 1), lane, sc);
+        load_codes(raw, q, lane, w);
+        bad_scale |= dequant_box(w, sc, q, dst, lane);
+      }
+      fence_proxy_async();  // the stores, seen by the tensor cores' reads
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(bar(sh.full[st]));
+        mbar_arrive(bar(sh.raw_empty[rs]));
+      }
+      c.advance(a);
+    }
+    if (!ok && lane == 0) fail();
     __syncwarp();  // reconverge before the CTA-wide barrier of the teardown
   } else if (warp >= kSWarps && warp < kSWarps + kXW) {
     // ------------------------------------------------------------ exchange warps
@@ -909,7 +1077,7 @@ __global__ void __launch_bounds__(Roles<kSolo>::kThreads, 1)
     // Thread = one query row (TMEM lane) and 32 of each page's 64 keys (key
     // half).  Page q: full scores (own S_b in fp32 + the peer's 16-bit
     // partial in receive slot b) -> mask -> row maximum shared with the
-    // partner warp -> online softmax -> P (bf16) into receive slot b, over
+    // partner warp -> online softmax -> P (bf16; f16 with an FP8 cache) into receive slot b, over
     // the partial this thread read there, in the layout of an MMA operand.
     // After a failure the loops keep running without work, so every named
     // barrier still sees both warps.
@@ -985,6 +1153,9 @@ __global__ void __launch_bounds__(Roles<kSolo>::kThreads, 1)
           const uint4 v = lat ? lat[k] : make_uint4(0, 0, 0, 0);
           w[4 * k + 0] = v.x; w[4 * k + 1] = v.y; w[4 * k + 2] = v.z; w[4 * k + 3] = v.w;
         }
+        if constexpr (kFp8) {
+          if (query_to_f16(w)) set_status(ws, MLA_ERR_RANGE);
+        }
         tmem_st32(lane_base + kColQ + 64 * half + 32 * c, w);
       }
       tmem_wait_st();
@@ -1025,6 +1196,9 @@ __global__ void __launch_bounds__(Roles<kSolo>::kThreads, 1)
         for (int k = 0; k < 8; ++k) {
           ld_shared_v4(src + ((k ^ (row & 7)) << 4), w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
           if (sc < 0) w[4 * k] = w[4 * k + 1] = w[4 * k + 2] = w[4 * k + 3] = 0u;
+        }
+        if constexpr (kFp8) {
+          if (query_to_f16(w)) set_status(ws, MLA_ERR_RANGE);
         }
         tmem_st32(lane_base + kColQ + 64 * half + 32 * c, w);
       }
@@ -1135,7 +1309,7 @@ __global__ void __launch_bounds__(Roles<kSolo>::kThreads, 1)
             const float p0 = ex2(fmaf(s[2 * j], a.scale_log2, -base));
             const float p1 = ex2(fmaf(s[2 * j + 1], a.scale_log2, -base));
             psum += p0 + p1;  // row sum of the unrounded weights
-            pk[j] = pack_bf16x2(p0, p1);
+            pk[j] = kFp8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
           }
           l_part += psum;
           // P row into receive slot b, over the peer partial this thread
@@ -1207,13 +1381,19 @@ __global__ void __launch_bounds__(Roles<kSolo>::kThreads, 1)
   // MMAs from landing in memory that is about to be released.
   // A drain that gives up (nothing in flight should take 100 ms) is
   // recorded as a timeout too, by the thread that gave up.
+  if (kFp8 && warp == kDqWarp && __any_sync(0xffffffffu, bad_scale) && lane == 0) set_status(ws, MLA_ERR_RANGE);
   __syncthreads();
   auto drain = [&](uint32_t b, uint32_t parity) {
     if (!mbar_wait_quiet(b, parity)) set_status(a.ws, MLA_ERR_TIMEOUT);
   };
   if (warp == kTmaWarp && lane == 0) {
-    for (uint32_t k = issued > (uint32_t)kStages ? issued - kStages : 0; k < issued; ++k)
-      drain(bar(sh.full[k % kStages]), (k / kStages) & 1);
+    if constexpr (kFp8) {  // a page's copies all land on its raw slot's barrier
+      for (uint32_t k = issued > (uint32_t)kRawSlots ? issued - kRawSlots : 0; k < issued; ++k)
+        drain(bar(sh.raw_full[k % kRawSlots]), (k / kRawSlots) & 1);
+    } else {
+      for (uint32_t k = issued > (uint32_t)NS ? issued - NS : 0; k < issued; ++k)
+        drain(bar(sh.full[k % NS]), (k / NS) & 1);
+    }
     if (!kSolo && issued > 0) drain(bar(sh.q_lat), 0);  // the first query's copies
   } else if ((warp == kMmaWarp || warp == kPvWarp) && lane == 0) {
     const int d = warp == kMmaWarp ? 0 : 1;
@@ -1382,13 +1562,13 @@ cudaError_t launch_plan(const int32_t* seq_lens, const int32_t* block_table, WsH
 namespace {
 constexpr int kCachedDevices = 64;
 struct DecodeDeviceInfo {
-  bool smem_set[2];
-  int units[2][4];  // [solo][clusters of 2, 4, 6, 8 CTAs]; 0 = not known yet
+  bool smem_set[2][2];  // [solo][fp8]
+  int units[2][2][4];   // [solo][fp8][clusters of 2, 4, 6, 8 CTAs]; 0 = not known yet
 };
 std::mutex g_decode_mu;
 DecodeDeviceInfo g_decode_info[kCachedDevices];
 
-template <bool kSolo>
+template <bool kSolo, bool kFp8>
 cudaError_t decode_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, int units, int csize,
                           cudaStream_t st) {
   int dev = 0;
@@ -1398,21 +1578,21 @@ cudaError_t decode_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, in
   bool set = false;
   if (cached) {
     std::lock_guard<std::mutex> lock(g_decode_mu);
-    set = g_decode_info[dev].smem_set[kSolo];
+    set = g_decode_info[dev].smem_set[kSolo][kFp8];
   }
   if (!set) {  // the attribute is per device
-    e = cudaFuncSetAttribute(decode_kernel<kSolo>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             decode_smem<kSolo>());
+    e = cudaFuncSetAttribute(decode_kernel<kSolo, kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             decode_smem<kSolo, kFp8>());
     if (e != cudaSuccess) return e;
     if (cached) {
       std::lock_guard<std::mutex> lock(g_decode_mu);
-      g_decode_info[dev].smem_set[kSolo] = true;
+      g_decode_info[dev].smem_set[kSolo][kFp8] = true;
     }
   }
   cfg = cudaLaunchConfig_t{};
   cfg.gridDim = dim3(units * csize);
-  cfg.blockDim = dim3(Roles<kSolo>::kThreads);
-  cfg.dynamicSmemBytes = decode_smem<kSolo>();
+  cfg.blockDim = dim3(Roles<kSolo, kFp8>::kThreads);
+  cfg.dynamicSmemBytes = decode_smem<kSolo, kFp8>();
   cfg.stream = st;
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = csize;
@@ -1425,7 +1605,7 @@ cudaError_t decode_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, in
   return cudaSuccess;
 }
 
-template <bool kSolo>
+template <bool kSolo, bool kFp8>
 int decode_max_units_mode(int csize, int* units) {
   const int slot = csize / 2 - 1;
   if (slot < 0 || slot > 3 || (csize & 1)) return MLA_ERR_UNSUPPORTED;
@@ -1434,43 +1614,53 @@ int decode_max_units_mode(int csize, int* units) {
   const bool cached = dev >= 0 && dev < kCachedDevices;
   if (cached) {
     std::lock_guard<std::mutex> lock(g_decode_mu);
-    if (g_decode_info[dev].units[kSolo][slot] > 0) {
-      *units = g_decode_info[dev].units[kSolo][slot];
+    if (g_decode_info[dev].units[kSolo][kFp8][slot] > 0) {
+      *units = g_decode_info[dev].units[kSolo][kFp8][slot];
       return MLA_OK;
     }
   }
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[2];
-  if (decode_config<kSolo>(cfg, attr, 1, csize, nullptr) != cudaSuccess) return MLA_ERR_CUDA;
+  if (decode_config<kSolo, kFp8>(cfg, attr, 1, csize, nullptr) != cudaSuccess) return MLA_ERR_CUDA;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, decode_kernel<kSolo>, &cfg) != cudaSuccess || n < 1) return MLA_ERR_CUDA;
+  if (cudaOccupancyMaxActiveClusters(&n, decode_kernel<kSolo, kFp8>, &cfg) != cudaSuccess || n < 1)
+    return MLA_ERR_CUDA;
   if (n > kMaxUnits) n = kMaxUnits;  // the workspace holds per-unit records for at most this many
   if (cached) {
     std::lock_guard<std::mutex> lock(g_decode_mu);
-    g_decode_info[dev].units[kSolo][slot] = n;
+    g_decode_info[dev].units[kSolo][kFp8][slot] = n;
   }
   *units = n;
   return MLA_OK;
 }
 }  // namespace
 
-int decode_max_units(bool solo, int csize, int* units) {
-  return solo ? decode_max_units_mode<true>(csize, units) : decode_max_units_mode<false>(csize, units);
+int decode_max_units(bool solo, bool fp8, int csize, int* units) {
+  if (fp8) return solo ? decode_max_units_mode<true, true>(csize, units) : decode_max_units_mode<false, true>(csize, units);
+  return solo ? decode_max_units_mode<true, false>(csize, units) : decode_max_units_mode<false, false>(csize, units);
 }
 
-cudaError_t launch_decode(bool solo, const CUtensorMap& tm_cache, const CUtensorMap& tm_rope,
-                          const CUtensorMap& tm_qrope, const CUtensorMap& tm_qlat, const DecodeArgs& a, int units,
-                          int csize, cudaStream_t st) {
+namespace {
+template <bool kSolo, bool kFp8>
+cudaError_t launch_decode_mode(const CUtensorMap& tm_cache, const CUtensorMap& tm_rope, const CUtensorMap& tm_qrope,
+                               const CUtensorMap& tm_qlat, const CUtensorMap& tm_scale, const DecodeArgs& a,
+                               int units, int csize, cudaStream_t st) {
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[2];
-  if (solo) {
-    cudaError_t e = decode_config<true>(cfg, attr, units, csize, st);
-    if (e != cudaSuccess) return e;
-    return cudaLaunchKernelEx(&cfg, decode_kernel<true>, tm_cache, tm_rope, tm_qrope, tm_qlat, a);
-  }
-  cudaError_t e = decode_config<false>(cfg, attr, units, csize, st);
+  cudaError_t e = decode_config<kSolo, kFp8>(cfg, attr, units, csize, st);
   if (e != cudaSuccess) return e;
-  return cudaLaunchKernelEx(&cfg, decode_kernel<false>, tm_cache, tm_rope, tm_qrope, tm_qlat, a);
+  return cudaLaunchKernelEx(&cfg, decode_kernel<kSolo, kFp8>, tm_cache, tm_rope, tm_qrope, tm_qlat, tm_scale, a);
+}
+}  // namespace
+
+cudaError_t launch_decode(bool solo, bool fp8, const CUtensorMap& tm_cache, const CUtensorMap& tm_rope,
+                          const CUtensorMap& tm_qrope, const CUtensorMap& tm_qlat, const CUtensorMap& tm_scale,
+                          const DecodeArgs& a, int units, int csize, cudaStream_t st) {
+  if (fp8)
+    return solo ? launch_decode_mode<true, true>(tm_cache, tm_rope, tm_qrope, tm_qlat, tm_scale, a, units, csize, st)
+                : launch_decode_mode<false, true>(tm_cache, tm_rope, tm_qrope, tm_qlat, tm_scale, a, units, csize, st);
+  return solo ? launch_decode_mode<true, false>(tm_cache, tm_rope, tm_qrope, tm_qlat, tm_scale, a, units, csize, st)
+              : launch_decode_mode<false, false>(tm_cache, tm_rope, tm_qrope, tm_qlat, tm_scale, a, units, csize, st);
 }
 
 }  // namespace mla

@@ -17,6 +17,8 @@ constexpr int kDr = 64;        // RoPE key width
 constexpr int kRow = kDc + kDr;  // 576 elements per cache row
 constexpr int kDhc = 128;      // content head dim
 constexpr int kRowsPerCta = 128;  // query rows (l, h) per CTA = MMA M
+// FP8 cache row (bytes): 512 e4m3 codes | 64 bf16 RoPE key | 4 fp32 scales
+constexpr int kFp8RopeByte = 512, kFp8ScaleByte = 640, kRowBytesFp8 = 656;
 
 // Decode workspace: a 32-byte header, then int arrays
 //   off[B+1]   page offset of each sequence in the flattened page order
@@ -90,7 +92,8 @@ unsigned long long decode_wait_limit_ns();
 int decode_stall_page();
 // the decode kernel plans its own split for batches up to these sizes (one
 // sequence a thread; its blocks have 480 threads in pair mode, for one
-// latent group, and 352 in solo mode, for grouped latents)
+// latent group, and 352 in solo mode, for grouped latents; 32 more with an
+// FP8 cache)
 constexpr int kPlanInKernelMaxB = 448, kPlanInKernelMaxBSolo = 352;
 
 // launchers (return cudaError_t of the launch)
@@ -107,9 +110,13 @@ cudaError_t launch_plan(const int32_t* seq_lens, const int32_t* block_table, WsH
 // solo: the kernel mode for 2, 4 or 8 latent groups (each CTA of a pair
 // serves the heads of its latent half, no exchange; tm_qrope then has boxes
 // of 32 x H/2); otherwise the pair mode for one group.
-cudaError_t launch_decode(bool solo, const CUtensorMap& tm_cache, const CUtensorMap& tm_rope,
-                          const CUtensorMap& tm_qrope, const CUtensorMap& tm_qlat, const DecodeArgs& a, int units,
-                          int csize, cudaStream_t st);
+// fp8: the cache rows are FP8 (kRowBytesFp8 bytes): tm_cache then holds
+// the codes as bytes (64 x 64 boxes, no swizzle), tm_rope the RoPE key as
+// bf16 of the same rows, tm_scale the scales as fp32 (4 x 64 boxes); in
+// bf16 mode tm_scale is not read.
+cudaError_t launch_decode(bool solo, bool fp8, const CUtensorMap& tm_cache, const CUtensorMap& tm_rope,
+                          const CUtensorMap& tm_qrope, const CUtensorMap& tm_qlat, const CUtensorMap& tm_scale,
+                          const DecodeArgs& a, int units, int csize, cudaStream_t st);
 // Launch with programmatic stream serialization: the kernel may start its
 // set-up while the kernel before it on the stream finishes (every kernel of
 // this library waits for its predecessor before touching global memory).
@@ -136,7 +143,7 @@ cudaError_t launch_combine(const float* o_part, const float* lse_part, const WsH
 cudaError_t launch_combine_project(const CUtensorMap& tmA, const float* o_part, const float* lse_part,
                                    const WsHeader* ws, void* out, void* o_lat, float* lse, int B, int Lq, int H,
                                    int G, int slots, cudaStream_t st);
-int decode_max_units(bool solo, int csize, int* units);  // clusters of csize CTAs resident at once
+int decode_max_units(bool solo, bool fp8, int csize, int* units);  // clusters of csize CTAs resident at once
 // The decompress branch (mla_prefill.cu).  tmC: cache rows (64 x 64 boxes,
 // 128-byte swizzle); tmWK, tmWV: W_UK, W_UV as [H, 128, d_g] (64 x 128 x 1
 // boxes); tmQN, tmQR: q_nope, q_rope as [B*Lq rows, H*128 / H*64 columns]

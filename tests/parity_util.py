@@ -32,13 +32,17 @@ def assert_close(got, ref, what, rel=REL_MAX, cos=COS_MIN):
     return err / max(scale, 1e-300)
 
 
+def is_fp8(case):
+    return case.meta.get("kv") == "fp8"
+
+
 def run_gpu(case, num_splits=0, device="cuda", fused=False):
     """Upload a case, run the four entry points (or three, with the fused
-    combine + project), return host copies."""
+    combine + project; the FP8 decode for an FP8 cache), return host copies."""
     t = {k: v.to(device) for k, v in case.tensors().items()}
     bufs = mla.DecodeBuffers(case.dims, device)
     mla.decode_step(case.dims, bufs, t["q_nope"], t["q_rope"], t["W_UK"], t["W_UV"], t["cache"],
-                    t["block_table"], t["seq_lens"], num_splits=num_splits, fused=fused)
+                    t["block_table"], t["seq_lens"], num_splits=num_splits, fused=fused, fp8=is_fp8(case))
     status = mla.mla_get_device_status(bufs.workspace)
     torch.cuda.synchronize()
     return dict(q_cat=bufs.q_cat.cpu(), o_lat=bufs.o_lat.cpu(), lse=bufs.lse.cpu(), out=bufs.out.cpu(),
@@ -60,7 +64,8 @@ def sample_pairs(case, heads_per_seq=None, seqs=None):
 
 def check_case(case, got, pairs, nthreads=0):
     """Compare o_lat, lse, out of the selected (b, h) pairs with the oracle."""
-    ref_out, ref_lat, ref_lse = oracle.decode(case.dims, **case.tensors(), sel=pairs, nthreads=nthreads)
+    ref_decode = oracle.decode_fp8 if is_fp8(case) else oracle.decode
+    ref_out, ref_lat, ref_lse = ref_decode(case.dims, **case.tensors(), sel=pairs, nthreads=nthreads)
     bi = np.array([p[0] for p in pairs])
     hi = np.array([p[1] for p in pairs])
     errs = {}
@@ -76,8 +81,9 @@ def run_decode_only(case, q_cat, num_splits=0, device="cuda"):
     t = {k: v.to(device) for k, v in case.tensors().items()}
     bufs = mla.DecodeBuffers(case.dims, device)
     bufs.q_cat.copy_(q_cat.to(device))
-    mla.mla_decode_paged(case.dims, bufs.q_cat, t["cache"], t["block_table"], t["seq_lens"], num_splits,
-                         bufs.o_part, bufs.lse_part, bufs.workspace)
+    decode = mla.mla_decode_paged_fp8 if is_fp8(case) else mla.mla_decode_paged
+    decode(case.dims, bufs.q_cat, t["cache"], t["block_table"], t["seq_lens"], num_splits, bufs.o_part,
+           bufs.lse_part, bufs.workspace)
     mla.mla_combine_splits(case.dims, bufs.o_part, bufs.lse_part, bufs.workspace, bufs.o_lat, bufs.lse)
     status = mla.mla_get_device_status(bufs.workspace)
     torch.cuda.synchronize()

@@ -78,6 +78,25 @@ def test_decode_rejects_bad_arguments(lib):
     assert decode(lib, d, lp=P(0x10002)) == -3
 
 
+def test_fp8_decode_rejects_bad_arguments(lib):
+    """mla_decode_paged_fp8 validates exactly as mla_decode_paged does."""
+    def decode8(d, q=A16, cache=A16, bt=A16, sl=A16, splits=0, op=A16, lp=A16, ws=A16, wsb=1 << 20):
+        return lib.mla_decode_paged_fp8(ctypes.byref(d), q, cache, bt, sl, splits, op, lp, ws, wsb, None)
+    d = dims()
+    assert lib.mla_decode_paged_fp8(None, A16, A16, A16, A16, 0, A16, A16, A16, 4096, None) == -1
+    assert decode8(d, cache=None) == -1
+    assert decode8(d, splits=-1) == -1
+    assert decode8(d, wsb=8) == -4
+    assert decode8(d, cache=A8) == -3
+    assert decode8(d, q=A8) == -3
+    assert decode8(d, lp=P(0x10002)) == -3
+    for field, value in (("G", 3), ("Lq", 5), ("d_c", 256)):
+        d = dims()
+        setattr(d, field, value)
+        assert decode8(d) == -2
+    assert mla.mla_status_string(-9) == "MLA_ERR_RANGE"
+
+
 def test_decode_rejects_index_overflow(lib):
     """Token and table indices are 32-bit on the device: dims whose cache rows
     or table entries would not fit are refused before any launch."""

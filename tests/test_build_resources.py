@@ -49,7 +49,8 @@ def resource_report(source, tmp_path):
 
 
 @pytest.mark.parametrize("source,limits", [
-    ("mla_decode.cu", {"decode_kernelILb0E": 128, "decode_kernelILb1E": 168}),
+    ("mla_decode.cu", {"decode_kernelILb0E": 128, "decode_kernelILb1E": 168,
+                       "decode_kernelILb0ELb1E": 128, "decode_kernelILb1ELb1E": 168}),
     ("mla_combine.cu", {"combine_kernel": 128}),
     ("mla_gemm.cu", {}),
 ])
