@@ -272,8 +272,10 @@ __device__ __forceinline__ bool dequant_box(const uint4 (&w)[8], const float (&s
     uint32_t h[8];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      h[2 * k] = mul_f16x2(e4m3x2_to_f16x2(cw[k]), s2);
-      h[2 * k + 1] = mul_f16x2(e4m3x2_to_f16x2(cw[k] >> 16), s2);
+      uint32_t lo, hi;
+      e4m3x4_to_f16x2x2(cw[k], lo, hi);
+      h[2 * k] = mul_f16x2(lo, s2);
+      h[2 * k + 1] = mul_f16x2(hi, s2);
     }
     const uint32_t drow = dst + q * kBoxBytes + row * 128;
     const int c0 = 2 * (lane & 3);

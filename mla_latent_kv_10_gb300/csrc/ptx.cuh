@@ -363,11 +363,12 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
   return pack_f16x2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
-// two e4m3 codes (low byte, high byte) -> two f16 (low, high half); exact
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
-  uint32_t r;
-  asm("{ .reg .b16 c; cvt.u16.u32 c, %1; cvt.rn.f16x2.e4m3x2 %0, c; }" : "=r"(r) : "r"(two_codes));
-  return r;
+// four e4m3 codes (bytes 0..3) -> two f16 pairs: lo = (byte 0, byte 1),
+// hi = (byte 2, byte 3), low half first; exact
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t four_codes, uint32_t& lo, uint32_t& hi) {
+  asm("{ .reg .b16 c0, c1; mov.b32 {c0, c1}, %2; cvt.rn.f16x2.e4m3x2 %0, c0; cvt.rn.f16x2.e4m3x2 %1, c1; }"
+      : "=r"(lo), "=r"(hi)
+      : "r"(four_codes));
 }
 __device__ __forceinline__ uint32_t mul_f16x2(uint32_t a, uint32_t b) {
   uint32_t r;
