@@ -372,6 +372,32 @@ def run_prefill(args, world, rank, local):
         ms[k] = e0.elapsed_time(e1) / args.steps
     clocks = sampler.stop()
     status = mla.mla_get_device_status(bufs.workspace, stream)
+
+    # end to end through the public API with host buffers: the new tokens'
+    # queries, the block table and lengths H2D from pinned memory, the
+    # output D2H, every step (plain calls, no graph)
+    h_in = {k: case.tensors()[k].pin_memory() for k in ("q_nope", "q_rope", "block_table", "seq_lens")}
+    h_out = torch.empty(bufs.out.shape, dtype=bufs.out.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in h_in.values())
+    d2h = h_out.numel() * h_out.element_size()
+
+    def e2e_step():
+        for k, v in h_in.items():
+            t[k].copy_(v, non_blocking=True)
+        dec()
+        att()
+        h_out.copy_(bufs.out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / args.steps
     peaks, peak_src = load_peaks()
     dec_flops, att_flops, dec_bytes, att_bytes = prefill_accounting(seq, d["Lq"], d["H"], d["G"], d["max_pages"])
     if rank != 0:
@@ -396,9 +422,14 @@ def run_prefill(args, world, rank, local):
         "roofline": {"bound": "tensor", "achieved": tf(att_flops, ms["att"]), "peak": peaks["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": tf(att_flops, ms["att"]) / peaks["bf16_tflops"], "traffic": None,
                      "kernel": "prefill_attn_kernel", "peak_source": peak_src},
+        "e2e": {"value": tf(dec_flops + att_flops, e2e_ms), "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": 2 * args.steps,
         "clocks": clocks,
         "device_status": mla.mla_status_string(status),
+        "cpu_baseline": {"omitted": "the fp64 oracle recomputes a decompressed key and value per (query, key) "
+                                    "pair: one (sequence, head) pair of this workload is hours of CPU time; the "
+                                    "decode workloads' lines carry the oracle baseline"},
     }
     print(json.dumps(line))
 
@@ -627,6 +658,7 @@ def main():
         "roofline_frac_step": max(step_bytes / (ms * 1e-3) / 1e9 / hbm,
                                   step_flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"]),
         "decode_kernel": {"ms": dec_ms, "gbs": achieved, "tflops": tflops_dec,
+                          "hbm_frac": achieved / hbm,  # on the cache format's bytes
                           "tensor_frac": tflops_dec / peaks["bf16_tflops"],
                           "bytes": dec_bytes, "flops": dec_flops,
                           "ms_single_launch_graph": dec_ms_one,
