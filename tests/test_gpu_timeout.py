@@ -25,11 +25,14 @@ def built():
     mla.mla_set_timeout_test(0, -1)
 
 
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
 @pytest.mark.parametrize("stall_page", [0, 2])
 @pytest.mark.parametrize("Lq,G", [(1, 1), (2, 1), (4, 4)])
-def test_wait_that_gives_up_sets_timeout_and_context_stays_usable(Lq, G, stall_page):
-    """Clusters of 2, 4 and 8 CTAs (one, two and four 128-row blocks)."""
-    c = make_case(B=2, Lq=Lq, H=128, G=G, seq_lens=[700, 300], table="perm", seed=95 + Lq)
+def test_wait_that_gives_up_sets_timeout_and_context_stays_usable(Lq, G, stall_page, kv):
+    """Clusters of 2, 4 and 8 CTAs (one, two and four 128-row blocks), over
+    the bf16 cache and over the FP8 cache (whose teardown also waits for the
+    raw-slot copies)."""
+    c = make_case(B=2, Lq=Lq, H=128, G=G, seq_lens=[700, 300], table="perm", seed=95 + Lq, kv=kv)
     mla.mla_set_timeout_test(50_000, stall_page)   # 50 us
     try:
         got = run_gpu(c, num_splits=2)
