@@ -26,7 +26,9 @@
  *     library never allocates device memory and never synchronises the
  *     stream except in mla_get_device_status.  Its only state is a
  *     per-device cache of launch limits (found on first use, guarded by a
- *     mutex) and the scratch array of mla_decode_attend_noalloc.
+ *     mutex), a cache of the 64 tensor maps encoded last (keyed by every
+ *     encoding argument, the buffer address included; guarded by a mutex),
+ *     and the scratch array of mla_decode_attend_noalloc.
  *   - bf16 tensors are passed as raw 16-bit storage (void*); fp32 as float*;
  *     indices as int32.  All tensors are dense, row-major, no padding.
  *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL
@@ -283,6 +285,25 @@ int mla_combine_project(const mla_dims* dims, const float* o_part,
                         const float* lse_part, const void* workspace,
                         size_t ws_bytes, const void* W_UV, void* out,
                         void* o_lat, float* lse, void* stream);
+
+/*
+ * mla_decode_step — one whole decode step in one call, for callers that
+ * would otherwise pay a host round trip per call:
+ *     mla_absorb_q -> mla_decode_paged (kv_fp8 = 0) or mla_decode_paged_fp8
+ *     (kv_fp8 != 0) with automatic splits -> mla_combine_splits +
+ *     mla_project_uv (fused = 0) or mla_combine_project (fused != 0)
+ * on `stream`, with the arguments, buffers and errors of those calls (the
+ * first error is returned and nothing after it is launched).  o_lat is
+ * required unless fused; lse may be NULL.  The same kernels as the separate
+ * calls, so the results are identical.
+ */
+int mla_decode_step(const mla_dims* dims, const void* q_nope, const void* q_rope,
+                    const void* W_UK, const void* W_UV, const void* kv_cache,
+                    int kv_fp8, const int32_t* block_table,
+                    const int32_t* seq_lens, void* q_cat, float* o_part,
+                    float* lse_part, void* workspace, size_t ws_bytes,
+                    void* o_lat, float* lse, void* out, int fused,
+                    void* stream);
 
 /*
  * ---- The decompress branch, for long query chunks.

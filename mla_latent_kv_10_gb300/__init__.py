@@ -13,7 +13,8 @@ import os
 
 __all__ = [
     "MLAError", "Dims", "load_library", "library_path",
-    "mla_absorb_q", "mla_decode_paged", "mla_decode_paged_fp8", "mla_combine_splits", "mla_project_uv", "mla_combine_project",
+    "mla_absorb_q", "mla_decode_paged", "mla_decode_paged_fp8", "mla_decode_step", "mla_combine_splits",
+    "mla_project_uv", "mla_combine_project",
     "mla_decode_workspace_size", "mla_decode_num_slots", "mla_decode_kernel_launches",
     "launches_per_step", "mla_get_device_status", "mla_set_timeout_test",
     "mla_status_string", "make_dims", "DecodeBuffers", "decode_step",
@@ -62,6 +63,7 @@ def load_library():
         "mla_decode_workspace_size": [DP, ctypes.POINTER(S)],
         "mla_decode_paged": [DP, P, P, P, P, I, P, P, P, S, P],
         "mla_decode_paged_fp8": [DP, P, P, P, P, I, P, P, P, S, P],
+        "mla_decode_step": [DP, P, P, P, P, P, I, P, P, P, P, P, P, S, P, P, P, I, P],
         "mla_combine_splits": [DP, P, P, P, S, P, P, P],
         "mla_project_uv": [DP, P, P, P, P],
         "mla_combine_project": [DP, P, P, P, S, P, P, P, P, P],
@@ -166,6 +168,17 @@ def mla_decode_paged_fp8(dims, q_cat, kv_cache_fp8, block_table, seq_lens, num_s
         _stream(stream)), "mla_decode_paged_fp8")
 
 
+def mla_decode_step(dims, q_nope, q_rope, W_UK, W_UV, kv_cache, kv_fp8, block_table, seq_lens, q_cat, o_part,
+                    lse_part, workspace, o_lat, lse, out, fused=False, stream=None):
+    """The whole decode step in one C call (absorb, decode over the bf16 or
+    FP8 cache, merge and projection)."""
+    _check(load_library().mla_decode_step(
+        _dims(dims), _ptr(q_nope), _ptr(q_rope), _ptr(W_UK), _ptr(W_UV), _ptr(kv_cache), int(bool(kv_fp8)),
+        _ptr(block_table), _ptr(seq_lens), _ptr(q_cat), _ptr(o_part), _ptr(lse_part), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(o_lat), _ptr(lse), _ptr(out), int(bool(fused)),
+        _stream(stream)), "mla_decode_step")
+
+
 def mla_combine_splits(dims, o_part, lse_part, workspace, o_lat, lse=None, stream=None):
     _check(load_library().mla_combine_splits(
         _dims(dims), _ptr(o_part), _ptr(lse_part), _ptr(workspace),
@@ -222,6 +235,10 @@ def decode_step(dims, bufs: DecodeBuffers, q_nope, q_rope, W_UK, W_UV, cache, bl
     project, which also writes o_lat and lse).  With ``fp8`` the cache is
     the FP8 layout of mla_decode_paged_fp8.  All tensors on the device;
     results land in ``bufs``."""
+    if num_splits == 0:  # one C call for the whole step
+        mla_decode_step(dims, q_nope, q_rope, W_UK, W_UV, cache, fp8, block_table, seq_lens, bufs.q_cat, bufs.o_part,
+                        bufs.lse_part, bufs.workspace, bufs.o_lat, bufs.lse, bufs.out, fused, stream)
+        return bufs.out
     mla_absorb_q(dims, q_nope, q_rope, W_UK, bufs.q_cat, stream)
     decode = mla_decode_paged_fp8 if fp8 else mla_decode_paged
     decode(dims, bufs.q_cat, cache, block_table, seq_lens, num_splits, bufs.o_part, bufs.lse_part,

@@ -1,6 +1,7 @@
 // mla_api.cu — the C ABI declared in include/mla.h: argument validation,
 // tensor-map encoding, kernel launches.  No allocation, no global state
-// beyond per-device launch-configuration caches.
+// beyond per-device launch-configuration caches and a cache of encoded
+// tensor maps.
 #include <cmath>
 #include <cstring>
 #include <atomic>
@@ -28,19 +29,63 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+// Encoded tensor maps, remembered by their complete encoding arguments: a
+// decode step encodes about nine, and a serving loop passes the same
+// buffers every step.  64 entries, replaced in turn; guarded by a mutex.
+struct MapKey {
+  const void* base;
+  int rank, swz, type;
+  cuuint64_t dims[3], strides[2];
+  cuuint32_t box[3];
+  bool operator==(const MapKey& o) const { return std::memcmp(this, &o, sizeof(MapKey)) == 0; }
+};
+constexpr int kMapCache = 64;
+struct MapCache {
+  MapKey key[kMapCache];
+  CUtensorMap map[kMapCache];
+  int used = 0, next = 0;
+};
+std::mutex g_map_mu;
+MapCache g_maps;
+
 // Tensor map (bf16 and 128-byte swizzle unless told otherwise); dims
 // innermost first; strides in bytes for dims 1..rank-1.
 int make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
              const cuuint64_t* strides, const cuuint32_t* box,
              CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B,
              CUtensorMapDataType type = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
+  if (rank < 1 || rank > 3) return MLA_ERR_INVALID_ARG;
+  MapKey k;
+  std::memset(&k, 0, sizeof(k));  // padding included: keys compare bytewise
+  k.base = base;
+  k.rank = rank;
+  k.swz = (int)swz;
+  k.type = (int)type;
+  for (int i = 0; i < rank; ++i) {
+    k.dims[i] = dims[i];
+    k.box[i] = box[i];
+    if (i + 1 < rank) k.strides[i] = strides[i];
+  }
+  {
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    for (int i = 0; i < g_maps.used; ++i)
+      if (g_maps.key[i] == k) {
+        *m = g_maps.map[i];
+        return MLA_OK;
+      }
+  }
   auto fn = encode_fn();
   if (!fn) return MLA_ERR_CUDA;
   cuuint32_t elem[3] = {1, 1, 1};
   CUresult r = fn(m, type, rank, const_cast<void*>(base), dims, strides,
                   box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_CUDA;
+  if (r != CUDA_SUCCESS) return MLA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_map_mu);
+  const int slot = g_maps.used < kMapCache ? g_maps.used++ : (g_maps.next++ % kMapCache);
+  g_maps.key[slot] = k;
+  g_maps.map[slot] = *m;
+  return MLA_OK;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -432,6 +477,25 @@ int mla_prefill_attend(const mla_dims* d, const void* q_nope, const void* q_rope
                                            static_cast<WsHeader*>(workspace), d->B, d->Lq, H,
                                            d->max_pages_per_seq, d->num_pages, d->scale, decode_wait_limit_ns(),
                                            static_cast<cudaStream_t>(stream)));
+}
+
+int mla_decode_step(const mla_dims* d, const void* q_nope, const void* q_rope, const void* W_UK, const void* W_UV,
+                    const void* kv_cache, int kv_fp8, const int32_t* block_table, const int32_t* seq_lens,
+                    void* q_cat, float* o_part, float* lse_part, void* workspace, size_t ws_bytes, void* o_lat,
+                    float* lse, void* out, int fused, void* stream) {
+  if (!out) return MLA_ERR_INVALID_ARG;
+  if (!fused && !o_lat) return MLA_ERR_INVALID_ARG;
+  int rc = mla_absorb_q(d, q_nope, q_rope, W_UK, q_cat, stream);
+  if (rc != MLA_OK) return rc;
+  rc = kv_fp8 ? mla_decode_paged_fp8(d, q_cat, kv_cache, block_table, seq_lens, 0, o_part, lse_part, workspace,
+                                     ws_bytes, stream)
+              : mla_decode_paged(d, q_cat, kv_cache, block_table, seq_lens, 0, o_part, lse_part, workspace, ws_bytes,
+                                 stream);
+  if (rc != MLA_OK) return rc;
+  if (fused) return mla_combine_project(d, o_part, lse_part, workspace, ws_bytes, W_UV, out, o_lat, lse, stream);
+  rc = mla_combine_splits(d, o_part, lse_part, workspace, ws_bytes, o_lat, lse, stream);
+  if (rc != MLA_OK) return rc;
+  return mla_project_uv(d, o_lat, W_UV, out, stream);
 }
 
 int mla_get_device_status(const void* workspace, void* stream) {

@@ -97,6 +97,23 @@ def test_fp8_decode_rejects_bad_arguments(lib):
     assert mla.mla_status_string(-9) == "MLA_ERR_RANGE"
 
 
+def test_decode_step_checks_arguments_before_any_launch(lib):
+    """mla_decode_step validates like the calls it chains: the first failing
+    call's code comes back and nothing is launched (no GPU needed here)."""
+    def step(d, q=A16, out=A16, o_lat=A16, fused=0, wsb=1 << 20, kv_fp8=0):
+        return lib.mla_decode_step(ctypes.byref(d), q, A16, A16, A16, A16, kv_fp8, A16, A16, A16, A16, A16, A16,
+                                   wsb, o_lat, None, out, fused, None)
+    d = dims()
+    assert step(d, out=None) == -1
+    assert step(d, o_lat=None) == -1     # the two-call merge needs o_lat
+    assert step(d, q=None) == -1         # absorb
+    assert step(d, q=A8) == -3
+    bad = dims()
+    bad.G = 3
+    assert step(bad) == -2
+    assert step(bad, kv_fp8=1, fused=1, o_lat=None) == -2
+
+
 def test_decode_rejects_index_overflow(lib):
     """Token and table indices are 32-bit on the device: dims whose cache rows
     or table entries would not fit are refused before any launch."""
