@@ -396,3 +396,35 @@ def test_decompress_branch_ignores_anything_past_sequence_end(shape, value):
     hi = np.array([p[1] for p in pairs])
     assert_close(bufs.out.cpu().to(torch.float64).numpy()[bi, :, hi], ref_out[bi, :, hi], "prefill out")
     assert_close(bufs.lse.cpu().to(torch.float64).numpy()[bi, :, hi], ref_lse[bi, :, hi], "prefill lse")
+
+
+@pytest.mark.parametrize("kv,fused", [("bf16", False), ("bf16", True), ("fp8", False)])
+def test_one_call_step_equals_the_separate_calls(kv, fused):
+    """mla_decode_step launches the same kernels as the four calls (three
+    with the fused merge), so its outputs are bit-equal; the second round
+    runs on other buffers of the same dims, so the tensor maps the library
+    remembers must follow the buffers."""
+    c = make_case(B=3, Lq=2, H=128, seq_lens=[2, 300, 900], table="perm", seed=191, kv=kv)
+    fp8 = kv == "fp8"
+    for _ in range(2):
+        t = {k: v.cuda() for k, v in c.tensors().items()}
+        one = mla.DecodeBuffers(c.dims, "cuda")
+        sep = mla.DecodeBuffers(c.dims, "cuda")
+        mla.mla_decode_step(c.dims, t["q_nope"], t["q_rope"], t["W_UK"], t["W_UV"], t["cache"], fp8, t["block_table"],
+                            t["seq_lens"], one.q_cat, one.o_part, one.lse_part, one.workspace, one.o_lat, one.lse,
+                            one.out, fused)
+        mla.mla_absorb_q(c.dims, t["q_nope"], t["q_rope"], t["W_UK"], sep.q_cat)
+        decode = mla.mla_decode_paged_fp8 if fp8 else mla.mla_decode_paged
+        decode(c.dims, sep.q_cat, t["cache"], t["block_table"], t["seq_lens"], 0, sep.o_part, sep.lse_part,
+               sep.workspace)
+        if fused:
+            mla.mla_combine_project(c.dims, sep.o_part, sep.lse_part, sep.workspace, t["W_UV"], sep.out, sep.o_lat,
+                                    sep.lse)
+        else:
+            mla.mla_combine_splits(c.dims, sep.o_part, sep.lse_part, sep.workspace, sep.o_lat, sep.lse)
+            mla.mla_project_uv(c.dims, sep.o_lat, t["W_UV"], sep.out)
+        assert mla.mla_get_device_status(one.workspace) == 0 and mla.mla_get_device_status(sep.workspace) == 0
+        for name in ("q_cat", "o_lat", "lse", "out"):
+            assert torch.equal(getattr(one, name), getattr(sep, name)), name
+    got = dict(o_lat=one.o_lat.cpu(), lse=one.lse.cpu(), out=one.out.cpu())
+    check_case(c, got, sample_pairs(c, 8))
