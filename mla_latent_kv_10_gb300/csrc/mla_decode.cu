@@ -128,17 +128,23 @@ static_assert(4 * kQBoxBytes == 4 * kXSlot, "the first query's latent half fills
 // mode, warps 8-11: exchange warps (one per quadrant, a whole score row per
 // thread); then the TMA producer and the QK and P.V issuers (warps 12-14 in
 // pair mode, 8-10 in solo mode, which exchanges nothing); with an FP8 cache
-// one more warp dequantises the pages.  15 or 16 warps leave 128 registers
-// a thread (four warps share an SM sub-partition's 64K); the 11 or 12 of
-// solo mode leave 168.
+// one more warp dequantises the pages.  A warp's SM sub-partition is its
+// index mod 4, and the TMEM quadrant of the softmax and exchange warps fixes
+// theirs; in pair mode over a bf16 cache the TMA producer runs as warp 15
+// (sub-partition 3, whose softmax warps have the most slack; measured 1 %
+// faster on the long and speculative workloads) and warp 12 idles.  15 or
+// 16 warps leave 128 registers a thread (four warps share an SM
+// sub-partition's 64K); the 11 or 12 of solo mode leave 168.
 constexpr int kSWarps = 8, kXWarps = 4;
 constexpr int kSoftmaxThreads = 32 * kSWarps, kXThreads = 32 * kXWarps;
 template <bool kSolo, bool kFp8>
 struct Roles {
   static constexpr int kX = kSolo ? 0 : kXWarps;  // exchange warps
-  static constexpr int kTma = kSWarps + kX, kMma = kTma + 1, kPv = kMma + 1;
+  static constexpr bool kTmaLast = !kSolo && !kFp8;
+  static constexpr int kTma = kTmaLast ? 15 : kSWarps + kX, kMma = kSWarps + kX + 1, kPv = kMma + 1;
+  static constexpr int kIdle = kTmaLast ? kSWarps + kX : -1;
   static constexpr int kDq = kFp8 ? kPv + 1 : -1;  // dequantising warp
-  static constexpr int kThreads = 32 * (kPv + 1 + (kFp8 ? 1 : 0));
+  static constexpr int kThreads = kTmaLast ? 512 : 32 * (kPv + 1 + (kFp8 ? 1 : 0));
 };
 static_assert(kPlanInKernelMaxB <= Roles<false, false>::kThreads &&
                   kPlanInKernelMaxBSolo <= Roles<true, false>::kThreads,
@@ -971,6 +977,8 @@ __global__ void __launch_bounds__(Roles<kSolo, kFp8>::kThreads, 1)
       if (!ok) fail();
     }
     __syncwarp();  // reconverge before the CTA-wide barrier of the teardown
+  } else if (warp == R::kIdle) {
+    __syncwarp();
   } else if (kFp8 && warp == kDqWarp) {
     // ------------------------------------------------------------ dequantising warp (FP8 cache)
     // Page p: raw slot p % 2 (this CTA's 256 codes of each of the 64 rows,

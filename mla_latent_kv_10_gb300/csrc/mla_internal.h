@@ -91,9 +91,9 @@ struct DecodeArgs {
 unsigned long long decode_wait_limit_ns();
 int decode_stall_page();
 // the decode kernel plans its own split for batches up to these sizes (one
-// sequence a thread; its blocks have 480 threads in pair mode, for one
-// latent group, and 352 in solo mode, for grouped latents; 32 more with an
-// FP8 cache)
+// sequence a thread; its blocks have 512 threads in pair mode, for one
+// latent group, and 352 in solo mode, for grouped latents, 384 with an FP8
+// cache)
 constexpr int kPlanInKernelMaxB = 448, kPlanInKernelMaxBSolo = 352;
 
 // launchers (return cudaError_t of the launch)
