@@ -41,10 +41,18 @@ struct MapKey {
 };
 constexpr int kMapCache = 64;
 struct MapCache {
+  uint64_t hash[kMapCache];  // scanned first; the key is compared only on a hash match
   MapKey key[kMapCache];
   CUtensorMap map[kMapCache];
   int used = 0, next = 0;
 };
+// FNV-1a over the key's bytes
+uint64_t map_hash(const MapKey& k) {
+  const unsigned char* p = reinterpret_cast<const unsigned char*>(&k);
+  uint64_t h = 1469598103934665603ull;
+  for (size_t i = 0; i < sizeof(MapKey); ++i) h = (h ^ p[i]) * 1099511628211ull;
+  return h;
+}
 std::mutex g_map_mu;
 MapCache g_maps;
 
@@ -66,10 +74,11 @@ int make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
     k.box[i] = box[i];
     if (i + 1 < rank) k.strides[i] = strides[i];
   }
+  const uint64_t hk = map_hash(k);
   {
     std::lock_guard<std::mutex> lock(g_map_mu);
     for (int i = 0; i < g_maps.used; ++i)
-      if (g_maps.key[i] == k) {
+      if (g_maps.hash[i] == hk && g_maps.key[i] == k) {
         *m = g_maps.map[i];
         return MLA_OK;
       }
@@ -83,6 +92,7 @@ int make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
   if (r != CUDA_SUCCESS) return MLA_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_map_mu);
   const int slot = g_maps.used < kMapCache ? g_maps.used++ : (g_maps.next++ % kMapCache);
+  g_maps.hash[slot] = hk;
   g_maps.key[slot] = k;
   g_maps.map[slot] = *m;
   return MLA_OK;
