@@ -299,7 +299,8 @@ def e2e_pipelined(args, mla, torch, dev, stream, case, t, caches, copies, fp8):
         stream.wait_event(ev["out"][j])  # the result two steps back has been read from this buffer
         x = ins[j]  # one mla_decode_step call (the separate calls when a split count is forced)
         mla.decode_step(d, bb[j], x["q_nope"], x["q_rope"], t["W_UK"], t["W_UV"], caches[i % copies],
-                        x["block_table"], x["seq_lens"], num_splits=args.splits, fused=args.fused, fp8=fp8)
+                        x["block_table"], x["seq_lens"], num_splits=args.splits, stream=stream,
+                        fused=args.fused, fp8=fp8)
         ev["done"][j].record(stream)
         with torch.cuda.stream(cs):
             if i + 1 < n:

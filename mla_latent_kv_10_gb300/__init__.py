@@ -101,9 +101,7 @@ def _dims(d):
 
 
 def _ptr(t):
-    if t is None:
-        return None
-    return ctypes.c_void_p(t.data_ptr())
+    return None if t is None else t.data_ptr()  # an int: ctypes makes it a void*
 
 
 def _stream(stream):
@@ -111,8 +109,8 @@ def _stream(stream):
         import torch
         stream = torch.cuda.current_stream()
     if hasattr(stream, "cuda_stream"):
-        return ctypes.c_void_p(stream.cuda_stream)
-    return ctypes.c_void_p(int(stream))
+        return stream.cuda_stream
+    return int(stream)
 
 
 def _check(rc, where):
@@ -226,6 +224,7 @@ class DecodeBuffers:
         self.o_lat = torch.empty(B, Lq, H, d_g, dtype=torch.bfloat16, device=device)
         self.lse = torch.empty(B, Lq, H, dtype=torch.float32, device=device)
         self.out = torch.empty(B, Lq, H, dims["d_hc"], dtype=torch.bfloat16, device=device)
+        self.dims_c = make_dims(self.dims)  # the C struct of these dims, built once
 
 
 def decode_step(dims, bufs: DecodeBuffers, q_nope, q_rope, W_UK, W_UV, cache, block_table, seq_lens,
@@ -236,7 +235,8 @@ def decode_step(dims, bufs: DecodeBuffers, q_nope, q_rope, W_UK, W_UV, cache, bl
     the FP8 layout of mla_decode_paged_fp8.  All tensors on the device;
     results land in ``bufs``."""
     if num_splits == 0:  # one C call for the whole step
-        mla_decode_step(dims, q_nope, q_rope, W_UK, W_UV, cache, fp8, block_table, seq_lens, bufs.q_cat, bufs.o_part,
+        dc = bufs.dims_c if (dims is bufs.dims or dims == bufs.dims) else dims
+        mla_decode_step(dc, q_nope, q_rope, W_UK, W_UV, cache, fp8, block_table, seq_lens, bufs.q_cat, bufs.o_part,
                         bufs.lse_part, bufs.workspace, bufs.o_lat, bufs.lse, bufs.out, fused, stream)
         return bufs.out
     mla_absorb_q(dims, q_nope, q_rope, W_UK, bufs.q_cat, stream)
