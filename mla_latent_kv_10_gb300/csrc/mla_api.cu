@@ -145,6 +145,7 @@ int row_blocks(const mla_dims* d) { return (d->Lq * d->H + kRowsPerCta - 1) / kR
 namespace mla {
 unsigned long long decode_wait_limit_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
 int decode_stall_page() { return g_stall_page.load(std::memory_order_relaxed); }
+int gemm_rows_box(int M);  // mla_gemm.cu: query rows per absorb/project CTA tile (the MMA's N)
 }  // namespace mla
 
 extern "C" {
@@ -185,7 +186,7 @@ int mla_absorb_q(const mla_dims* d, const void* q_nope, const void* q_rope, cons
   {
     cuuint64_t dims[3] = {(cuuint64_t)kDhc, (cuuint64_t)H, (cuuint64_t)M};
     cuuint64_t strides[2] = {(cuuint64_t)kDhc * 2, (cuuint64_t)H * kDhc * 2};
-    cuuint32_t box[3] = {64, 1, kRowsPerCta};
+    cuuint32_t box[3] = {64, 1, (cuuint32_t)gemm_rows_box(M)};
     if ((rc = make_map(&tA, q_nope, 3, dims, strides, box)) != MLA_OK) return rc;
   }
   {
@@ -207,13 +208,13 @@ int mla_project_uv(const mla_dims* d, const void* o_lat, const void* W_UV, void*
   {
     cuuint64_t dims[3] = {(cuuint64_t)dg, (cuuint64_t)H, (cuuint64_t)M};
     cuuint64_t strides[2] = {(cuuint64_t)dg * 2, (cuuint64_t)H * dg * 2};
-    cuuint32_t box[3] = {64, 1, kRowsPerCta};
+    cuuint32_t box[3] = {64, 1, (cuuint32_t)gemm_rows_box(M)};
     if ((rc = make_map(&tA, o_lat, 3, dims, strides, box)) != MLA_OK) return rc;
   }
   {
     cuuint64_t dims[3] = {(cuuint64_t)dg, (cuuint64_t)kDhc, (cuuint64_t)H};
     cuuint64_t strides[2] = {(cuuint64_t)dg * 2, (cuuint64_t)kDhc * dg * 2};
-    cuuint32_t box[3] = {64, 64, 1};  // 64 output rows of W_UV per CTA
+    cuuint32_t box[3] = {64, kDhc, 1};  // all 128 output rows of W_UV[h] per CTA
     if ((rc = make_map(&tB, W_UV, 3, dims, strides, box)) != MLA_OK) return rc;
   }
   return cuda_status(launch_project(tA, tB, out, M, H, dg, static_cast<cudaStream_t>(stream)));
