@@ -101,7 +101,8 @@ __device__ __forceinline__ void merge_row(int s0, int nseg, const float* __restr
 // one CTA fits an SM at a time, so a grid of about one CTA per SM finishes
 // in one wave.  The first partials' loads are issued before the row
 // weights are known, so the CTA waits for two dependent global round trips
-// (split records, then log-sum-exps and partials together), not three.
+// (the plan's batch with the sequence's split record, then log-sum-exps and
+// partials together), not three.
 // The log-sum-exp of each row's partials is reduced with warp shuffles over
 // the partial index and turned into per-partial weights in shared memory;
 // the weighted sum reads the chunk-major partials coalesced (32 consecutive
@@ -124,10 +125,14 @@ __global__ void __launch_bounds__(kCombineThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   griddep_wait();
   griddep_launch_dependents();
-  if (ws->B != B) return;
+  // the plan's batch and this sequence's split record are requested
+  // together (their places follow from the argument B, and the workspace
+  // holds at least that much); a plan written for another batch is not
+  // followed
   const WsView v = ws_view(ws, B);
-  const int s0r = v.slot0[b];
-  const int nseg = (s0r < 0 || s0r >= slots) ? 0 : min(v.nslot[b], slots - s0r);
+  const int plan_b = ws->B, s0r = v.slot0[b], nsl = v.nslot[b];
+  if (plan_b != B) return;
+  const int nseg = (s0r < 0 || s0r >= slots) ? 0 : min(nsl, slots - s0r);
   const size_t seg0 = (size_t)(s0r < 0 ? 0 : s0r);
   const bool table = nseg <= kCombineMaxSeg;
 
@@ -151,10 +156,11 @@ __global__ void __launch_bounds__(kCombineThreads, 1)
         pv[jj][k] = (valid && j0 + jj < nseg) ? __ldcs(sj + k * chunk_stride) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
   };
-  issue(0);
 
   // log-sum-exp per row (warp w: rows w, w + 16), then weights.  Lane j
-  // keeps partial j's value (and j+32's) of the rows in registers.
+  // keeps partial j's value (and j+32's) of the rows in registers.  These
+  // loads go out ahead of the first partials', so the weights are worked
+  // out while the partials arrive.
   constexpr int kRowsPerWarp = kCombineRows / kWarps;
   float x0[kRowsPerWarp], x1[kRowsPerWarp];
 #pragma unroll
@@ -163,6 +169,7 @@ __global__ void __launch_bounds__(kCombineThreads, 1)
     x0[k] = (lr < rows && lane < nseg) ? lse_part[(seg0 + lane) * rows + lr] : -INFINITY;
     x1[k] = (lr < rows && lane + 32 < nseg) ? lse_part[(seg0 + lane + 32) * rows + lr] : -INFINITY;
   }
+  issue(0);
 #pragma unroll
   for (int k = 0; k < kRowsPerWarp; ++k) {
     const int rr = warp + kWarps * k, lr = r0 + rr;
