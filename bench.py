@@ -14,7 +14,10 @@ replays of a graph holding only it.
 Default workload: DeepSeek-V3 dims, B=16, Lq=1, H=128, all seq_lens 4096,
 64-token pages, contiguous block tables.  Its 75.5 MB cache fits in the
 129 MB L2, so the timed loop rotates through 4 copies of the cache (302 MB),
-which keeps every step's cache reads coming from HBM.
+which keeps every step's cache reads coming from HBM; it also rotates
+through copies of W_UK and W_UV (2.2x the L2 in all: 9 copies, 302 MB, on
+this workload), so that, as in a model with many layers, no step finds its
+weights in L2.
 
 Prints ONE JSON line (rank 0).  `value` is latent-KV GB/s of the whole step:
 the latent cache bytes one step reads (every cached row once, 1152 B per
@@ -255,7 +258,7 @@ def run_reference(args, world, rank):
     print(json.dumps(line))
 
 
-def e2e_pipelined(args, mla, torch, dev, stream, case, t, caches, copies, fp8):
+def e2e_pipelined(args, mla, torch, dev, stream, case, t, caches, weights, fp8):
     """Mean ms per step of the end-to-end loop (see main), and the H2D / D2H
     bytes each step copies.  The step's inputs (q_nope, q_rope, block table,
     lengths) sit in one pinned host buffer and go up in one copy into one
@@ -298,7 +301,8 @@ def e2e_pipelined(args, mla, torch, dev, stream, case, t, caches, copies, fp8):
         stream.wait_event(ev["in"][j])
         stream.wait_event(ev["out"][j])  # the result two steps back has been read from this buffer
         x = ins[j]  # one mla_decode_step call (the separate calls when a split count is forced)
-        mla.decode_step(d, bb[j], x["q_nope"], x["q_rope"], t["W_UK"], t["W_UV"], caches[i % copies],
+        w_uk, w_uv = weights[i % len(weights)]
+        mla.decode_step(d, bb[j], x["q_nope"], x["q_rope"], w_uk, w_uv, caches[i % len(caches)],
                         x["block_table"], x["seq_lens"], num_splits=args.splits, stream=stream,
                         fused=args.fused, fp8=fp8)
         ev["done"][j].record(stream)
@@ -609,6 +613,12 @@ def main():
     cache_bytes = t["cache"].numel() * t["cache"].element_size()
     copies = max(1, math.ceil(2.2 * L2_BYTES / cache_bytes))
     caches = [t["cache"]] + [t["cache"].clone() for _ in range(copies - 1)]
+    # the weights rotate too, so that no step finds its W_UK and W_UV in L2
+    # (a model with many layers reads each layer's weights from HBM)
+    w_bytes = sum(t[k].numel() * t[k].element_size() for k in ("W_UK", "W_UV"))
+    wcopies = max(1, math.ceil(2.2 * L2_BYTES / w_bytes))
+    weights = [(t["W_UK"], t["W_UV"])] + [(t["W_UK"].clone(), t["W_UV"].clone()) for _ in range(wcopies - 1)]
+    nrot = max(copies, wcopies)  # step graphs: step c uses cache copy c % copies, weights c % wcopies
     bufs = mla.DecodeBuffers(d, dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -618,8 +628,8 @@ def main():
     dec_bytes = acc.decode_bytes(seq, Lq, H, G, kv=args.kv)
     dec_flops = acc.decode_flops(seq, Lq, H, G, causal=bool(d["causal"]))
 
-    def pre():
-        mla.mla_absorb_q(d, t["q_nope"], t["q_rope"], t["W_UK"], bufs.q_cat)
+    def pre(c):
+        mla.mla_absorb_q(d, t["q_nope"], t["q_rope"], weights[c % wcopies][0], bufs.q_cat)
 
     decode = mla.mla_decode_paged_fp8 if fp8 else mla.mla_decode_paged
 
@@ -627,18 +637,19 @@ def main():
         decode(d, bufs.q_cat, caches[c], t["block_table"], t["seq_lens"], args.splits, bufs.o_part,
                bufs.lse_part, bufs.workspace)
 
-    def post():
+    def post(c):
+        w_uv = weights[c % wcopies][1]
         if not args.fused:
             mla.mla_combine_splits(d, bufs.o_part, bufs.lse_part, bufs.workspace, bufs.o_lat, bufs.lse)
-            mla.mla_project_uv(d, bufs.o_lat, t["W_UV"], bufs.out)
+            mla.mla_project_uv(d, bufs.o_lat, w_uv, bufs.out)
         else:
-            mla.mla_combine_project(d, bufs.o_part, bufs.lse_part, bufs.workspace, t["W_UV"], bufs.out,
+            mla.mla_combine_project(d, bufs.o_part, bufs.lse_part, bufs.workspace, w_uv, bufs.out,
                                     bufs.o_lat, bufs.lse)
 
     def step(i):
-        pre()
+        pre(i)
         dec(i % copies)
-        post()
+        post(i)
 
     # warm-up through the plain API (sets kernel attributes, checks status)
     for i in range(args.warmup):
@@ -661,14 +672,15 @@ def main():
     side = torch.cuda.Stream(dev)
     side.wait_stream(stream)
     with torch.cuda.stream(side):
-        g_step = [torch.cuda.CUDAGraph() for _ in range(copies)]
+        g_step = [torch.cuda.CUDAGraph() for _ in range(nrot)]
         g_one = [torch.cuda.CUDAGraph() for _ in range(copies)]
         g_chain = torch.cuda.CUDAGraph()
-        for c in range(copies):
+        for c in range(nrot):
             with torch.cuda.graph(g_step[c], stream=side):
-                pre()
-                dec(c)
-                post()
+                pre(c)
+                dec(c % copies)
+                post(c)
+        for c in range(copies):
             with torch.cuda.graph(g_one[c], stream=side):
                 dec(c)
         with torch.cuda.graph(g_chain, stream=side):
@@ -677,8 +689,8 @@ def main():
     stream.wait_stream(side)
     torch.cuda.synchronize(dev)
 
-    for i in range(max(3, args.warmup)):
-        g_step[i % copies].replay()
+    for i in range(max(nrot, args.warmup)):
+        g_step[i % nrot].replay()
         g_one[i % copies].replay()
         g_chain.replay()
     torch.cuda.synchronize(dev)
@@ -698,7 +710,7 @@ def main():
     time.sleep(0.3)
     t_start.record(stream)
     for i in range(args.steps):
-        g_step[i % copies].replay()
+        g_step[i % nrot].replay()
     t_end.record(stream)
     for i in range(args.steps):
         ev_chain[i][0].record(stream)
@@ -715,7 +727,7 @@ def main():
     n_sus = max(args.steps, int(1000.0 / max(step_ms_est, 1e-3)))
     s_start.record(stream)
     for i in range(n_sus):
-        g_step[i % copies].replay()
+        g_step[i % nrot].replay()
     s_end.record(stream)
     torch.cuda.synchronize(dev)
     clocks = sampler.stop()
@@ -735,7 +747,7 @@ def main():
     # step i+1 go up on a copy stream while step i computes, and the result
     # of step i comes down there once it is done: two sets of device inputs
     # and outputs, events between the streams.
-    e2e_ms, h2d, d2h, e2e_steps = e2e_pipelined(args, mla, torch, dev, stream, case, t, caches, copies, fp8)
+    e2e_ms, h2d, d2h, e2e_steps = e2e_pipelined(args, mla, torch, dev, stream, case, t, caches, weights, fp8)
     e2e_ms = max_over_ranks(e2e_ms, pg, dev)
 
     peaks, peak_src = load_peaks()
@@ -758,7 +770,9 @@ def main():
                    "Lq": Lq, "H": H, "G": G, "kv": args.kv,
                    "seq_len_mean": sum(seq) / len(seq), "page_size": 64,
                    "parallelism": "replicas" if world > 1 else "single",
-                   "l2": "inputs larger than L2: %d rotating cache copies (%.0f MB)" % (copies, copies * cache_bytes / 1e6)},
+                   "l2": "inputs larger than L2: %d rotating cache copies (%.0f MB), %d rotating copies of "
+                         "W_UK and W_UV (%.0f MB)" % (copies, copies * cache_bytes / 1e6, wcopies,
+                                                     wcopies * w_bytes / 1e6)},
         "value_counts": "latent KV cache bytes read per step (%d B, %d B a token) over the step time"
                         % (kv_bytes, acc.row_bytes(args.kv)),
         "step_gbs": job_rate(world, step_bytes, ms) / 1e9,
