@@ -44,8 +44,11 @@ def test_absorb_q_matches_oracle(B, Lq, H, G):
 # ---------------------------------------------------------------- step: project
 
 @pytest.mark.parametrize("B,Lq,H,G", [(2, 1, 16, 1), (16, 1, 128, 1), (64, 2, 128, 1), (5, 1, 128, 2),
-                                      (4, 4, 128, 4), (3, 2, 64, 8)])
+                                      (4, 4, 128, 4), (3, 2, 64, 8), (130, 1, 16, 1), (67, 2, 16, 2)])
 def test_project_uv_matches_oracle(B, Lq, H, G):
+    """Query rows: a few (one 16-row MMA), 128 (the W_UV ring refilled
+    through fewer slots than chunks) and more than 128 (a second, ragged
+    row block)."""
     c = make_case(B=B, Lq=Lq, H=H, G=G, seq_lens=[1] * B, seed=200 + B)
     d_g = 512 // G
     gen = torch.Generator().manual_seed(7)
