@@ -14,6 +14,7 @@
 // of the workspace.  A plan written for another
 // batch is not followed, and every slot range is clipped to the `slots`
 // partials the caller allocated.
+#include <atomic>
 #include <cmath>
 
 #include "mla_internal.h"
@@ -108,15 +109,19 @@ __device__ __forceinline__ void merge_row(int s0, int nseg, const float* __restr
 // the weighted sum reads the chunk-major partials coalesced (32 consecutive
 // rows per warp access).  The bf16 result is staged in shared memory and
 // written out as contiguous row pieces.
+// A grid of more CTAs than SMs (many sequences, or several query rows a
+// sequence) runs the 256-thread form instead: each thread sums twice the
+// chunks with half the partials in flight, and two CTAs share an SM, so
+// one CTA's round trips overlap the other's.
 constexpr int kCombineRows = 32, kCombineCols = 256, kCombineMaxSeg = 64, kCombineThreads = 512;
-template <int DG>
-__global__ void __launch_bounds__(kCombineThreads, 1)
+template <int DG, int kThreads, int kBatch>
+__global__ void __launch_bounds__(kThreads, kCombineThreads / kThreads)
     combine_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part,
                    const WsHeader* __restrict__ ws, __nv_bfloat16* __restrict__ o_lat,
                    float* __restrict__ lse_out, int B, int Lq, int H, int G, int slots) {
   constexpr int kCols = DG < kCombineCols ? DG : kCombineCols;  // columns of this CTA
-  constexpr int kWarps = kCombineThreads / 32;
-  static_assert(DG % kCols == 0 && (kCols / 4) % (kCombineThreads / 32) == 0, "latent slice in whole CTA column ranges");
+  constexpr int kWarps = kThreads / 32;
+  static_assert(DG % kCols == 0 && (kCols / 4) % kWarps == 0, "latent slice in whole CTA column ranges");
   __shared__ __align__(16) __nv_bfloat16 tile[kCombineRows][kCols + 8];
   __shared__ float wts[kCombineMaxSeg][kCombineRows];
   __shared__ float lrow[kCombineRows];
@@ -142,7 +147,7 @@ __global__ void __launch_bounds__(kCombineThreads, 1)
   const bool valid = row < rows;
   const int h = valid ? row % H : 0, g = (h * G) / H;
   constexpr int kChunks = kCols / 4, kPer = kChunks / kWarps;  // chunks of this thread: warp + kWarps*k
-  constexpr int kBatch = 4;  // partials whose loads are all issued before any is used
+  // kBatch: partials whose loads are all issued before any is used
   const float4* src = reinterpret_cast<const float4*>(o_part) +
                       (size_t)(g * (DG / 4) + cz * kChunks + warp) * rows + row;
   const size_t slot_stride = (size_t)(kDc / 4) * rows, chunk_stride = (size_t)kWarps * rows;
@@ -228,7 +233,7 @@ __global__ void __launch_bounds__(kCombineThreads, 1)
   }
   __syncthreads();
   constexpr int kPieces = kCols * 2 / 16;  // 16-byte pieces per row
-  for (int i = threadIdx.x; i < kCombineRows * kPieces; i += kCombineThreads) {
+  for (int i = threadIdx.x; i < kCombineRows * kPieces; i += kThreads) {
     const int rr = i / kPieces, pc = i % kPieces;
     if (r0 + rr < rows)
       reinterpret_cast<uint4*>(o_lat + ((size_t)b * rows + r0 + rr) * DG + cz * kCols)[pc] =
@@ -389,12 +394,30 @@ __global__ void __launch_bounds__(kCpThreads, 1)
   }
 }
 
+// SMs of the current device (read once; every device this runs on is alike)
+int device_sms() {
+  static std::atomic<int> sms{0};
+  int n = sms.load(std::memory_order_relaxed);
+  if (n == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      n = 1;
+    sms.store(n, std::memory_order_relaxed);
+  }
+  return n;
+}
+
 template <int DG>
 cudaError_t launch_combine_dg(const float* o_part, const float* lse_part, const WsHeader* ws, __nv_bfloat16* ol,
                               float* lse, int B, int Lq, int H, int G, int slots, cudaStream_t st) {
   constexpr int kCols = DG < kCombineCols ? DG : kCombineCols;
-  dim3 grid(B, (Lq * H + kCombineRows - 1) / kCombineRows, DG / kCols), block(kCombineThreads);
-  combine_kernel<DG><<<grid, block, 0, st>>>(o_part, lse_part, ws, ol, lse, B, Lq, H, G, slots);
+  dim3 grid(B, (Lq * H + kCombineRows - 1) / kCombineRows, DG / kCols);
+  if ((long long)grid.x * grid.y * grid.z > device_sms())  // more than one wave: two CTAs an SM
+    combine_kernel<DG, kCombineThreads / 2, 2><<<grid, kCombineThreads / 2, 0, st>>>(o_part, lse_part, ws, ol, lse,
+                                                                                    B, Lq, H, G, slots);
+  else
+    combine_kernel<DG, kCombineThreads, 4><<<grid, kCombineThreads, 0, st>>>(o_part, lse_part, ws, ol, lse, B, Lq,
+                                                                            H, G, slots);
   return cudaGetLastError();
 }
 template <int DG>
