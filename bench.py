@@ -65,6 +65,12 @@ WORKLOAD_TEXT = {
 }
 
 
+def rotation_copies(nbytes):
+    """Copies of an input of nbytes that a timed loop rotates through so
+    that no step finds it in L2: at least 2.2x the L2 in all."""
+    return max(1, math.ceil(2.2 * L2_BYTES / nbytes))
+
+
 def workload_text(args):
     text = WORKLOAD_TEXT[args.workload]
     return text + ", FP8 E4M3 cache" if getattr(args, "kv", "bf16") == "fp8" else text
@@ -611,12 +617,12 @@ def main():
     B, Lq, H, G = d["B"], d["Lq"], d["H"], d["G"]
     t = {k: v.to(dev) for k, v in case.tensors().items()}
     cache_bytes = t["cache"].numel() * t["cache"].element_size()
-    copies = max(1, math.ceil(2.2 * L2_BYTES / cache_bytes))
+    copies = rotation_copies(cache_bytes)
     caches = [t["cache"]] + [t["cache"].clone() for _ in range(copies - 1)]
     # the weights rotate too, so that no step finds its W_UK and W_UV in L2
     # (a model with many layers reads each layer's weights from HBM)
     w_bytes = sum(t[k].numel() * t[k].element_size() for k in ("W_UK", "W_UV"))
-    wcopies = max(1, math.ceil(2.2 * L2_BYTES / w_bytes))
+    wcopies = rotation_copies(w_bytes)
     weights = [(t["W_UK"], t["W_UV"])] + [(t["W_UK"].clone(), t["W_UV"].clone()) for _ in range(wcopies - 1)]
     nrot = max(copies, wcopies)  # step graphs: step c uses cache copy c % copies, weights c % wcopies
     bufs = mla.DecodeBuffers(d, dev)

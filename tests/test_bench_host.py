@@ -75,3 +75,16 @@ def test_reference_arm_runs_on_rank_zero_only():
     class Args:
         workload, steps, warmup = "dsv3", 1, 0
     assert bench.run_reference(Args(), 2, 1) is None  # returns before any work
+
+
+def test_rotation_copies_exceed_l2():
+    """The timed loops rotate copies of the cache and of the weights that
+    hold more than twice the L2 in all, so no step finds its inputs there:
+    the dsv3 cache (75.5 MB) in 4 copies, the one-group weights (33.6 MB)
+    in 9, the two-group weights (16.8 MB) in 18, a cache larger than L2
+    in one."""
+    for nbytes, want in ((16 * 4096 * 1152, 4), (2 * 128 * 128 * 512 * 2, 9), (2 * 128 * 128 * 256 * 2, 18),
+                         (900 * 2 ** 20, 1)):
+        n = bench.rotation_copies(nbytes)
+        assert n == want, (nbytes, n)
+        assert n * nbytes >= 2.2 * bench.L2_BYTES or n == 1 and nbytes >= 2.2 * bench.L2_BYTES
